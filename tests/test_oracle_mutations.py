@@ -1,0 +1,113 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one slip in a private copy of the oracle's C source (on the
+CPU, in a temporary directory), builds it, and runs the pin suite
+(tests/test_oracle_pins.py) against that copy.  The pins must fail for every
+planted slip.
+"""
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SOURCE = os.path.join(ROOT, "oracle", "cc_oracle.c")
+
+MUTATIONS = {
+    "drop first-moment bias correction":
+        ("const float m_hat = m_new / bias_corr1;", "const float m_hat = m_new;"),
+    "drop second-moment bias correction":
+        ("const float v_hat = v_new / bias_corr2;", "const float v_hat = v_new;"),
+    "eps inside the square root":
+        ("const float denom = sqrtf(v_hat) + eps;",
+         "const float denom = sqrtf(v_hat + eps);"),
+    "update sign flipped":
+        ("const float p_new = p_decayed - update;",
+         "const float p_new = p_decayed + update;"),
+    "weight decay dropped":
+        ("const float p_decayed = master[i] * decay;",
+         "const float p_decayed = master[i];"),
+    "decay not scaled by lr":
+        ("const float lr_wd = lr * weight_decay;",
+         "const float lr_wd = weight_decay;"),
+    "replica 0 skipped":
+        ("s = oracle_bf16_widen(grads[0][i]);\n            for (int r = 1;",
+         "s = 0.0f;\n            for (int r = 1;"),
+    "last replica dropped":
+        ("for (int r = 1; r < R; ++r) s = s + oracle_bf16_widen(grads[r][i]);",
+         "for (int r = 1; r < R - 1; ++r) s = s + oracle_bf16_widen(grads[r][i]);"),
+    "loss scale multiplied in":
+        ("const float inv_scale = 1.0f / grad_scale;",
+         "const float inv_scale = grad_scale;"),
+    "betas swapped in the first moment":
+        ("const float m_decayed = beta1 * m[i];",
+         "const float m_decayed = beta2 * m[i];"),
+    "second moment of g, not g*g":
+        ("const float v_in = one_minus_b2 * g_sq;",
+         "const float v_in = one_minus_b2 * g;"),
+    "bias correction off by one step":
+        ("pow((double)beta1, (double)step)", "pow((double)beta1, (double)(step + 1))"),
+    "lr dropped from the update":
+        ("const float update = lr * ratio;", "const float update = ratio * 1e-3f;"),
+    "bf16 cast truncates":
+        ("return (uint16_t)((u + 0x7FFFu + lsb) >> 16);",
+         "return (uint16_t)(u >> 16);"),
+    "bf16 ties away from zero":
+        ("return (uint16_t)((u + 0x7FFFu + lsb) >> 16);",
+         "return (uint16_t)((u + 0x8000u) >> 16);"),
+    "accumulator never restarted":
+        ("            if (first)\n                acc[r][i] = g;",
+         "            if (0)\n                acc[r][i] = g;"),
+    "accumulator ignored for r > 0":
+        ("float local = acc[r][i] + oracle_bf16_widen(grads[r][i]);",
+         "float local = oracle_bf16_widen(grads[r][i]);"),
+    "only replica 0 receives parameters":
+        ("for (int r = 0; r < R; ++r) params_out[r][i] = b;",
+         "params_out[0][i] = b; for (int r = 1; r < R; ++r) params_out[r][i] = 0;"),
+}
+
+
+def _run_pins_on(mutated_source: str) -> subprocess.CompletedProcess:
+    work = tempfile.mkdtemp(prefix="oracle_mutant_")
+    try:
+        ign = shutil.ignore_patterns("*.so", "__pycache__", "_build")
+        shutil.copytree(os.path.join(ROOT, "oracle"), os.path.join(work, "oracle"),
+                        ignore=ign)
+        with open(os.path.join(work, "oracle", "cc_oracle.c"), "w") as f:
+            f.write(mutated_source)
+        shutil.copytree(os.path.join(ROOT, "tests"), os.path.join(work, "tests"),
+                        ignore=ign)
+        pkg = "gradient_reduce_optimizer_gb300"
+        os.makedirs(os.path.join(work, pkg))
+        for name in ("__init__.py", "workloads.py"):
+            shutil.copy(os.path.join(ROOT, pkg, name), os.path.join(work, pkg))
+        shutil.copy(os.path.join(ROOT, "pytest.ini"), work)
+        return subprocess.run(
+            [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:warnings",
+             "tests/test_oracle_pins.py"],
+            cwd=work, capture_output=True, text=True, timeout=300)
+    finally:
+        shutil.rmtree(work, ignore_errors=True)
+
+
+def test_every_planted_slip_fails_a_pin():
+    src = open(SOURCE).read()
+    for name, (old, _) in MUTATIONS.items():
+        assert src.count(old) == 1, f"mutation site not unique: {name}"
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        results = dict(zip(MUTATIONS, ex.map(
+            lambda kv: _run_pins_on(src.replace(*kv)), MUTATIONS.values())))
+    survivors = [n for n, r in results.items() if r.returncode == 0]
+    assert not survivors, f"pins missed: {survivors}"
+    broken = [n for n, r in results.items()
+              if r.returncode != 1 or "failed" not in r.stdout]
+    assert not broken, f"mutant did not build/run cleanly: {broken}"
+
+
+def test_unmutated_copy_passes():
+    r = _run_pins_on(open(SOURCE).read())
+    assert r.returncode == 0, r.stdout[-2000:]
