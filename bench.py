@@ -1,0 +1,519 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused data-parallel step on GB300.
+
+One step = the whole hot path on the BERT-large parameter list (336,226,108
+parameters, 398 tensors) with R = 8 emulated replicas: the slab laid out in
+reverse layer order by the bucket planner, then the fused reduce + AdamW +
+redistribute kernel launched bucket by bucket (25 MiB buckets) through the
+C ABI.  Printed as one JSON line (rank 0):
+
+  value      parameters per second, device-timed (CUDA events, inputs
+             resident in HBM, inputs 14.8 GB >> 129 MB L2 so no flush)
+  e2e        the same step through the C ABI with the gradients copied in
+             from pinned host memory and the updated bf16 parameters copied
+             back every step
+  roofline   achieved HBM GB/s of the fused kernel (algorithmic bytes
+             (4R + 24) per parameter) against the measured copy bandwidth
+  overlap    the step-time decomposition of the bucketed step behind a
+             proxy backward of bf16 GEMMs: T_bwd, T_comm, overlapped and
+             sequential step times, exposed ms
+  cpu_baseline  the oracle (single-threaded C) on a bounded sample
+
+`--impl reference` times the oracle alone on the host cores (the reference
+arm).  Under torchrun (N > 1) every rank runs its own independent step on
+its own GPU (replicas only: the emulated R-replica step has no exchange
+between GPUs); the JSON reports the total over ranks against the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused DP step params/s and HBM GB/s (% of ~8 TB/s) at R=8; exposed ms/step"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCE = os.path.join(ROOT, "gradient_reduce_optimizer_gb300", "csrc",
+                             "cc_dp_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_step_kernel_traffic.json")
+
+
+# ---------------------------------------------------------------------------
+# Process group (replicas only) and cross-rank reductions
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_scalar(x: float, world: int, op: str, device="cpu") -> float:
+    """Max or sum of a float over ranks (identity for one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(ms_per_step: float, units_per_step: float, world: int,
+              device="cpu"):
+    """Whole-job throughput: units of all ranks over the slowest rank."""
+    slowest = reduce_scalar(ms_per_step, world, "max", device)
+    total_units = reduce_scalar(units_per_step, world, "sum", device)
+    return slowest, total_units / (slowest * 1e-3)
+
+
+# ---------------------------------------------------------------------------
+# Peaks, profile figures and clocks
+# ---------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic_per_param(R: int):
+    """DRAM bytes per parameter of the fused kernel from the committed ncu
+    summary, if it was taken on the current kernel source and this R."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_sha") != kernel_sha() or int(d.get("R", -1)) != R:
+        return None
+    return float(d["dram_bytes"]) / float(d["elements"])
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]),
+                                 power=float(parts[3]), hw=parts[5], hwt=parts[6],
+                                 swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 250.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------
+# Workload
+# ---------------------------------------------------------------------------
+
+def build_workload(device, R_override=None, bucket_mib=25):
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+
+    w = wl.bert_large_r8(bucket_bytes=bucket_mib * wl.MiB)
+    if R_override:
+        w.R = R_override
+    numel, layer_of = w.numel(), w.layer_of()
+    offsets, buckets, n_slab = capi.cc_plan_buckets(numel, w.bucket_bytes)
+    lay = wl.element_layer_map(numel, layer_of, offsets, n_slab, device=device)
+    per_layer = wl.layer_scales(max(layer_of) + 1, *w.layer_scale, device=device)
+    scale = per_layer[lay.clamp(min=0).long()]
+    grads = wl.make_grads(w.R, n_slab, w.grad_sigma, device=device,
+                          elem_scale=scale, mask=lay >= 0)
+    del lay, scale
+    master, m, v = wl.make_state(n_slab, w.step, w.grad_sigma, device=device)
+    outs = [torch.empty(n_slab, dtype=torch.bfloat16, device=device)
+            for _ in range(w.R)]
+    torch.cuda.synchronize()
+    return dict(w=w, numel=numel, layer_of=layer_of, offsets=offsets,
+                buckets=buckets, n_slab=n_slab, grads=grads, master=master,
+                m=m, v=v, outs=outs)
+
+
+def step_args(wk, step):
+    w = wk["w"]
+    return dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps,
+                weight_decay=w.weight_decay, step=step, grad_scale=w.grad_scale)
+
+
+def launches_per_step(n_slab, bucket_bytes):
+    per = max(8, bucket_bytes // 16 * 8) if bucket_bytes else n_slab
+    return (n_slab + per - 1) // per
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_inputs(R, sample, seed_offset=0):
+    """The first `sample` slab elements of the BERT-large R-replica workload,
+    generated on the host with the same recipe (layer scales, padding)."""
+    import numpy as np
+    import torch
+    import oracle
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+
+    w = wl.bert_large_r8()
+    numel, layer_of = w.numel(), w.layer_of()
+    offsets, _, n_slab = oracle.plan_buckets(numel, w.bucket_bytes)
+    sample = min(sample, n_slab)
+    lay = torch.full((sample,), -1, dtype=torch.int32)
+    for t, (k, l) in enumerate(zip(numel, layer_of)):
+        lo, hi = offsets[t], min(offsets[t] + k, sample)
+        if lo < sample:
+            lay[lo:hi] = l
+    per_layer = wl.layer_scales(max(layer_of) + 1, *w.layer_scale)
+    scale = per_layer[lay.clamp(min=0).long()]
+    grads = wl.make_grads(R, sample, w.grad_sigma, elem_scale=scale, mask=lay >= 0)
+    master, m, v = wl.make_state(sample, w.step, w.grad_sigma)
+    g16 = [g.view(torch.int16).numpy().view(np.uint16).copy() for g in grads]
+    st = [x.numpy().copy() for x in (master, m, v)]
+    hp = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps,
+              weight_decay=w.weight_decay, step=w.step, grad_scale=w.grad_scale)
+    return g16, st, hp, sample
+
+
+def time_oracle(R, sample, min_seconds, max_seconds):
+    import oracle
+    g16, st, hp, sample = oracle_sample_inputs(R, sample)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.fused_dp_step(g16, *st, **hp)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or el >= max_seconds:
+            break
+    return sample * passes / el, sample, passes, el
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    from gradient_reduce_optimizer_gb300 import build as gbuild
+    from gradient_reduce_optimizer_gb300 import capi
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    gbuild.build()
+    capi.lib()
+
+    wk = build_workload(dev, bucket_mib=args.bucket_mib)
+    w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
+    n_params = w.n
+    bb = w.bucket_bytes
+    stream = torch.cuda.current_stream()
+
+    def one_step(step):
+        capi.cc_fused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"],
+                              wk["outs"], n_slab, R, bb, stream=stream,
+                              **step_args(wk, step))
+
+    for i in range(args.warmup):
+        one_step(w.step + i)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        one_step(w.step + args.warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_local = ev0.elapsed_time(ev1) / args.steps
+    ms, value = aggregate(ms_local, float(n_params), world, device=dev)
+
+    bytes_per_param = 4 * R + 24
+    launches = launches_per_step(n_slab, bb)
+    per_launch_elems = n_slab / launches
+    launch_ms = ms_local / launches           # launches run back to back
+    achieved = bytes_per_param * per_launch_elems / (launch_ms * 1e-3) / 1e9
+    peak, peak_src = measured_hbm_peak()
+    tpp = profiled_traffic_per_param(R)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": (round(tpp * per_launch_elems) if tpp else None),
+                "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": round(bytes_per_param * per_launch_elems),
+                "kernel": f"fused_step_kernel<R={R}>",
+                "launches_per_step": launches}
+
+    result = {
+        "metric": METRIC, "value": round(value), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": (f"BERT-large parameter list (336,226,108 params, 398 tensors), "
+                         f"R={R} emulated replicas, {args.bucket_mib} MiB buckets in "
+                         "reverse layer order, AdamW wd=0.01 step>=10, bf16 grads "
+                         "N(0,1e-3) x U(0.5,2) per layer"),
+            "R": R, "n_params": n_params, "n_slab": n_slab,
+            "bucket_bytes": bb, "launches_per_step": launches,
+            "parallelism": f"replicas x{world} (R={R} emulated per GPU)",
+            "l2": "inputs 14.8 GB per GPU, larger than the 129 MB L2: no flush",
+        },
+        "hbm_gbs": round(bytes_per_param * n_slab / (ms * 1e-3) / 1e9, 1),
+        "hbm_pct_of_8tbs": round(100 * bytes_per_param * n_slab / (ms * 1e-3) / 8e12, 2),
+        "roofline": roofline,
+        "clocks": clk,
+        "gpu_launches": launches * args.steps,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, wk, stream, world, dev)
+    if not args.no_overlap:
+        result["overlap"] = run_overlap(args, wk, dev, [args.bucket_mib])
+        if args.sweep:
+            result["overlap_sweep"] = run_overlap(args, wk, dev, [1, 4, 25, 100, 500])
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, passes, el = time_oracle(R, args.cpu_sample, 10.0, 30.0)
+        result["cpu_baseline"] = {
+            "value": round(v), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"first {sample:,} slab elements of the same workload (R={R}), "
+                       f"{passes} passes in {el:.1f} s, single-threaded C oracle")}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return result
+
+
+def run_e2e(args, wk, stream, world, dev):
+    """The step through the C ABI with host buffers: every step copies the R
+    gradient slabs in from pinned host memory and the updated bf16
+    parameters (one replica; the others are bit-identical) back out."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
+    host_grads = [g.cpu().pin_memory() for g in wk["grads"]]
+    host_out = torch.empty(n_slab, dtype=torch.bfloat16).pin_memory()
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def e2e_step(step):
+        for h, d in zip(host_grads, wk["grads"]):
+            d.copy_(h, non_blocking=True)
+        capi.cc_fused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"],
+                              wk["outs"], n_slab, R, w.bucket_bytes,
+                              stream=stream, **step_args(wk, step))
+        host_out.copy_(wk["outs"][0], non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(w.step + i)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        e2e_step(w.step + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_local = ev0.elapsed_time(ev1) / steps
+    ms, value = aggregate(ms_local, float(w.n), world, device=dev)
+    return {"value": round(value), "unit": UNIT,
+            "h2d_bytes_per_step": 2 * R * n_slab, "d2h_bytes_per_step": 2 * n_slab,
+            "ms_per_step": round(ms, 3), "steps": steps}
+
+
+def run_overlap(args, wk, dev, mibs):
+    """Exposed time of the bucketed step behind a proxy backward of 24 layers
+    x 3 bf16 GEMMs (M=8192, N=K=1024); buckets planned at each size."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    w = wk["w"]
+    M, N, K = 8192, 1024, 1024
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    A = torch.randn(M * K, generator=g, device=dev).to(torch.bfloat16)
+    B = torch.randn(K * N, generator=g, device=dev).to(torch.bfloat16)
+    C = torch.empty(M * N, dtype=torch.bfloat16, device=dev)
+    out = []
+    for mib in mibs:
+        offsets, buckets, n_slab = capi.cc_plan_buckets(wk["numel"], mib << 20)
+        assert n_slab == wk["n_slab"] and offsets == wk["offsets"]
+        ready = capi.cc_bucket_ready_layers(wk["numel"], wk["layer_of"], offsets, buckets)
+        r = capi.cc_overlap_bench(
+            grads=wk["grads"], master=wk["master"], m=wk["m"], v=wk["v"],
+            params_out=wk["outs"], n=n_slab, R=w.R, buckets=buckets,
+            ready_layers=ready, num_layers=24, gemms_per_layer=3, gemm_m=M,
+            gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
+            warmup=args.warmup, iters=args.overlap_iters,
+            max_ctas=args.overlap_ctas, side_priority_high=args.side_priority,
+            **step_args(wk, w.step))
+        r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
+        r["bucket_mib"] = mib
+        r["exposed_pct_of_bwd"] = round(100 * r["exposed_ms"] / r["t_bwd_ms"], 1)
+        r["bwd_tflops"] = round(24 * 3 * 2 * M * N * K / (r["t_bwd_ms"] * 1e-3) / 1e12, 1)
+        out.append(r)
+    return out[0] if len(out) == 1 else out
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if world > 1:
+        dist_init(world, "gloo")
+    if rank != 0:
+        barrier(world)
+        return None
+    from oracle import build as obuild
+    obuild.build()
+    import oracle
+    R = 8
+    g16, st, hp, sample = oracle_sample_inputs(R, args.ref_sample)
+    for _ in range(args.warmup):
+        oracle.fused_dp_step(g16, *st, **hp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fused_dp_step(g16, *st, **hp)
+    el = time.perf_counter() - t0
+    value = sample * args.steps / el
+    desc = (f"first {sample:,} slab elements of the BERT-large R=8 workload per "
+            "step, single-threaded C oracle")
+    result = {
+        "metric": METRIC, "value": round(value), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": "BERT-large parameter list, R=8, 25 MiB buckets "
+                   "(bounded sample per step)", "R": R, "sample_elements": sample},
+        "cpu_baseline": {"value": round(value), "unit": UNIT, "cores": 1,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+    barrier(world)
+    return result
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--bucket-mib", type=int, default=25)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-overlap", action="store_true")
+    p.add_argument("--overlap-iters", type=int, default=20)
+    p.add_argument("--overlap-ctas", type=int, default=0)
+    p.add_argument("--side-priority", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="also run the 1/4/25/100/500 MiB bucket sweep")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=1 << 22)
+    p.add_argument("--ref-sample", type=int, default=1 << 20)
+    a = p.parse_args(argv)
+    a.warmup = max(3, a.warmup)     # at least 3 untimed warm-up steps
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    _, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,264 @@
+"""Python binding of the C ABI in include/cc_dp.h (argument marshalling only).
+
+Every function has the name of the C entry point it calls.  Pointer
+arguments accept ``torch.Tensor`` (their ``data_ptr()``) or plain integers;
+``stream`` accepts a ``torch.cuda.Stream``, a raw ``cudaStream_t`` integer,
+or ``None`` for torch's current stream.  A non-OK status raises
+:class:`CCError` carrying the status and the library's one-line reason.
+
+There is no fallback: if ``libcc_dp.so`` has not been built, every call
+raises.  Build it with ``python -c "import __graft_entry__ as g; g.build()"``
+or ``python gradient_reduce_optimizer_gb300/build.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence, Tuple
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(PKG, "libcc_dp.so")
+
+CC_MAX_R = 16
+CC_PAD_ELEMS = 8
+CC_OK = 0
+CC_ERR_INVALID = -1
+CC_ERR_ALIAS = -2
+CC_ERR_MISALIGNED = -3
+CC_ERR_CUDA = -4
+CC_ERR_UNSUPPORTED = -5
+CC_ERR_CAPACITY = -6
+
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_f = ctypes.c_float
+_i = ctypes.c_int
+
+
+class CCError(RuntimeError):
+    def __init__(self, status: int, func: str, reason: str):
+        self.status = status
+        self.func = func
+        self.reason = reason
+        super().__init__(f"{func}: {status_name(status)}: {reason}")
+
+
+class cc_overlap_cfg(ctypes.Structure):
+    _fields_ = [
+        ("grads", _vp), ("acc", _vp), ("master", _vp), ("m", _vp), ("v", _vp),
+        ("params_out", _vp), ("n", _sz), ("R", _i),
+        ("bucket_begin", _vp), ("bucket_end", _vp),
+        ("bucket_ready_layer", _vp), ("num_buckets", _i),
+        ("lr", _f), ("beta1", _f), ("beta2", _f), ("eps", _f),
+        ("weight_decay", _f), ("step", _i), ("grad_scale", _f),
+        ("num_layers", _i), ("gemms_per_layer", _i),
+        ("gemm_m", _i), ("gemm_n", _i), ("gemm_k", _i),
+        ("gemm_a", _vp), ("gemm_b", _vp), ("gemm_c", _vp),
+        ("warmup", _i), ("iters", _i), ("max_ctas", _i),
+        ("side_priority_high", _i),
+    ]
+
+
+class cc_overlap_result(ctypes.Structure):
+    _fields_ = [
+        ("t_bwd_ms", _f), ("t_comm_ms", _f), ("t_step_overlap_ms", _f),
+        ("t_step_seq_ms", _f), ("exposed_ms", _f), ("exposed_bound_ms", _f),
+        ("num_buckets", _i),
+    ]
+
+
+_SIGNATURES = {
+    "cc_status_string": ([_i], ctypes.c_char_p),
+    "cc_last_error": ([], ctypes.c_char_p),
+    "cc_fused_dp_step": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _f, _f, _f,
+                          _f, _f, _i, _f, _i, _vp], _i),
+    "cc_accumulate_local": ([_vp, _vp, _sz, _i, _i, _vp], _i),
+    "cc_fused_dp_step_accum": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _sz,
+                                _f, _f, _f, _f, _f, _i, _f, _i, _vp], _i),
+    "cc_fused_dp_bucket": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _sz,
+                            _f, _f, _f, _f, _f, _i, _f, _i, _vp], _i),
+    "cc_plan_buckets": ([_vp, _i, _sz, _vp, _vp, _vp, _i, _vp, _vp], _i),
+    "cc_bucket_ready_layers": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _vp], _i),
+    "cc_overlap_bench": ([ctypes.POINTER(cc_overlap_cfg),
+                          ctypes.POINTER(cc_overlap_result)], _i),
+    "cc_l2_flush": ([_vp, _sz, _vp], _i),
+}
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(
+                f"{LIBRARY} is missing: the CUDA library must be built "
+                "(python gradient_reduce_optimizer_gb300/build.py); "
+                "there is no fallback path")
+        L = ctypes.CDLL(LIBRARY)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = L
+    return _LIB
+
+
+def status_name(status: int) -> str:
+    return lib().cc_status_string(status).decode()
+
+
+def cc_status_string(status: int) -> str:
+    return status_name(status)
+
+
+def cc_last_error() -> str:
+    return lib().cc_last_error().decode()
+
+
+def _check(status: int, func: str) -> None:
+    if status != CC_OK:
+        raise CCError(status, func, cc_last_error())
+
+
+def _addr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _addr_array(xs) -> Optional[ctypes.Array]:
+    if xs is None:
+        return None
+    return (_vp * max(1, len(xs)))(*[_addr(x) for x in xs])
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def cc_fused_dp_step(grads, master, m, v, params_out, n: int, R: int,
+                     bucket_bytes: int, lr: float, beta1: float, beta2: float,
+                     eps: float, weight_decay: float, step: int,
+                     grad_scale: float, accum_k: int = 1, stream=None) -> None:
+    _check(lib().cc_fused_dp_step(
+        _addr_array(grads), _addr(master), _addr(m), _addr(v),
+        _addr_array(params_out), n, R, bucket_bytes, lr, beta1, beta2, eps,
+        weight_decay, step, grad_scale, accum_k, _stream(stream)),
+        "cc_fused_dp_step")
+
+
+def cc_fused_dp_step_accum(grads, acc, master, m, v, params_out, n: int,
+                           R: int, bucket_bytes: int, lr: float, beta1: float,
+                           beta2: float, eps: float, weight_decay: float,
+                           step: int, grad_scale: float, accum_k: int,
+                           stream=None) -> None:
+    _check(lib().cc_fused_dp_step_accum(
+        _addr_array(grads), _addr_array(acc), _addr(master), _addr(m),
+        _addr(v), _addr_array(params_out), n, R, bucket_bytes, lr, beta1,
+        beta2, eps, weight_decay, step, grad_scale, accum_k, _stream(stream)),
+        "cc_fused_dp_step_accum")
+
+
+def cc_fused_dp_bucket(grads, acc, master, m, v, params_out, n: int, R: int,
+                       begin: int, end: int, lr: float, beta1: float,
+                       beta2: float, eps: float, weight_decay: float,
+                       step: int, grad_scale: float, max_ctas: int = 0,
+                       stream=None) -> None:
+    _check(lib().cc_fused_dp_bucket(
+        _addr_array(grads), _addr_array(acc), _addr(master), _addr(m),
+        _addr(v), _addr_array(params_out), n, R, begin, end, lr, beta1, beta2,
+        eps, weight_decay, step, grad_scale, max_ctas, _stream(stream)),
+        "cc_fused_dp_bucket")
+
+
+def cc_accumulate_local(grads, acc, n: int, R: int, first: bool,
+                        stream=None) -> None:
+    _check(lib().cc_accumulate_local(_addr_array(grads), _addr_array(acc), n,
+                                     R, int(bool(first)), _stream(stream)),
+           "cc_accumulate_local")
+
+
+def cc_plan_buckets(numel: Sequence[int], bucket_bytes: int
+                    ) -> Tuple[List[int], List[Tuple[int, int]], int]:
+    """Returns (offsets, [(begin, end), ...], n_padded)."""
+    T = len(numel)
+    c_numel = (_sz * T)(*numel)
+    offsets = (_sz * T)()
+    count = _i(0)
+    n_pad = _sz(0)
+    L = lib()
+    st = L.cc_plan_buckets(c_numel, T, bucket_bytes, offsets, None, None, 0,
+                           ctypes.byref(count), ctypes.byref(n_pad))
+    if st not in (CC_OK, CC_ERR_CAPACITY):
+        _check(st, "cc_plan_buckets")
+    cap = count.value
+    b = (_sz * max(1, cap))()
+    e = (_sz * max(1, cap))()
+    _check(L.cc_plan_buckets(c_numel, T, bucket_bytes, offsets, b, e, cap,
+                             ctypes.byref(count), ctypes.byref(n_pad)),
+           "cc_plan_buckets")
+    return (list(offsets), [(b[i], e[i]) for i in range(count.value)],
+            n_pad.value)
+
+
+def cc_bucket_ready_layers(numel: Sequence[int], layer_of: Sequence[int],
+                           offsets: Sequence[int],
+                           buckets: Sequence[Tuple[int, int]]) -> List[int]:
+    T, B = len(numel), len(buckets)
+    out = (_i * max(1, B))()
+    _check(lib().cc_bucket_ready_layers(
+        (_sz * T)(*numel), (_i * T)(*layer_of), (_sz * T)(*offsets), T,
+        (_sz * max(1, B))(*[b for b, _ in buckets]),
+        (_sz * max(1, B))(*[e for _, e in buckets]), B, out),
+        "cc_bucket_ready_layers")
+    return list(out)[:B]
+
+
+def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
+                     buckets: Sequence[Tuple[int, int]],
+                     ready_layers: Sequence[int], lr: float, beta1: float,
+                     beta2: float, eps: float, weight_decay: float, step: int,
+                     grad_scale: float, num_layers: int, gemms_per_layer: int,
+                     gemm_m: int, gemm_n: int, gemm_k: int, gemm_a, gemm_b,
+                     gemm_c, warmup: int = 3, iters: int = 20,
+                     max_ctas: int = 0, side_priority_high: bool = False,
+                     acc=None) -> Dict[str, float]:
+    B = len(buckets)
+    keep = dict(
+        g=_addr_array(grads), o=_addr_array(params_out),
+        a=_addr_array(acc) if acc is not None else None,
+        bb=(_sz * B)(*[b for b, _ in buckets]),
+        be=(_sz * B)(*[e for _, e in buckets]),
+        rl=(_i * B)(*ready_layers))
+    cfg = cc_overlap_cfg(
+        grads=ctypes.cast(keep["g"], _vp),
+        acc=ctypes.cast(keep["a"], _vp) if keep["a"] is not None else None,
+        master=_addr(master), m=_addr(m), v=_addr(v),
+        params_out=ctypes.cast(keep["o"], _vp), n=n, R=R,
+        bucket_begin=ctypes.cast(keep["bb"], _vp),
+        bucket_end=ctypes.cast(keep["be"], _vp),
+        bucket_ready_layer=ctypes.cast(keep["rl"], _vp), num_buckets=B,
+        lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay,
+        step=step, grad_scale=grad_scale, num_layers=num_layers,
+        gemms_per_layer=gemms_per_layer, gemm_m=gemm_m, gemm_n=gemm_n,
+        gemm_k=gemm_k, gemm_a=_addr(gemm_a), gemm_b=_addr(gemm_b),
+        gemm_c=_addr(gemm_c), warmup=warmup, iters=iters, max_ctas=max_ctas,
+        side_priority_high=int(bool(side_priority_high)))
+    res = cc_overlap_result()
+    _check(lib().cc_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
+           "cc_overlap_bench")
+    return {name: getattr(res, name) for name, _ in res._fields_}
+
+
+def cc_l2_flush(buf, nbytes: int, stream=None) -> None:
+    _check(lib().cc_l2_flush(_addr(buf), nbytes, _stream(stream)),
+           "cc_l2_flush")

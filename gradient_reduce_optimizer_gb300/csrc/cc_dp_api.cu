@@ -1,0 +1,411 @@
+// C ABI of the fused data-parallel step (include/cc_dp.h): argument
+// validation, the host-side AdamW scalars, the bucket planner and the
+// per-bucket launch loop.  Every step of the arithmetic runs in the kernels
+// of cc_dp_kernels.cu; this file only checks, plans and launches.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "cc_dp_internal.h"
+
+namespace ccdp {
+
+namespace {
+thread_local char g_last_error[512] = "";
+}
+
+const char *last_error() { return g_last_error; }
+
+int fail(int status, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int fail_cuda(cudaError_t e, const char *what) {
+    return fail(CC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+}
+
+namespace {
+
+bool finite(float x) { return std::isfinite(x); }
+
+using MemGetAddressRangeFn = CUresult (*)(CUdeviceptr *, size_t *, CUdeviceptr);
+
+MemGetAddressRangeFn address_range_fn() {
+    static MemGetAddressRangeFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<MemGetAddressRangeFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+int check_device_range(const void *ptr, size_t bytes, const char *name) {
+    MemGetAddressRangeFn fn = address_range_fn();
+    if (!fn) return fail(CC_ERR_UNSUPPORTED, "cuMemGetAddressRange unavailable");
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    const CUresult r = fn(&base, &size, reinterpret_cast<CUdeviceptr>(ptr));
+    if (r != CUDA_SUCCESS)
+        return fail(CC_ERR_INVALID, "%s=%p is not in a device allocation (CUresult %d)",
+                    name, ptr, static_cast<int>(r));
+    const uintptr_t p = reinterpret_cast<uintptr_t>(ptr);
+    if (p - base > size || bytes > size - (p - base))
+        return fail(CC_ERR_INVALID,
+                    "%s: %zu bytes at %p run past the end of its allocation "
+                    "(%zu bytes at %p)", name, bytes, ptr, size,
+                    reinterpret_cast<void *>(base));
+    return CC_OK;
+}
+
+int ensure_device() {
+    int major = 0, minor = 0;
+    const cudaError_t e = check_device(&major, &minor);
+    if (e != cudaSuccess) {
+        if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver)
+            return fail(CC_ERR_UNSUPPORTED, "no usable CUDA device: %s",
+                        cudaGetErrorString(e));
+        return fail_cuda(e, "device query");
+    }
+    if (major != 10 || minor != 3)
+        return fail(CC_ERR_UNSUPPORTED,
+                    "built for sm_103a (GB300); device is sm_%d%d", major, minor);
+    return CC_OK;
+}
+
+int make_scalars(float lr, float beta1, float beta2, float eps,
+                 float weight_decay, int step, float grad_scale,
+                 AdamScalars *c) {
+    if (!finite(lr) || lr < 0.0f) return fail(CC_ERR_INVALID, "lr=%g must be finite and >= 0", lr);
+    if (!finite(beta1) || beta1 < 0.0f || beta1 >= 1.0f)
+        return fail(CC_ERR_INVALID, "beta1=%g must be in [0, 1)", beta1);
+    if (!finite(beta2) || beta2 < 0.0f || beta2 >= 1.0f)
+        return fail(CC_ERR_INVALID, "beta2=%g must be in [0, 1)", beta2);
+    if (!finite(eps) || eps < 0.0f) return fail(CC_ERR_INVALID, "eps=%g must be finite and >= 0", eps);
+    if (!finite(weight_decay) || weight_decay < 0.0f)
+        return fail(CC_ERR_INVALID, "weight_decay=%g must be finite and >= 0", weight_decay);
+    if (step < 1) return fail(CC_ERR_INVALID, "step=%d must be >= 1", step);
+    if (!finite(grad_scale) || grad_scale <= 0.0f)
+        return fail(CC_ERR_INVALID, "grad_scale=%g must be finite and > 0", grad_scale);
+
+    // Each scalar is one binary32 rounding of its definition (this file is
+    // built with -ffp-contract=off, so nothing here fuses).
+    c->beta1 = beta1;
+    c->beta2 = beta2;
+    c->one_minus_b1 = 1.0f - beta1;
+    c->one_minus_b2 = 1.0f - beta2;
+    const double t = static_cast<double>(step);
+    c->bias_corr1 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta1), t));
+    c->bias_corr2 = static_cast<float>(1.0 - std::pow(static_cast<double>(beta2), t));
+    c->lr = lr;
+    c->eps = eps;
+    const float lr_wd = lr * weight_decay;
+    c->decay = 1.0f - lr_wd;
+    c->inv_scale = 1.0f / grad_scale;
+    if (!(c->bias_corr1 > 0.0f) || !(c->bias_corr2 > 0.0f))
+        return fail(CC_ERR_INVALID, "bias correction underflows (beta too close to 1)");
+    if (!finite(c->inv_scale))
+        return fail(CC_ERR_INVALID, "1/grad_scale overflows (grad_scale=%g)", grad_scale);
+    return CC_OK;
+}
+
+namespace {
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+    bool written;
+    const char *name;
+    int index;
+};
+
+bool overlap(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+}  // namespace
+
+int validate_slabs(const void *const *grads, const float *const *acc,
+                   float *master, float *m, float *v, void *const *params_out,
+                   size_t n, int R, bool need_acc, Slabs *s) {
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    if (!grads || !params_out) return fail(CC_ERR_INVALID, "grads/params_out arrays are NULL");
+    if (need_acc && !acc) return fail(CC_ERR_INVALID, "acc array is NULL");
+    if (!master || !m || !v) return fail(CC_ERR_INVALID, "master/m/v is NULL");
+    if (n > (SIZE_MAX / 8)) return fail(CC_ERR_INVALID, "n=%zu too large", n);
+    s->R = R;
+    s->master = master;
+    s->m = m;
+    s->v = v;
+    std::vector<Range> ranges;
+    ranges.reserve(3 * CC_MAX_R + 3);
+    auto add = [&](const void *p, size_t bytes, bool written, const char *name,
+                   int idx) -> int {
+        if (!p) return fail(CC_ERR_INVALID, "%s[%d] is NULL", name, idx);
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+            return fail(CC_ERR_MISALIGNED, "%s[%d]=%p is not 16-byte aligned", name, idx, p);
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        ranges.push_back({lo, lo + bytes, written, name, idx});
+        return CC_OK;
+    };
+    int st;
+    for (int r = 0; r < R; ++r) {
+        s->grads[r] = grads[r];
+        s->out[r] = params_out[r];
+        s->acc[r] = need_acc ? acc[r] : nullptr;
+        if ((st = add(grads[r], 2 * n, false, "grads", r)) != CC_OK) return st;
+        if ((st = add(params_out[r], 2 * n, true, "params_out", r)) != CC_OK) return st;
+        if (need_acc && (st = add(acc[r], 4 * n, false, "acc", r)) != CC_OK) return st;
+    }
+    for (int r = R; r < CC_MAX_R; ++r) {
+        s->grads[r] = nullptr;
+        s->out[r] = nullptr;
+        s->acc[r] = nullptr;
+    }
+    if ((st = add(master, 4 * n, true, "master", 0)) != CC_OK) return st;
+    if ((st = add(m, 4 * n, true, "m", 0)) != CC_OK) return st;
+    if ((st = add(v, 4 * n, true, "v", 0)) != CC_OK) return st;
+    for (size_t i = 0; i < ranges.size(); ++i)
+        for (size_t j = i + 1; j < ranges.size(); ++j)
+            if ((ranges[i].written || ranges[j].written) && overlap(ranges[i], ranges[j]))
+                return fail(CC_ERR_ALIAS, "%s[%d] overlaps %s[%d]", ranges[i].name,
+                            ranges[i].index, ranges[j].name, ranges[j].index);
+    if ((st = ensure_device()) != CC_OK) return st;
+    for (const Range &r : ranges)
+        if ((st = check_device_range(reinterpret_cast<const void *>(r.lo), r.hi - r.lo,
+                                     r.name)) != CC_OK)
+            return st;
+    return CC_OK;
+}
+
+size_t bucket_elems(size_t bucket_bytes, size_t n) {
+    if (bucket_bytes == 0) return n;
+    const size_t e = bucket_bytes / 16 * CC_PAD_ELEMS;
+    return e < CC_PAD_ELEMS ? CC_PAD_ELEMS : e;
+}
+
+int run_step(const Slabs &s, const AdamScalars &c, size_t n, size_t bucket_bytes,
+             cudaStream_t stream) {
+    const size_t per = bucket_elems(bucket_bytes, n);
+    for (size_t b = 0; b < n; b += per) {
+        const size_t e = std::min(n, b + per);
+        const cudaError_t err = launch_fused(s, c, b, e, 0, stream);
+        if (err != cudaSuccess) return fail_cuda(err, "fused step launch");
+    }
+    return CC_OK;
+}
+
+}  // namespace ccdp
+
+using namespace ccdp;
+
+extern "C" {
+
+const char *cc_status_string(int status) {
+    switch (status) {
+        case CC_OK: return "CC_OK";
+        case CC_ERR_INVALID: return "CC_ERR_INVALID";
+        case CC_ERR_ALIAS: return "CC_ERR_ALIAS";
+        case CC_ERR_MISALIGNED: return "CC_ERR_MISALIGNED";
+        case CC_ERR_CUDA: return "CC_ERR_CUDA";
+        case CC_ERR_UNSUPPORTED: return "CC_ERR_UNSUPPORTED";
+        case CC_ERR_CAPACITY: return "CC_ERR_CAPACITY";
+        default: return "CC_ERR_UNKNOWN";
+    }
+}
+
+const char *cc_last_error(void) { return last_error(); }
+
+int cc_fused_dp_step_accum(const void *const *grads, const float *const *acc,
+                           float *master, float *m, float *v,
+                           void *const *params_out, size_t n, int R,
+                           size_t bucket_bytes, float lr, float beta1,
+                           float beta2, float eps, float weight_decay,
+                           int step, float grad_scale, int accum_k,
+                           void *stream) {
+    if (accum_k < 1) return fail(CC_ERR_INVALID, "accum_k=%d must be >= 1", accum_k);
+    if (accum_k > 1 && !acc)
+        return fail(CC_ERR_INVALID, "accum_k=%d needs the accumulators (acc is NULL)", accum_k);
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    AdamScalars c;
+    int st = make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
+    if (st != CC_OK) return st;
+    if (n == 0) return CC_OK;
+    Slabs s;
+    st = validate_slabs(grads, acc, master, m, v, params_out, n, R, acc != nullptr, &s);
+    if (st != CC_OK) return st;
+    return run_step(s, c, n, bucket_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int cc_fused_dp_step(const void *const *grads, float *master, float *m,
+                     float *v, void *const *params_out, size_t n, int R,
+                     size_t bucket_bytes, float lr, float beta1, float beta2,
+                     float eps, float weight_decay, int step, float grad_scale,
+                     int accum_k, void *stream) {
+    if (accum_k != 1)
+        return fail(CC_ERR_INVALID,
+                    "accum_k=%d: accumulated steps need cc_fused_dp_step_accum", accum_k);
+    return cc_fused_dp_step_accum(grads, nullptr, master, m, v, params_out, n, R,
+                                  bucket_bytes, lr, beta1, beta2, eps,
+                                  weight_decay, step, grad_scale, 1, stream);
+}
+
+int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
+                       float *master, float *m, float *v,
+                       void *const *params_out, size_t n, int R, size_t begin,
+                       size_t end, float lr, float beta1, float beta2,
+                       float eps, float weight_decay, int step,
+                       float grad_scale, int max_ctas, void *stream) {
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    if (begin > end || end > n)
+        return fail(CC_ERR_INVALID, "range [%zu, %zu) not inside [0, %zu)", begin, end, n);
+    if (begin % CC_PAD_ELEMS != 0)
+        return fail(CC_ERR_MISALIGNED, "begin=%zu is not a multiple of %d", begin, CC_PAD_ELEMS);
+    if (max_ctas < 0) return fail(CC_ERR_INVALID, "max_ctas=%d must be >= 0", max_ctas);
+    AdamScalars c;
+    int st = make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
+    if (st != CC_OK) return st;
+    if (begin == end) return CC_OK;
+    Slabs s;
+    st = validate_slabs(grads, acc, master, m, v, params_out, n, R, acc != nullptr, &s);
+    if (st != CC_OK) return st;
+    const cudaError_t e =
+        launch_fused(s, c, begin, end, max_ctas, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused bucket launch");
+}
+
+int cc_accumulate_local(const void *const *grads, float *const *acc, size_t n,
+                        int R, int first, void *stream) {
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    if (n == 0) return CC_OK;
+    if (!grads || !acc) return fail(CC_ERR_INVALID, "grads/acc arrays are NULL");
+    if (n > (SIZE_MAX / 8)) return fail(CC_ERR_INVALID, "n=%zu too large", n);
+    std::vector<Range> ranges;
+    for (int r = 0; r < R; ++r) {
+        const void *ps[2] = {grads[r], acc[r]};
+        const size_t bytes[2] = {2 * n, 4 * n};
+        const char *names[2] = {"grads", "acc"};
+        for (int k = 0; k < 2; ++k) {
+            if (!ps[k]) return fail(CC_ERR_INVALID, "%s[%d] is NULL", names[k], r);
+            if (reinterpret_cast<uintptr_t>(ps[k]) % 16 != 0)
+                return fail(CC_ERR_MISALIGNED, "%s[%d]=%p is not 16-byte aligned",
+                            names[k], r, ps[k]);
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(ps[k]);
+            ranges.push_back({lo, lo + bytes[k], k == 1, names[k], r});
+        }
+    }
+    for (size_t i = 0; i < ranges.size(); ++i)
+        for (size_t j = i + 1; j < ranges.size(); ++j)
+            if ((ranges[i].written || ranges[j].written) && overlap(ranges[i], ranges[j]))
+                return fail(CC_ERR_ALIAS, "%s[%d] overlaps %s[%d]", ranges[i].name,
+                            ranges[i].index, ranges[j].name, ranges[j].index);
+    int st = ensure_device();
+    if (st != CC_OK) return st;
+    for (const Range &r : ranges)
+        if ((st = check_device_range(reinterpret_cast<const void *>(r.lo), r.hi - r.lo,
+                                     r.name)) != CC_OK)
+            return st;
+    const cudaError_t e =
+        launch_accumulate(grads, acc, R, n, first != 0, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CC_OK : fail_cuda(e, "accumulate launch");
+}
+
+int cc_plan_buckets(const size_t *numel, int num_tensors, size_t bucket_bytes,
+                    size_t *offsets_out, size_t *bucket_begin_out,
+                    size_t *bucket_end_out, int capacity,
+                    int *num_buckets_out, size_t *n_padded_out) {
+    if (num_tensors < 1 || !numel || !offsets_out || !num_buckets_out)
+        return fail(CC_ERR_INVALID, "need num_tensors >= 1, numel, offsets_out, num_buckets_out");
+    if (capacity < 0 || (capacity > 0 && (!bucket_begin_out || !bucket_end_out)))
+        return fail(CC_ERR_INVALID, "capacity=%d with NULL bucket arrays", capacity);
+    // Slab position of the next tensor, start of the open bucket, and the
+    // open bucket's bf16 bytes.  Walk from the last tensor to the first.
+    size_t pos = 0, open_begin = 0, open_bytes = 0;
+    int count = 0;
+    auto emit = [&](size_t b, size_t e) {
+        if (count < capacity) {
+            bucket_begin_out[count] = b;
+            bucket_end_out[count] = e;
+        }
+        ++count;
+    };
+    for (int t = num_tensors - 1; t >= 0; --t) {
+        const size_t k = numel[t];
+        if (k > SIZE_MAX / 4 - pos)
+            return fail(CC_ERR_INVALID, "slab size overflows at tensor %d", t);
+        const size_t span = (k + CC_PAD_ELEMS - 1) / CC_PAD_ELEMS * CC_PAD_ELEMS;
+        offsets_out[t] = pos;
+        pos += span;
+        open_bytes += 2 * span;
+        if (bucket_bytes != 0 && open_bytes >= bucket_bytes) {
+            if (pos > open_begin) emit(open_begin, pos);
+            open_begin = pos;
+            open_bytes = 0;
+        }
+    }
+    if (pos > open_begin) emit(open_begin, pos);
+    *num_buckets_out = count;
+    if (n_padded_out) *n_padded_out = pos;
+    if (count > capacity)
+        return fail(CC_ERR_CAPACITY, "%d buckets, capacity %d", count, capacity);
+    return CC_OK;
+}
+
+int cc_bucket_ready_layers(const size_t *numel, const int *layer_of,
+                           const size_t *offsets, int num_tensors,
+                           const size_t *bucket_begin,
+                           const size_t *bucket_end, int num_buckets,
+                           int *ready_layer_out) {
+    if (num_tensors < 1 || num_buckets < 1 || !numel || !layer_of || !offsets ||
+        !bucket_begin || !bucket_end || !ready_layer_out)
+        return fail(CC_ERR_INVALID, "NULL array or empty list");
+    for (int b = 0; b < num_buckets; ++b) {
+        if (bucket_end[b] <= bucket_begin[b] || (b > 0 && bucket_begin[b] < bucket_end[b - 1]))
+            return fail(CC_ERR_INVALID, "bucket %d range is empty or out of order", b);
+        ready_layer_out[b] = -1;
+    }
+    // Each non-empty tensor finds its bucket by binary search on the bucket
+    // starts; the bucket keeps the lowest layer it has seen.
+    for (int t = 0; t < num_tensors; ++t) {
+        if (numel[t] == 0) continue;
+        const size_t *it = std::upper_bound(bucket_begin, bucket_begin + num_buckets, offsets[t]);
+        const int b = static_cast<int>(it - bucket_begin) - 1;
+        if (b < 0 || offsets[t] >= bucket_end[b])
+            return fail(CC_ERR_INVALID, "tensor %d at %zu lies in no bucket", t, offsets[t]);
+        if (ready_layer_out[b] < 0 || layer_of[t] < ready_layer_out[b])
+            ready_layer_out[b] = layer_of[t];
+    }
+    for (int b = 0; b < num_buckets; ++b)
+        if (ready_layer_out[b] < 0) return fail(CC_ERR_INVALID, "bucket %d holds no tensor", b);
+    return CC_OK;
+}
+
+int cc_l2_flush(void *buf, size_t bytes, void *stream) {
+    if (!buf) return fail(CC_ERR_INVALID, "buf is NULL");
+    if (reinterpret_cast<uintptr_t>(buf) % 16 != 0)
+        return fail(CC_ERR_MISALIGNED, "buf=%p is not 16-byte aligned", buf);
+    int st = ensure_device();
+    if (st != CC_OK) return st;
+    if ((st = check_device_range(buf, bytes, "buf")) != CC_OK) return st;
+    const cudaError_t e = launch_l2_flush(buf, bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CC_OK : fail_cuda(e, "l2 flush launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Internal interface between the C-ABI layer and the kernels of the fused
+// data-parallel step.  Not installed; the public ABI is include/cc_dp.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "cc_dp.h"
+
+namespace ccdp {
+
+// AdamW scalars, each rounded to binary32 once on the host (see
+// make_scalars in cc_dp_api.cu for how each is formed).
+struct AdamScalars {
+    float beta1, beta2;
+    float one_minus_b1, one_minus_b2;
+    float bias_corr1, bias_corr2;
+    float lr, eps;
+    float decay;      // 1 - lr*wd  (decoupled weight decay factor)
+    float inv_scale;  // 1 / grad_scale
+};
+
+// The slabs of one step.  Pointers are whole-slab bases; kernels index them
+// by element.  acc[r] are all null when the step does not accumulate.
+struct Slabs {
+    int R;
+    const void *grads[CC_MAX_R];   // bf16[n]
+    const float *acc[CC_MAX_R];    // fp32[n] or null
+    void *out[CC_MAX_R];           // bf16[n]
+    float *master, *m, *v;         // fp32[n]
+};
+
+// Enqueue the fused reduce + AdamW + redistribute kernel over elements
+// [begin, end) on `stream`.  Requires begin % CC_PAD_ELEMS == 0 and 16-byte
+// aligned slab bases (checked by the caller).  max_ctas > 0 caps the grid.
+cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
+                         size_t end, int max_ctas, cudaStream_t stream);
+
+// Enqueue one local accumulation micro-step over [0, n).
+cudaError_t launch_accumulate(const void *const *grads, float *const *acc,
+                              int R, size_t n, bool first,
+                              cudaStream_t stream);
+
+// Enqueue a write of `bytes` (rounded down to 16) into `buf`.
+cudaError_t launch_l2_flush(void *buf, size_t bytes, cudaStream_t stream);
+
+// Compute capability of the current device (queried once per device).
+cudaError_t check_device(int *major, int *minor);
+
+// ---- host-side helpers of the C-ABI layer (cc_dp_api.cu) -----------------
+
+// Record a one-line reason for cc_last_error() and return `status`.
+int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail_cuda(cudaError_t e, const char *what);
+const char *last_error();
+
+// CC_OK if the current device is an sm_103 GB300, else CC_ERR_UNSUPPORTED.
+int ensure_device();
+
+// CC_OK if [ptr, ptr + bytes) lies inside one device allocation.
+int check_device_range(const void *ptr, size_t bytes, const char *name);
+
+// Validate and round the AdamW hyper-parameters to the kernel's scalars.
+int make_scalars(float lr, float beta1, float beta2, float eps,
+                 float weight_decay, int step, float grad_scale,
+                 AdamScalars *c);
+
+// Validate a slab set (R, pointers, alignment, aliasing, device ranges of n
+// elements) and fill `s`.  need_acc selects whether acc[] is used.
+int validate_slabs(const void *const *grads, const float *const *acc,
+                   float *master, float *m, float *v, void *const *params_out,
+                   size_t n, int R, bool need_acc, Slabs *s);
+
+}  // namespace ccdp

@@ -1,0 +1,402 @@
+// Kernels of the fused data-parallel step for sm_103a (GB300).
+//
+// The path is a pure HBM stream: per element it reads R bf16 gradients and
+// the fp32 master/m/v, and writes master/m/v and R bf16 parameters, about
+// 0.3 flop per byte, so there is no contraction for the tensor cores.  What
+// matters is that every byte moves once, in full 32-byte sectors, with
+// enough loads in flight per SM to cover HBM latency:
+//   * one thread owns 8 consecutive elements, so each replica's gradient and
+//     parameter is one 16-byte access and each fp32 array two; a warp
+//     touches 512 contiguous bytes per bf16 stream and 1 KiB per fp32
+//     stream;
+//   * all of a thread's loads (R + 6 vectors, R = 8 gives 224 bytes) are
+//     issued before any arithmetic, so each thread has them all in flight;
+//   * streaming cache hints (ld/st .cs, evict-first) keep the single-use
+//     stream from displacing other kernels' working sets in L2;
+//   * a grid-stride loop over a grid sized to the SM count times resident
+//     blocks (occupancy), so all 152 SMs stay busy to the end of a bucket.
+//
+// Arithmetic is IEEE binary32 with each operation rounded on its own
+// (__fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn never contract to FMA), in the
+// order given in include/cc_dp.h, so the results are bit-identical to any
+// other correctly rounded evaluation of that order.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "cc_dp_internal.h"
+
+#ifndef CC_DP_THREADS
+#define CC_DP_THREADS 256
+#endif
+
+namespace ccdp {
+namespace {
+
+constexpr int kThreads = CC_DP_THREADS;
+
+struct FusedParams {
+    const uint4 *g[CC_MAX_R];      // 8 bf16 per vector
+    const float4 *acc[CC_MAX_R];   // 2 float4 per vector
+    uint4 *out[CC_MAX_R];
+    float4 *master, *m, *v;        // 2 float4 per vector
+    AdamScalars c;
+    size_t vec_begin;              // first 8-element vector of the range
+    size_t num_vec;                // full vectors in the range
+    size_t tail_begin;             // first element of the partial vector
+    int tail_len;                  // 0..7 elements after the full vectors
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) {
+    return __uint_as_float(w << 16);
+}
+__device__ __forceinline__ float bf16_hi(uint32_t w) {
+    return __uint_as_float(w & 0xFFFF0000u);
+}
+__device__ __forceinline__ float bf16_at(const void *base, size_t i) {
+    const unsigned short h = static_cast<const unsigned short *>(base)[i];
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+__device__ __forceinline__ void widen8(const uint4 q, float t[8]) {
+    t[0] = bf16_lo(q.x); t[1] = bf16_hi(q.x);
+    t[2] = bf16_lo(q.y); t[3] = bf16_hi(q.y);
+    t[4] = bf16_lo(q.z); t[5] = bf16_hi(q.z);
+    t[6] = bf16_lo(q.w); t[7] = bf16_hi(q.w);
+}
+
+// Two fp32 -> bf16x2, round to nearest even; a lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// One AdamW step on one element, given the reduced gradient s.
+__device__ __forceinline__ void adamw(float s, float &p, float &m, float &v,
+                                      const AdamScalars &c) {
+    const float g = __fmul_rn(s, c.inv_scale);
+    const float m_new = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.one_minus_b1, g));
+    const float v_new = __fadd_rn(__fmul_rn(c.beta2, v),
+                                  __fmul_rn(c.one_minus_b2, __fmul_rn(g, g)));
+    const float m_hat = __fdiv_rn(m_new, c.bias_corr1);
+    const float v_hat = __fdiv_rn(v_new, c.bias_corr2);
+    const float denom = __fadd_rn(__fsqrt_rn(v_hat), c.eps);
+    const float update = __fmul_rn(c.lr, __fdiv_rn(m_hat, denom));
+    p = __fsub_rn(__fmul_rn(p, c.decay), update);
+    m = m_new;
+    v = v_new;
+}
+
+template <int R, bool ACC>
+__device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
+    // Issue every load of this vector before any arithmetic.
+    uint4 gq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) gq[r] = __ldcs(p.g[r] + vi);
+    float4 aq[ACC ? R : 1][2];
+    if constexpr (ACC) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            aq[r][0] = __ldcs(p.acc[r] + 2 * vi);
+            aq[r][1] = __ldcs(p.acc[r] + 2 * vi + 1);
+        }
+    }
+    const float4 w0 = __ldcs(p.master + 2 * vi), w1 = __ldcs(p.master + 2 * vi + 1);
+    const float4 m0 = __ldcs(p.m + 2 * vi), m1 = __ldcs(p.m + 2 * vi + 1);
+    const float4 v0 = __ldcs(p.v + 2 * vi), v1 = __ldcs(p.v + 2 * vi + 1);
+
+    // Reduce in replica order.
+    float s[8], t[8];
+    widen8(gq[0], s);
+    if constexpr (ACC) {
+        const float a0[8] = {aq[0][0].x, aq[0][0].y, aq[0][0].z, aq[0][0].w,
+                             aq[0][1].x, aq[0][1].y, aq[0][1].z, aq[0][1].w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(a0[k], s[k]);
+    }
+#pragma unroll
+    for (int r = 1; r < R; ++r) {
+        widen8(gq[r], t);
+        if constexpr (ACC) {
+            const float ar[8] = {aq[r][0].x, aq[r][0].y, aq[r][0].z, aq[r][0].w,
+                                 aq[r][1].x, aq[r][1].y, aq[r][1].z, aq[r][1].w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], __fadd_rn(ar[k], t[k]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], t[k]);
+        }
+    }
+
+    float pw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) adamw(s[k], pw[k], mm[k], vv[k], p.c);
+
+    __stcs(p.master + 2 * vi, make_float4(pw[0], pw[1], pw[2], pw[3]));
+    __stcs(p.master + 2 * vi + 1, make_float4(pw[4], pw[5], pw[6], pw[7]));
+    __stcs(p.m + 2 * vi, make_float4(mm[0], mm[1], mm[2], mm[3]));
+    __stcs(p.m + 2 * vi + 1, make_float4(mm[4], mm[5], mm[6], mm[7]));
+    __stcs(p.v + 2 * vi, make_float4(vv[0], vv[1], vv[2], vv[3]));
+    __stcs(p.v + 2 * vi + 1, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    uint4 o;
+    o.x = pack_bf16x2(pw[0], pw[1]);
+    o.y = pack_bf16x2(pw[2], pw[3]);
+    o.z = pack_bf16x2(pw[4], pw[5]);
+    o.w = pack_bf16x2(pw[6], pw[7]);
+#pragma unroll
+    for (int r = 0; r < R; ++r) __stcs(p.out[r] + vi, o);
+}
+
+// One element of the partial last vector (scalar accesses).
+template <int R, bool ACC>
+__device__ __forceinline__ void fused_scalar(const FusedParams &p, size_t i) {
+    float s = bf16_at(p.g[0], i);
+    if constexpr (ACC) s = __fadd_rn(reinterpret_cast<const float *>(p.acc[0])[i], s);
+#pragma unroll
+    for (int r = 1; r < R; ++r) {
+        const float t = bf16_at(p.g[r], i);
+        if constexpr (ACC)
+            s = __fadd_rn(s, __fadd_rn(reinterpret_cast<const float *>(p.acc[r])[i], t));
+        else
+            s = __fadd_rn(s, t);
+    }
+    float *pm = reinterpret_cast<float *>(p.master);
+    float *mm = reinterpret_cast<float *>(p.m);
+    float *vv = reinterpret_cast<float *>(p.v);
+    float pw = pm[i], m = mm[i], v = vv[i];
+    adamw(s, pw, m, v, p.c);
+    pm[i] = pw;
+    mm[i] = m;
+    vv[i] = v;
+    const __nv_bfloat16 b = __float2bfloat16_rn(pw);
+#pragma unroll
+    for (int r = 0; r < R; ++r) reinterpret_cast<__nv_bfloat16 *>(p.out[r])[i] = b;
+}
+
+template <int R, bool ACC>
+__global__ void __launch_bounds__(kThreads)
+fused_step_kernel(const __grid_constant__ FusedParams p) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+         i < p.num_vec; i += stride)
+        fused_vector<R, ACC>(p, p.vec_begin + i);
+    if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len)
+        fused_scalar<R, ACC>(p, p.tail_begin + threadIdx.x);
+}
+
+// ---------------------------------------------------------------------------
+// Local accumulation micro-step: acc[r] = (first ? 0 : acc[r]) + g[r], where
+// "first" copies the gradient (no addition, so -0 stays -0).
+// ---------------------------------------------------------------------------
+struct AccumParams {
+    const uint4 *g[CC_MAX_R];
+    float4 *acc[CC_MAX_R];
+    size_t num_vec;
+    size_t tail_begin;
+    int tail_len;
+};
+
+template <bool FIRST>
+__global__ void __launch_bounds__(kThreads)
+accumulate_kernel(const __grid_constant__ AccumParams p) {
+    const int r = blockIdx.y;
+    const uint4 *g = p.g[r];
+    float4 *acc = p.acc[r];
+    const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+         i < p.num_vec; i += stride) {
+        const uint4 q = __ldcs(g + i);
+        float t[8];
+        widen8(q, t);
+        if constexpr (FIRST) {
+            __stcs(acc + 2 * i, make_float4(t[0], t[1], t[2], t[3]));
+            __stcs(acc + 2 * i + 1, make_float4(t[4], t[5], t[6], t[7]));
+        } else {
+            const float4 a0 = __ldcs(acc + 2 * i), a1 = __ldcs(acc + 2 * i + 1);
+            __stcs(acc + 2 * i, make_float4(__fadd_rn(a0.x, t[0]), __fadd_rn(a0.y, t[1]),
+                                            __fadd_rn(a0.z, t[2]), __fadd_rn(a0.w, t[3])));
+            __stcs(acc + 2 * i + 1,
+                   make_float4(__fadd_rn(a1.x, t[4]), __fadd_rn(a1.y, t[5]),
+                               __fadd_rn(a1.z, t[6]), __fadd_rn(a1.w, t[7])));
+        }
+    }
+    if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len) {
+        const size_t i = p.tail_begin + threadIdx.x;
+        float *a = reinterpret_cast<float *>(acc);
+        const float t = bf16_at(g, i);
+        a[i] = FIRST ? t : __fadd_rn(a[i], t);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+l2_flush_kernel(uint4 *buf, size_t num_vec, uint32_t salt) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+         i < num_vec; i += stride)
+        buf[i] = make_uint4(salt, static_cast<uint32_t>(i), salt, 0u);
+}
+
+// ---------------------------------------------------------------------------
+// Launch helpers
+// ---------------------------------------------------------------------------
+
+using FusedKernel = void (*)(FusedParams);
+
+template <int R>
+FusedKernel pick_fused(bool acc) {
+    return acc ? fused_step_kernel<R, true> : fused_step_kernel<R, false>;
+}
+
+FusedKernel fused_kernel_for(int R, bool acc) {
+    switch (R) {
+        case 1: return pick_fused<1>(acc);
+        case 2: return pick_fused<2>(acc);
+        case 3: return pick_fused<3>(acc);
+        case 4: return pick_fused<4>(acc);
+        case 5: return pick_fused<5>(acc);
+        case 6: return pick_fused<6>(acc);
+        case 7: return pick_fused<7>(acc);
+        case 8: return pick_fused<8>(acc);
+        case 9: return pick_fused<9>(acc);
+        case 10: return pick_fused<10>(acc);
+        case 11: return pick_fused<11>(acc);
+        case 12: return pick_fused<12>(acc);
+        case 13: return pick_fused<13>(acc);
+        case 14: return pick_fused<14>(acc);
+        case 15: return pick_fused<15>(acc);
+        case 16: return pick_fused<16>(acc);
+        default: return nullptr;
+    }
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    cudaError_t status = cudaSuccess;
+    int sm_count = 0;
+    int major = 0, minor = 0;
+    int fused_blocks_per_sm[CC_MAX_R + 1][2] = {};
+};
+
+DeviceInfo g_devices[kMaxDevices];
+
+cudaError_t device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e == cudaSuccess) {
+            d.sm_count = prop.multiProcessorCount;
+            d.major = prop.major;
+            d.minor = prop.minor;
+            for (int r = 1; r <= CC_MAX_R && e == cudaSuccess; ++r)
+                for (int a = 0; a < 2 && e == cudaSuccess; ++a)
+                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &d.fused_blocks_per_sm[r][a],
+                        reinterpret_cast<const void *>(fused_kernel_for(r, a != 0)),
+                        kThreads, 0);
+        }
+        d.status = e;
+        d.ready = true;
+    }
+    *out = &d;
+    return d.status;
+}
+
+size_t div_up(size_t a, size_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+cudaError_t check_device(int *major, int *minor) {
+    DeviceInfo *d = nullptr;
+    const cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return e;
+    *major = d->major;
+    *minor = d->minor;
+    return cudaSuccess;
+}
+
+cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
+                         size_t end, int max_ctas, cudaStream_t stream) {
+    if (end <= begin) return cudaSuccess;
+    DeviceInfo *d = nullptr;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return e;
+    const bool acc = s.acc[0] != nullptr;
+    FusedParams p{};
+    for (int r = 0; r < s.R; ++r) {
+        p.g[r] = static_cast<const uint4 *>(s.grads[r]);
+        p.acc[r] = reinterpret_cast<const float4 *>(s.acc[r]);
+        p.out[r] = static_cast<uint4 *>(s.out[r]);
+    }
+    p.master = reinterpret_cast<float4 *>(s.master);
+    p.m = reinterpret_cast<float4 *>(s.m);
+    p.v = reinterpret_cast<float4 *>(s.v);
+    p.c = c;
+    p.vec_begin = begin / CC_PAD_ELEMS;
+    p.num_vec = (end - begin) / CC_PAD_ELEMS;
+    p.tail_begin = begin + p.num_vec * CC_PAD_ELEMS;
+    p.tail_len = static_cast<int>(end - p.tail_begin);
+
+    size_t blocks = div_up(p.num_vec, kThreads);
+    const size_t resident =
+        static_cast<size_t>(d->sm_count) *
+        static_cast<size_t>(d->fused_blocks_per_sm[s.R][acc ? 1 : 0]);
+    if (resident > 0 && blocks > resident) blocks = resident;
+    if (max_ctas > 0 && blocks > static_cast<size_t>(max_ctas)) blocks = max_ctas;
+    if (blocks == 0) blocks = 1;
+    fused_kernel_for(s.R, acc)<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accumulate(const void *const *grads, float *const *acc,
+                              int R, size_t n, bool first,
+                              cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    DeviceInfo *d = nullptr;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return e;
+    AccumParams p{};
+    for (int r = 0; r < R; ++r) {
+        p.g[r] = static_cast<const uint4 *>(grads[r]);
+        p.acc[r] = reinterpret_cast<float4 *>(acc[r]);
+    }
+    p.num_vec = n / CC_PAD_ELEMS;
+    p.tail_begin = p.num_vec * CC_PAD_ELEMS;
+    p.tail_len = static_cast<int>(n - p.tail_begin);
+    size_t blocks = div_up(p.num_vec, kThreads);
+    const size_t cap = div_up(static_cast<size_t>(d->sm_count) * 8, R);
+    if (blocks > cap) blocks = cap;
+    if (blocks == 0) blocks = 1;
+    const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(R));
+    if (first)
+        accumulate_kernel<true><<<grid, kThreads, 0, stream>>>(p);
+    else
+        accumulate_kernel<false><<<grid, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_l2_flush(void *buf, size_t bytes, cudaStream_t stream) {
+    const size_t nv = bytes / 16;
+    if (nv == 0) return cudaSuccess;
+    DeviceInfo *d = nullptr;
+    cudaError_t e = device_info(&d);
+    if (e != cudaSuccess) return e;
+    static uint32_t salt = 0x9E3779B9u;
+    salt = salt * 1664525u + 1013904223u;
+    size_t blocks = div_up(nv, kThreads);
+    const size_t cap = static_cast<size_t>(d->sm_count) * 8;
+    if (blocks > cap) blocks = cap;
+    l2_flush_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
+        static_cast<uint4 *>(buf), nv, salt);
+    return cudaGetLastError();
+}
+
+}  // namespace ccdp

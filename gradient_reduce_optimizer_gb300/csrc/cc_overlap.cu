@@ -1,0 +1,224 @@
+// Overlap measurement for the bucketed fused step (cc_overlap_bench in
+// include/cc_dp.h).
+//
+// "Communication Optimization › Communication Overlap": DDP launches each
+// bucket's reduction on a separate CUDA stream as soon as all gradients in it
+// are ready, last layer first, and the step time is approximately
+// T_fwd + T_bwd + max(0, T_comm - T_overlap).  Here the backward pass is a
+// proxy of bf16 GEMMs on a compute stream that records one event per layer;
+// the side stream waits on the event of each bucket's ready layer and then
+// launches that bucket's fused reduce+AdamW+redistribute kernel.  The naive
+// synchronous schedule (backward, then reduction and optimizer, in strict
+// phases) is the sequential arm.  Stream ordering uses events only: no
+// kernel waits on a flag.
+
+#include <cublas_v2.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "cc_dp_internal.h"
+
+namespace ccdp {
+namespace {
+
+struct Resources {
+    cudaStream_t comp = nullptr, side = nullptr;
+    cudaEvent_t start = nullptr, stop = nullptr, side_done = nullptr;
+    std::vector<cudaEvent_t> layer;
+    cublasHandle_t blas = nullptr;
+
+    ~Resources() {
+        if (comp) cudaStreamSynchronize(comp);
+        if (side) cudaStreamSynchronize(side);
+        if (blas) cublasDestroy(blas);
+        for (cudaEvent_t e : layer)
+            if (e) cudaEventDestroy(e);
+        if (start) cudaEventDestroy(start);
+        if (stop) cudaEventDestroy(stop);
+        if (side_done) cudaEventDestroy(side_done);
+        if (comp) cudaStreamDestroy(comp);
+        if (side) cudaStreamDestroy(side);
+    }
+};
+
+struct Bench {
+    const cc_overlap_cfg &cfg;
+    const Slabs &slabs;
+    const AdamScalars &scalars;
+    Resources &res;
+
+    // One layer's GEMMs: C[M,N] = A[M,K] B[K,N] in row-major terms, i.e.
+    // C^T = B^T A^T for column-major cuBLAS.
+    cublasStatus_t gemms() {
+        const float alpha = 1.0f, beta = 0.0f;
+        for (int g = 0; g < cfg.gemms_per_layer; ++g) {
+            const cublasStatus_t st = cublasGemmEx(
+                res.blas, CUBLAS_OP_N, CUBLAS_OP_N, cfg.gemm_n, cfg.gemm_m, cfg.gemm_k,
+                &alpha, cfg.gemm_b, CUDA_R_16BF, cfg.gemm_n, cfg.gemm_a, CUDA_R_16BF,
+                cfg.gemm_k, &beta, cfg.gemm_c, CUDA_R_16BF, cfg.gemm_n,
+                CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+            if (st != CUBLAS_STATUS_SUCCESS) return st;
+        }
+        return CUBLAS_STATUS_SUCCESS;
+    }
+
+    int backward(bool record_layers) {
+        for (int l = cfg.num_layers - 1; l >= 0; --l) {
+            const cublasStatus_t st = gemms();
+            if (st != CUBLAS_STATUS_SUCCESS)
+                return fail(CC_ERR_CUDA, "cublasGemmEx failed (status %d)", static_cast<int>(st));
+            if (record_layers) {
+                const cudaError_t e = cudaEventRecord(res.layer[l], res.comp);
+                if (e != cudaSuccess) return fail_cuda(e, "layer event record");
+            }
+        }
+        return CC_OK;
+    }
+
+    int buckets(cudaStream_t s, bool wait_ready, int max_ctas) {
+        for (int b = 0; b < cfg.num_buckets; ++b) {
+            cudaError_t e = cudaSuccess;
+            if (wait_ready) e = cudaStreamWaitEvent(s, res.layer[cfg.bucket_ready_layer[b]], 0);
+            if (e == cudaSuccess)
+                e = launch_fused(slabs, scalars, cfg.bucket_begin[b], cfg.bucket_end[b],
+                                 max_ctas, s);
+            if (e != cudaSuccess) return fail_cuda(e, "bucket launch");
+        }
+        return CC_OK;
+    }
+
+    // Runs one arm once and returns its elapsed milliseconds in *ms.
+    int arm(int which, float *ms) {
+        cudaError_t e = cudaEventRecord(res.start, res.comp);
+        if (e != cudaSuccess) return fail_cuda(e, "start event");
+        int st = CC_OK;
+        switch (which) {
+            case 0:  // backward alone
+                st = backward(false);
+                break;
+            case 1:  // all buckets alone, on the compute stream
+                st = buckets(res.comp, false, 0);
+                break;
+            case 2: {  // overlapped: ready-driven buckets on the side stream
+                if ((e = cudaStreamWaitEvent(res.side, res.start, 0)) != cudaSuccess)
+                    return fail_cuda(e, "side wait");
+                if ((st = backward(true)) != CC_OK) return st;
+                if ((st = buckets(res.side, true, cfg.max_ctas)) != CC_OK) return st;
+                if ((e = cudaEventRecord(res.side_done, res.side)) != cudaSuccess)
+                    return fail_cuda(e, "side done event");
+                if ((e = cudaStreamWaitEvent(res.comp, res.side_done, 0)) != cudaSuccess)
+                    return fail_cuda(e, "join wait");
+                break;
+            }
+            case 3:  // naive synchronous: backward, then every bucket
+                if ((st = backward(false)) != CC_OK) return st;
+                st = buckets(res.comp, false, 0);
+                break;
+        }
+        if (st != CC_OK) return st;
+        if ((e = cudaEventRecord(res.stop, res.comp)) != cudaSuccess) return fail_cuda(e, "stop event");
+        if ((e = cudaEventSynchronize(res.stop)) != cudaSuccess) return fail_cuda(e, "arm sync");
+        if ((e = cudaEventElapsedTime(ms, res.start, res.stop)) != cudaSuccess)
+            return fail_cuda(e, "elapsed time");
+        return CC_OK;
+    }
+
+    int median(int which, float *out) {
+        float ms = 0.0f;
+        for (int i = 0; i < cfg.warmup; ++i) {
+            const int st = arm(which, &ms);
+            if (st != CC_OK) return st;
+        }
+        std::vector<float> t(cfg.iters);
+        for (int i = 0; i < cfg.iters; ++i) {
+            const int st = arm(which, &t[i]);
+            if (st != CC_OK) return st;
+        }
+        std::sort(t.begin(), t.end());
+        *out = (cfg.iters % 2) ? t[cfg.iters / 2]
+                               : 0.5f * (t[cfg.iters / 2 - 1] + t[cfg.iters / 2]);
+        return CC_OK;
+    }
+};
+
+}  // namespace
+}  // namespace ccdp
+
+using namespace ccdp;
+
+extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out) {
+    if (!cfg || !out) return fail(CC_ERR_INVALID, "cfg/out is NULL");
+    const cc_overlap_cfg &c = *cfg;
+    if (c.num_layers < 1 || c.gemms_per_layer < 0 || c.gemm_m < 1 || c.gemm_n < 1 ||
+        c.gemm_k < 1)
+        return fail(CC_ERR_INVALID, "proxy backward shape must be positive");
+    if (c.iters < 1 || c.iters > 1000 || c.warmup < 0 || c.warmup > 1000)
+        return fail(CC_ERR_INVALID, "iters=%d must be in 1..1000, warmup in 0..1000", c.iters);
+    if (c.max_ctas < 0) return fail(CC_ERR_INVALID, "max_ctas=%d must be >= 0", c.max_ctas);
+    if (c.num_buckets < 1 || !c.bucket_begin || !c.bucket_end || !c.bucket_ready_layer)
+        return fail(CC_ERR_INVALID, "need at least one bucket");
+    for (int b = 0; b < c.num_buckets; ++b) {
+        if (c.bucket_begin[b] % CC_PAD_ELEMS != 0)
+            return fail(CC_ERR_MISALIGNED, "bucket %d begins at %zu", b, c.bucket_begin[b]);
+        if (c.bucket_begin[b] >= c.bucket_end[b] || c.bucket_end[b] > c.n)
+            return fail(CC_ERR_INVALID, "bucket %d range [%zu, %zu) invalid for n=%zu", b,
+                        c.bucket_begin[b], c.bucket_end[b], c.n);
+        if (c.bucket_ready_layer[b] < 0 || c.bucket_ready_layer[b] >= c.num_layers)
+            return fail(CC_ERR_INVALID, "bucket %d ready layer %d out of range", b,
+                        c.bucket_ready_layer[b]);
+    }
+    AdamScalars sc;
+    int st = make_scalars(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, c.step,
+                          c.grad_scale, &sc);
+    if (st != CC_OK) return st;
+    if (c.n == 0) return fail(CC_ERR_INVALID, "n must be > 0");
+    Slabs slabs;
+    st = validate_slabs(c.grads, c.acc, c.master, c.m, c.v, c.params_out, c.n, c.R,
+                        c.acc != nullptr, &slabs);
+    if (st != CC_OK) return st;
+    if (c.gemms_per_layer > 0) {
+        if (!c.gemm_a || !c.gemm_b || !c.gemm_c)
+            return fail(CC_ERR_INVALID, "GEMM operand buffers are NULL");
+        const size_t M = c.gemm_m, N = c.gemm_n, K = c.gemm_k;
+        if ((st = check_device_range(c.gemm_a, 2 * M * K, "gemm_a")) != CC_OK) return st;
+        if ((st = check_device_range(c.gemm_b, 2 * K * N, "gemm_b")) != CC_OK) return st;
+        if ((st = check_device_range(c.gemm_c, 2 * M * N, "gemm_c")) != CC_OK) return st;
+    }
+
+    Resources res;
+    cudaError_t e;
+    int lo = 0, hi = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess)
+        return fail_cuda(e, "priority range");
+    if ((e = cudaStreamCreateWithPriority(&res.comp, cudaStreamNonBlocking, lo)) != cudaSuccess)
+        return fail_cuda(e, "compute stream");
+    if ((e = cudaStreamCreateWithPriority(&res.side, cudaStreamNonBlocking,
+                                          c.side_priority_high ? hi : lo)) != cudaSuccess)
+        return fail_cuda(e, "side stream");
+    if ((e = cudaEventCreate(&res.start)) != cudaSuccess ||
+        (e = cudaEventCreate(&res.stop)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&res.side_done, cudaEventDisableTiming)) != cudaSuccess)
+        return fail_cuda(e, "event create");
+    res.layer.assign(c.num_layers, nullptr);
+    for (int l = 0; l < c.num_layers; ++l)
+        if ((e = cudaEventCreateWithFlags(&res.layer[l], cudaEventDisableTiming)) != cudaSuccess)
+            return fail_cuda(e, "layer event create");
+    if (cublasCreate(&res.blas) != CUBLAS_STATUS_SUCCESS)
+        return fail(CC_ERR_CUDA, "cublasCreate failed");
+    if (cublasSetStream(res.blas, res.comp) != CUBLAS_STATUS_SUCCESS)
+        return fail(CC_ERR_CUDA, "cublasSetStream failed");
+
+    Bench bench{c, slabs, sc, res};
+    cc_overlap_result r{};
+    if ((st = bench.median(0, &r.t_bwd_ms)) != CC_OK) return st;
+    if ((st = bench.median(1, &r.t_comm_ms)) != CC_OK) return st;
+    if ((st = bench.median(2, &r.t_step_overlap_ms)) != CC_OK) return st;
+    if ((st = bench.median(3, &r.t_step_seq_ms)) != CC_OK) return st;
+    r.exposed_ms = r.t_step_overlap_ms - r.t_bwd_ms;
+    r.exposed_bound_ms = std::max(0.0f, r.t_comm_ms - r.t_bwd_ms);
+    r.num_buckets = c.num_buckets;
+    *out = r;
+    return CC_OK;
+}

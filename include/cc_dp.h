@@ -1,0 +1,285 @@
+/*
+ * cc_dp.h -- C ABI of the GB300 fused data-parallel step.
+ *
+ * One pass over R emulated data-parallel replicas that does, per element:
+ *   reduce   the R bf16 gradient replicas, summed in fixed order r = 0..R-1
+ *            in fp32 (stands in for the ReduceScatter),
+ *   update   one AdamW step in fp32 on the fp32 master weights and moments,
+ *   gather   the bf16-rounded parameters stored to all R replica slabs
+ *            (stands in for the AllGather),
+ * launched bucket by bucket in reverse layer order.
+ *
+ * Sources.  "LIT-735: Breaking the Computation and Communication Abstraction
+ * Barrier in Distributed Machine Learning Workloads" (CoCoNet), Key
+ * takeaways: the data-parallel result is a fused ReduceScatter-optimizer-
+ * AllGather for BERT training with Adam.  "Communication Optimization ›
+ * Communication Overlap": DDP groups parameters into fixed-size buckets
+ * (default 25 MB), launches each bucket as soon as its gradients are ready on
+ * a separate stream, last layer first; the step-time equation T_step ~
+ * T_fwd + T_bwd + max(0, T_comm - T_overlap).  "Overlapping Communication and
+ * Computation": with gradient accumulation, k-1 micro-steps only accumulate
+ * locally and one step in k carries the whole reduction.
+ *
+ * Arithmetic (each operation a separately rounded IEEE binary32 op):
+ *   s   = g[0] + g[1] + ... + g[R-1]          left to right, from g[0]
+ *         (with accumulators: s = (acc[0]+g[0]) + (acc[1]+g[1]) + ...)
+ *   g^  = s * fl(1/grad_scale)
+ *   m'  = beta1*m + fl(1-beta1)*g^
+ *   v'  = beta2*v + fl(1-beta2)*(g^*g^)
+ *   p'  = p*fl(1 - lr*wd) - lr*((m'/bc1) / (sqrt(v'/bc2) + eps))
+ *         with bcX = (float)(1 - betaX^step) computed in double
+ *   out[r] = bf16 round-to-nearest-even of p', for every r
+ * NaN and Inf propagate; no step is skipped.
+ *
+ * Conventions shared by every entry point:
+ *  - Device pointers are caller-owned device memory (e.g. from torch).  The
+ *    library never frees them.  Host pointer arrays (grads[], params_out[],
+ *    acc[]) are read during the call only.
+ *  - Every slab base must be 16-byte aligned (CC_ERR_MISALIGNED otherwise).
+ *  - Each device range [ptr, ptr + bytes) must lie inside one device
+ *    allocation; a range that does not is rejected with CC_ERR_INVALID
+ *    before any launch.
+ *  - Written ranges must not overlap one another nor any read range
+ *    (CC_ERR_ALIAS); master, m and v are updated in place.  Read-only
+ *    ranges (gradients, accumulators) may alias each other.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *    enqueue work and never synchronise.  The returned status covers host
+ *    validation and launch errors; a fault inside a kernel surfaces at the
+ *    caller's next synchronisation.
+ *  - On any error nothing has been launched by that call, except
+ *    CC_ERR_CUDA from a launch, which may follow earlier buckets' launches.
+ *  - cc_last_error() gives a one-line reason for the last failing call on
+ *    the calling thread.
+ *  - Sizes are in elements unless the name says bytes.  "MB" in bucket sizes
+ *    is MiB (2^20 bytes) of bf16 gradient per replica.
+ */
+#ifndef CC_DP_H
+#define CC_DP_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of this ABI are exported; everything else in the library is
+ * hidden. */
+#if defined(__GNUC__)
+#define CC_API __attribute__((visibility("default")))
+#else
+#define CC_API
+#endif
+
+/* Largest number of emulated replicas one call handles. */
+#define CC_MAX_R 16
+/* Every tensor span in a planned slab is padded to this many elements
+ * (16 bytes of bf16), so every bucket starts on a 16-byte boundary. */
+#define CC_PAD_ELEMS 8
+
+typedef enum cc_status {
+    CC_OK = 0,
+    CC_ERR_INVALID = -1,      /* bad argument (pointer, size, hyper-parameter) */
+    CC_ERR_ALIAS = -2,        /* a written range overlaps another range */
+    CC_ERR_MISALIGNED = -3,   /* a slab base (or bucket start) is not 16-byte aligned */
+    CC_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed */
+    CC_ERR_UNSUPPORTED = -5,  /* no usable device, or not an sm_103 device */
+    CC_ERR_CAPACITY = -6      /* an output array is too small; count reported */
+} cc_status;
+
+/* Name of a status code ("CC_OK", ...).  Never NULL. */
+CC_API const char *cc_status_string(int status);
+
+/* One-line reason for the last non-OK status returned on this thread. */
+CC_API const char *cc_last_error(void);
+
+/*
+ * cc_fused_dp_step -- reduce R gradient replicas, take one AdamW step and
+ * redistribute the parameters, bucket by bucket (CoCoNet's fused
+ * ReduceScatter-Adam-AllGather, Key takeaways of LIT-735; DDP bucketing,
+ * Communication Overlap).
+ *
+ *   grads[R]       bf16[n] each, read.  Replica r's gradient slab.
+ *   master, m, v   fp32[n], read and written in place: master weights and
+ *                  the two Adam moments.
+ *   params_out[R]  bf16[n] each, written: every replica's parameter slab.
+ *   n              elements per slab (0 is a no-op returning CC_OK; the
+ *                  pointers are then not examined).
+ *   R              replicas, 1..CC_MAX_R.
+ *   bucket_bytes   bf16 gradient bytes per bucket and replica; [0, n) is
+ *                  cut into consecutive buckets of floor(bucket_bytes/16)*8
+ *                  elements (at least 8), launched in slab order, one kernel
+ *                  launch per bucket.  0 = one bucket.  Slabs laid out by
+ *                  cc_plan_buckets hold the last layer first, so slab order
+ *                  is reverse layer order.  Values never depend on the cut.
+ *   lr >= 0, 0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0, weight_decay >= 0:
+ *                  finite AdamW hyper-parameters (decoupled decay).
+ *   step >= 1      the step number t in the bias corrections.
+ *   grad_scale     finite, > 0: the loss scale the gradients carry.
+ *   accum_k        must be 1 here; accumulated steps (k > 1) need the
+ *                  accumulators of cc_fused_dp_step_accum.
+ *   stream         cudaStream_t.
+ *
+ * Returns CC_OK or a negative cc_status.  Allocates nothing.
+ */
+CC_API int cc_fused_dp_step(const void *const *grads, float *master, float *m,
+                     float *v, void *const *params_out, size_t n, int R,
+                     size_t bucket_bytes, float lr, float beta1, float beta2,
+                     float eps, float weight_decay, int step, float grad_scale,
+                     int accum_k, void *stream);
+
+/*
+ * cc_accumulate_local -- one of the k-1 local micro-steps of gradient
+ * accumulation ("Overlapping Communication and Computation", paragraph on
+ * accumulation): acc[r] = g[r] (first != 0) or acc[r] + g[r], elementwise in
+ * fp32, for every replica; no value crosses replicas.
+ *
+ *   grads[R]  bf16[n] each, read.     acc[R]  fp32[n] each, written.
+ *   n, R, stream as above.            first   nonzero on micro-step 1.
+ */
+CC_API int cc_accumulate_local(const void *const *grads, float *const *acc, size_t n,
+                        int R, int first, void *stream);
+
+/*
+ * cc_fused_dp_step_accum -- the reducing k-th step of gradient accumulation:
+ * as cc_fused_dp_step, but each replica's local total acc[r] + g[r] is formed
+ * first and those totals are summed across replicas in order r = 0..R-1.
+ *
+ *   acc[R]    fp32[n] each, read (not modified): replica r's sum of micro-
+ *             steps 1..k-1 from cc_accumulate_local.  May be NULL only
+ *             when accum_k == 1 (then identical to cc_fused_dp_step).
+ *   accum_k   >= 1, the number of micro-steps in this optimizer step.
+ */
+CC_API int cc_fused_dp_step_accum(const void *const *grads, const float *const *acc,
+                           float *master, float *m, float *v,
+                           void *const *params_out, size_t n, int R,
+                           size_t bucket_bytes, float lr, float beta1,
+                           float beta2, float eps, float weight_decay,
+                           int step, float grad_scale, int accum_k,
+                           void *stream);
+
+/*
+ * cc_fused_dp_bucket -- the fused step on one element range [begin, end) of
+ * the slabs, as one kernel launch: the unit a scheduler launches when a
+ * bucket's gradients become ready (DDP bucketing, Communication Overlap).
+ * Slab pointers and n describe the whole slabs, as for cc_fused_dp_step_accum
+ * (acc may be NULL).  begin must be a multiple of CC_PAD_ELEMS (else
+ * CC_ERR_MISALIGNED) and begin <= end <= n.  max_ctas > 0 caps the grid (a
+ * CTA budget that leaves SMs to concurrent compute); 0 = fill the GPU.
+ */
+CC_API int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
+                       float *master, float *m, float *v,
+                       void *const *params_out, size_t n, int R, size_t begin,
+                       size_t end, float lr, float beta1, float beta2,
+                       float eps, float weight_decay, int step,
+                       float grad_scale, int max_ctas, void *stream);
+
+/*
+ * cc_plan_buckets -- lay tensors out in reverse layer order and cut them into
+ * buckets (Communication Overlap: backward produces the last layer's
+ * gradients first, buckets hold a configurable size, default 25 MB, and the
+ * last layer's bucket launches first; Overlapping Communication and
+ * Computation: a very large single tensor is not split).  Host only: no
+ * CUDA call.
+ *
+ *   numel[T]          tensor sizes in forward (layer) order.
+ *   bucket_bytes      cap in bf16 bytes; a bucket closes as soon as its
+ *                     padded spans reach the cap; 0 = one bucket.
+ *   offsets_out[T]    written: tensor t's first slab element.  Spans are
+ *                     padded to CC_PAD_ELEMS; tensor T-1 is at offset 0.
+ *   bucket_begin_out, bucket_end_out [capacity]: written, element ranges
+ *                     in launch order.  Buckets with no elements are not
+ *                     emitted (a trailing run of empty tensors).
+ *   capacity          length of the two bucket arrays.  If it is too small
+ *                     the call writes *num_buckets_out and returns
+ *                     CC_ERR_CAPACITY (pass 0 and NULLs to query).
+ *   num_buckets_out   written: number of buckets.
+ *   n_padded_out      written: slab length in elements (may be NULL).
+ */
+CC_API int cc_plan_buckets(const size_t *numel, int num_tensors, size_t bucket_bytes,
+                    size_t *offsets_out, size_t *bucket_begin_out,
+                    size_t *bucket_end_out, int capacity,
+                    int *num_buckets_out, size_t *n_padded_out);
+
+/*
+ * cc_bucket_ready_layers -- for each bucket, the backward layer after which
+ * all its gradients exist: the lowest layer index among its non-empty
+ * tensors (backward runs from the highest layer down).  Host only.
+ *
+ *   layer_of[T]  layer of each tensor (forward order).  Other arrays as
+ *                returned by cc_plan_buckets.  ready_layer_out[num_buckets]
+ *                written.
+ */
+CC_API int cc_bucket_ready_layers(const size_t *numel, const int *layer_of,
+                           const size_t *offsets, int num_tensors,
+                           const size_t *bucket_begin,
+                           const size_t *bucket_end, int num_buckets,
+                           int *ready_layer_out);
+
+/*
+ * cc_overlap_bench -- measure how much of the bucketed fused step hides
+ * behind a proxy backward pass ("Communication Overlap": step-time equation;
+ * DDP launches each bucket on a separate stream once ready; "naive
+ * synchronous data-parallel" runs backward, then the reduction, then the
+ * optimizer, in strict phases).
+ *
+ * The proxy backward runs num_layers x gemms_per_layer bf16 GEMMs
+ * (C[M,N] = A[M,K] B[K,N], fp32 accumulation, cuBLAS) on a compute stream,
+ * layer num_layers-1 first, and records an event after each layer.  Bucket b
+ * launches on a side stream once the event of bucket_ready_layer[b] has
+ * fired.  Four arms are timed with CUDA events, each the median of `iters`
+ * runs after `warmup` runs:
+ *   t_bwd_ms          the GEMMs alone;
+ *   t_comm_ms         all buckets alone, back to back;
+ *   t_step_overlap_ms GEMMs and ready-driven buckets together;
+ *   t_step_seq_ms     GEMMs, then all buckets, on one stream.
+ * exposed_ms = t_step_overlap_ms - t_bwd_ms; exposed_bound_ms =
+ * max(0, t_comm_ms - t_bwd_ms), the least any schedule can expose.
+ *
+ * The slabs are stepped for real (master/m/v change on every run).  The GEMM
+ * operands are caller-owned bf16 device buffers: A holds M*K, B K*N and C
+ * M*N elements.  The call synchronises its own streams, creates and destroys
+ * its streams, events and cuBLAS handle, and allocates no device memory of
+ * its own beyond what cuBLAS takes for its handle.
+ */
+typedef struct cc_overlap_cfg {
+    const void *const *grads;      /* [R] bf16[n] */
+    const float *const *acc;       /* [R] fp32[n] or NULL */
+    float *master, *m, *v;         /* fp32[n] */
+    void *const *params_out;       /* [R] bf16[n] */
+    size_t n;
+    int R;
+    const size_t *bucket_begin;    /* [num_buckets], launch order */
+    const size_t *bucket_end;
+    const int *bucket_ready_layer; /* [num_buckets], in [0, num_layers) */
+    int num_buckets;
+    float lr, beta1, beta2, eps, weight_decay;
+    int step;
+    float grad_scale;
+    int num_layers, gemms_per_layer;
+    int gemm_m, gemm_n, gemm_k;
+    void *gemm_a, *gemm_b, *gemm_c;  /* bf16 device buffers */
+    int warmup, iters;             /* iters in 1..1000 */
+    int max_ctas;                  /* bucket kernels' CTA cap while overlapped; 0 = full */
+    int side_priority_high;        /* nonzero: side stream at the highest priority */
+} cc_overlap_cfg;
+
+typedef struct cc_overlap_result {
+    float t_bwd_ms, t_comm_ms, t_step_overlap_ms, t_step_seq_ms;
+    float exposed_ms, exposed_bound_ms;
+    int num_buckets;
+} cc_overlap_result;
+
+CC_API int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out);
+
+/*
+ * cc_l2_flush -- overwrite `bytes` of the caller's device buffer `buf`
+ * (16-byte aligned) so that a timed kernel that follows finds none of its
+ * data in L2.  Measurement helper; not part of the step.
+ */
+CC_API int cc_l2_flush(void *buf, size_t bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CC_DP_H */

@@ -1,0 +1,212 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol,
+plans buckets exactly like the oracle, and rejects bad arguments before any
+launch.  No kernel runs here (no GPU needed)."""
+import os
+import random
+import re
+
+import pytest
+
+import oracle
+from gradient_reduce_optimizer_gb300 import build as gbuild
+from gradient_reduce_optimizer_gb300 import capi
+from gradient_reduce_optimizer_gb300 import workloads as wl
+from plan_fixtures import load_cases
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cc_dp.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gbuild.build()
+    return capi.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\bCC_API\b[^;(]*?\b(cc_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 10
+    L = capi.lib()
+    for name in names:
+        assert hasattr(L, name), name
+    # and the binding covers every one of them under the same name
+    for name in names:
+        assert callable(getattr(capi, name)), name
+
+
+def test_status_strings():
+    assert capi.cc_status_string(0) == "CC_OK"
+    for code, name in [(-1, "CC_ERR_INVALID"), (-2, "CC_ERR_ALIAS"),
+                       (-3, "CC_ERR_MISALIGNED"), (-4, "CC_ERR_CUDA"),
+                       (-5, "CC_ERR_UNSUPPORTED"), (-6, "CC_ERR_CAPACITY")]:
+        assert capi.cc_status_string(code) == name
+    assert capi.cc_status_string(-99) == "CC_ERR_UNKNOWN"
+
+
+# ---------------------------------------------------------------------------
+# Planner: bit-exact against the oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", load_cases(), ids=lambda c: c["name"])
+def test_planner_hand_counted(case):
+    offsets, buckets, n_pad = capi.cc_plan_buckets(case["numel"],
+                                                   case["bucket_bytes"])
+    assert (offsets, buckets, n_pad) == (case["offsets"], case["buckets"],
+                                         case["n_padded"])
+    assert capi.cc_bucket_ready_layers(case["numel"], case["layer"], offsets,
+                                       buckets) == case["ready"]
+
+
+@pytest.mark.parametrize("tensors", ["bert", "gpt2"])
+@pytest.mark.parametrize("mib", [0, 1, 4, 25, 100, 500])
+def test_planner_model_lists_match_oracle(tensors, mib):
+    t = wl.bert_large_tensors() if tensors == "bert" else wl.gpt2_slice_tensors()
+    numel = [x[1] for x in t]
+    layer_of = [x[2] for x in t]
+    mine = capi.cc_plan_buckets(numel, mib * wl.MiB)
+    ref = oracle.plan_buckets(numel, mib * wl.MiB)
+    assert mine == ref
+    assert (capi.cc_bucket_ready_layers(numel, layer_of, mine[0], mine[1]) ==
+            oracle.bucket_ready_layers(numel, layer_of, ref[0], ref[1]))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_planner_random_lists_match_oracle(seed):
+    rnd = random.Random(1000 + seed)
+    T = rnd.randint(1, 80)
+    numel = [rnd.choice([0, 1, 3, 8, 15, 16, 17, 255, 4096, 99991])
+             for _ in range(T)]
+    if sum(numel) == 0:
+        numel[-1] = 5
+    layer_of = sorted(rnd.randint(0, 20) for _ in range(T))
+    cap = rnd.choice([0, 1, 16, 17, 512, 8192, 1 << 20])
+    mine = capi.cc_plan_buckets(numel, cap)
+    ref = oracle.plan_buckets(numel, cap)
+    assert mine == ref
+    assert (capi.cc_bucket_ready_layers(numel, layer_of, mine[0], mine[1]) ==
+            oracle.bucket_ready_layers(numel, layer_of, ref[0], ref[1]))
+
+
+def test_planner_capacity_and_bad_input():
+    L = capi.lib()
+    import ctypes
+    numel = (ctypes.c_size_t * 3)(10, 20, 30)
+    offs = (ctypes.c_size_t * 3)()
+    b = (ctypes.c_size_t * 1)()
+    e = (ctypes.c_size_t * 1)()
+    cnt = ctypes.c_int(0)
+    st = L.cc_plan_buckets(numel, 3, 16, offs, b, e, 1, ctypes.byref(cnt), None)
+    assert st == capi.CC_ERR_CAPACITY and cnt.value == 3
+    assert L.cc_plan_buckets(numel, 0, 16, offs, b, e, 1, ctypes.byref(cnt),
+                             None) == capi.CC_ERR_INVALID
+    assert L.cc_plan_buckets(numel, 3, 16, offs, None, None, 2,
+                             ctypes.byref(cnt), None) == capi.CC_ERR_INVALID
+
+
+# ---------------------------------------------------------------------------
+# Argument validation (returns before touching any device)
+# ---------------------------------------------------------------------------
+
+ADAM = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+            step=1, grad_scale=1.0)
+MB = 1 << 20
+
+
+def fake_slabs(R, n, base=1 << 40):
+    """Aligned, non-overlapping fake addresses (never dereferenced)."""
+    stride = ((4 * n + 4095) // 4096 + 1) * 4096
+    addr = iter(range(base, base + stride * (3 * R + 8), stride))
+    grads = [next(addr) for _ in range(R)]
+    outs = [next(addr) for _ in range(R)]
+    acc = [next(addr) for _ in range(R)]
+    master, m, v = next(addr), next(addr), next(addr)
+    return grads, acc, master, m, v, outs
+
+
+def step_status(grads, master, m, v, outs, n, R, **kw):
+    args = dict(ADAM)
+    args.update(kw)
+    accum_k = args.pop("accum_k", 1)
+    try:
+        capi.cc_fused_dp_step(grads, master, m, v, outs, n, R, 0,
+                              accum_k=accum_k, stream=0, **args)
+        return capi.CC_OK
+    except capi.CCError as err:
+        return err.status
+
+
+@pytest.mark.parametrize("kw", [
+    dict(lr=-1.0), dict(lr=float("nan")), dict(beta1=1.0), dict(beta1=-0.1),
+    dict(beta2=1.0), dict(eps=-1e-8), dict(eps=float("inf")),
+    dict(weight_decay=-0.1), dict(step=0), dict(grad_scale=0.0),
+    dict(grad_scale=float("inf")), dict(grad_scale=1e-45), dict(accum_k=2),
+    dict(accum_k=0),
+])
+def test_rejects_bad_hyper_parameters(kw):
+    g, _, p, m, v, o = fake_slabs(2, 64)
+    assert step_status(g, p, m, v, o, 64, 2, **kw) == capi.CC_ERR_INVALID
+
+
+@pytest.mark.parametrize("R", [0, 17, -1])
+def test_rejects_bad_replica_count(R):
+    g, _, p, m, v, o = fake_slabs(16, 64)
+    assert step_status(g, p, m, v, o, 64, R) == capi.CC_ERR_INVALID
+
+
+def test_n_zero_is_a_no_op():
+    assert step_status([0, 0], 0, 0, 0, [0, 0], 0, 2) == capi.CC_OK
+
+
+def test_rejects_null_and_misaligned_and_aliased():
+    g, _, p, m, v, o = fake_slabs(3, 1000)
+    assert step_status(g, 0, m, v, o, 1000, 3) == capi.CC_ERR_INVALID
+    assert step_status([g[0], 0, g[2]], p, m, v, o, 1000, 3) == capi.CC_ERR_INVALID
+    assert step_status(g, p + 8, m, v, o, 1000, 3) == capi.CC_ERR_MISALIGNED
+    assert step_status(g, p, m, v, [o[0], o[1] + 2, o[2]], 1000, 3) == \
+        capi.CC_ERR_MISALIGNED
+    # a parameter slab overlapping a gradient slab
+    assert step_status(g, p, m, v, [o[0], g[1] + 1024, o[2]], 1000, 3) == \
+        capi.CC_ERR_ALIAS
+    # m overlapping master
+    assert step_status(g, p, p + 16, v, o, 1000, 3) == capi.CC_ERR_ALIAS
+    # two output replicas sharing memory
+    assert step_status(g, p, m, v, [o[0], o[0], o[2]], 1000, 3) == capi.CC_ERR_ALIAS
+    # read-only gradient slabs may alias each other
+    st = step_status([g[0], g[0], g[0]], p, m, v, o, 1000, 3)
+    assert st in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID)  # no device / fake ptr
+
+
+def test_fake_pointers_never_reach_a_launch():
+    """Valid-looking fake addresses fail at the device checks: without a GPU
+    as CC_ERR_UNSUPPORTED, with one as CC_ERR_INVALID (not allocated)."""
+    g, acc, p, m, v, o = fake_slabs(4, 4096)
+    assert step_status(g, p, m, v, o, 4096, 4) in (capi.CC_ERR_UNSUPPORTED,
+                                                    capi.CC_ERR_INVALID)
+
+
+def test_bucket_and_accumulate_validation():
+    g, acc, p, m, v, o = fake_slabs(2, 1000)
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_fused_dp_bucket(g, None, p, m, v, o, 1000, 2, 4, 100, stream=0,
+                                **ADAM)
+    assert ei.value.status == capi.CC_ERR_MISALIGNED
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_fused_dp_bucket(g, None, p, m, v, o, 1000, 2, 8, 1001, stream=0,
+                                **ADAM)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_fused_dp_step_accum(g, None, p, m, v, o, 1000, 2, 0, accum_k=4,
+                                    stream=0, **ADAM)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_accumulate_local(g, [acc[0], g[1]], 1000, 2, True, stream=0)
+    assert ei.value.status == capi.CC_ERR_ALIAS
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_accumulate_local(g, [acc[0], acc[1] + 4], 1000, 2, True, stream=0)
+    assert ei.value.status == capi.CC_ERR_MISALIGNED

@@ -1,0 +1,294 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle.
+
+Bar: bit-identical master/m/v and bf16 parameters on every case (NaN
+payloads excepted: a NaN must meet a NaN).  The operation order is fixed in
+include/cc_dp.h and both sides round every binary32 operation separately, so
+the benchmark spec's tolerance (1e-5 relative on fp32 state, 1 bf16 ulp on
+parameters) is never needed; bit equality is asserted instead.
+
+Element by element at sizes the oracle finishes in seconds (spanning many
+thread blocks, grid-stride rounds and a ragged tail), and on sampled
+elements at the full workload sizes in the launch configuration the
+benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gradient_reduce_optimizer_gb300 import build as gbuild
+from gradient_reduce_optimizer_gb300 import capi
+from gradient_reduce_optimizer_gb300 import workloads as wl
+from gpu_common import (DEV, assert_bits, compare_all, f32, gpu_step, host_copy,
+                        hp_of, new_slabs, oracle_step, planned_workload_slabs,
+                        random_inputs, u16, workload_grads)
+
+pytestmark = pytest.mark.gpu
+
+HP1 = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0,
+           step=1, grad_scale=1.0)
+HP10 = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
+            step=10, grad_scale=1.0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    gbuild.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return capi.lib()
+
+
+def check_full(s, hp, bucket_bytes=0, label=""):
+    grads, state, _ = host_copy(s)
+    gpu_step(s, hp, bucket_bytes)
+    torch.cuda.synchronize()
+    outs = oracle_step(grads, state, hp)
+    compare_all(s, state, outs, label=label)
+
+
+# ---------------------------------------------------------------------------
+# Element-by-element parity
+# ---------------------------------------------------------------------------
+
+def test_flat_1m_r2_step1():
+    """R=2, n=1,048,576, one bucket, step 1, m=v=0: every element."""
+    w = wl.flat_1m_r2()
+    grads = wl.make_grads(2, w.n, w.grad_sigma, device=DEV)
+    master, m, v = wl.make_state(w.n, 1, w.grad_sigma, device=DEV)
+    check_full(new_slabs(grads, master, m, v), hp_of(w))
+
+
+@pytest.mark.parametrize("n", list(range(1, 65)))
+def test_small_n_r8(n):
+    check_full(new_slabs(*random_inputs(8, n, seed=n, step=3)),
+               dict(HP10, step=3), label=f"n={n} ")
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 7, 12, 16])
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 15, 17, 63, 2049])
+def test_small_n_all_r(R, n):
+    check_full(new_slabs(*random_inputs(R, n, seed=100 * R + n, step=7)),
+               dict(HP10, step=7), label=f"R={R} n={n} ")
+
+
+@pytest.mark.parametrize("R", [1, 4, 8, 16])
+def test_many_blocks_ragged_tail(R):
+    """Several grid-stride rounds over all SMs plus a 5-element tail."""
+    n = 8 * 256 * 152 * 3 + 8 * 37 + 5
+    s = new_slabs(*random_inputs(R, n, seed=R, step=5, premultiply=1024.0))
+    check_full(s, dict(HP10, step=5, grad_scale=1024.0))
+
+
+def test_bucket_cut_does_not_change_values():
+    n = 3 * 1024 * 1024 + 5
+    base = random_inputs(4, n, seed=7, step=4)
+    ref = None
+    for bb in (0, 16, 48, 4096, 1 << 20, 25 << 20):
+        s = new_slabs([g.clone() for g in base[0]], *[t.clone() for t in base[1:]])
+        gpu_step(s, dict(HP10, step=4), bucket_bytes=bb)
+        torch.cuda.synchronize()
+        got = ([f32(t) for t in (s.master, s.m, s.v)] + [u16(o) for o in s.outs])
+        if ref is None:
+            ref = got
+            grads, state, _ = host_copy(new_slabs(*base))
+            outs = oracle_step(grads, state, dict(HP10, step=4))
+            compare_all(s, state, outs, label="bucket 0 ")
+        else:
+            for a, b in zip(got, ref):
+                assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), bb
+
+
+@pytest.mark.parametrize("max_ctas", [0, 1, 7, 152])
+def test_bucket_entry_point_over_planned_buckets(max_ctas):
+    """cc_fused_dp_bucket over a planned layout, bucket by bucket."""
+    t = wl.bert_large_tensors(layers=2, hidden=256, ffn=1024, vocab=999,
+                              positions=64)
+    numel = [x[1] for x in t]
+    offsets, buckets, n_slab = oracle.plan_buckets(numel, 64 * 1024)
+    assert len(buckets) > 4
+    s = new_slabs(*random_inputs(3, n_slab, seed=11, step=2))
+    grads, state, _ = host_copy(s)
+    hp = dict(HP10, step=2)
+    for b, e in buckets:
+        capi.cc_fused_dp_bucket(s.grads, None, s.master, s.m, s.v, s.outs, n_slab,
+                                3, b, e, max_ctas=max_ctas, **hp)
+    torch.cuda.synchronize()
+    compare_all(s, state, oracle_step(grads, state, hp))
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 8, 16])
+def test_integer_gradients_sum_exactly(R):
+    n = 100_003
+    grads = wl.integer_grads(R, n, device=DEV)
+    master = torch.ones(n, device=DEV)
+    m = torch.full((n,), 7.0, device=DEV)
+    v = torch.full((n,), 3.0, device=DEV)
+    s = new_slabs(grads, master, m, v)
+    hp = dict(lr=0.0, beta1=0.0, beta2=0.0, eps=1e-8, weight_decay=0.0, step=1,
+              grad_scale=1.0)
+    gpu_step(s, hp)
+    torch.cuda.synchronize()
+    exact = sum(g.float().cpu().numpy().astype(np.int64) for g in grads)
+    assert np.array_equal(f32(s.m), exact.astype(np.float32))
+    assert np.array_equal(f32(s.v), (exact * exact).astype(np.float32))
+    # integer gradients under the normal hyper-parameters: bit-exact too
+    s2 = new_slabs(wl.integer_grads(R, n, device=DEV), *random_inputs(1, n, 3, step=10)[1:])
+    check_full(s2, HP10)
+
+
+def test_replicas_bit_identical():
+    s = new_slabs(*random_inputs(16, 1 << 20, seed=5, step=2))
+    gpu_step(s, dict(HP10, step=2))
+    torch.cuda.synchronize()
+    ref = s.outs[0].view(torch.int16)
+    for o in s.outs[1:]:
+        assert torch.equal(o.view(torch.int16), ref)
+
+
+def test_special_values_propagate_like_the_oracle():
+    vals = torch.tensor([0.0, -0.0, float("inf"), -float("inf"), float("nan"),
+                         1e-40, -1e-40, 3e38, -3e38, 1e-3, 65504.0, 2.0 ** -133],
+                        dtype=torch.float32)
+    n = 4096 + 3
+    g = torch.Generator().manual_seed(9)
+    pick = lambda: vals[torch.randint(0, vals.numel(), (n,), generator=g)]
+    grads = [pick().to(torch.bfloat16).to(DEV) for _ in range(3)]
+    master = pick().to(DEV)
+    m = pick().to(DEV)
+    v = pick().abs().to(DEV)
+    check_full(new_slabs(grads, master, m, v), dict(HP10, step=2))
+
+
+@pytest.mark.parametrize("hp", [
+    dict(lr=0.0, beta1=0.0, beta2=0.0, eps=0.0, weight_decay=0.0, step=1, grad_scale=1.0),
+    dict(lr=1e-2, beta1=0.5, beta2=0.75, eps=1e-3, weight_decay=0.5, step=1000, grad_scale=3.0),
+    dict(lr=1.5e-4, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, step=2, grad_scale=65536.0),
+])
+def test_hyper_parameter_corners(hp):
+    check_full(new_slabs(*random_inputs(4, 50_001, seed=3, step=2,
+                                        premultiply=hp["grad_scale"])), hp)
+
+
+@pytest.mark.parametrize("R,k", [(1, 2), (3, 3), (8, 4), (16, 2)])
+def test_accumulation_matches_oracle(R, k):
+    n = 200_003
+    grads0, master, m, v = random_inputs(R, n, seed=R * 10 + k, step=6)
+    s = new_slabs(grads0, master, m, v, with_acc=True)
+    hp = dict(HP10, step=6)
+    ref_acc = [np.empty(n, np.float32) for _ in range(R)]
+    for j in range(k - 1):
+        gj = [t for t in random_inputs(R, n, seed=1000 + j, step=1)[0]]
+        capi.cc_accumulate_local(gj, s.acc, n, R, j == 0)
+        oracle.accumulate_local([u16(t) for t in gj], ref_acc, first=(j == 0))
+    torch.cuda.synchronize()
+    for r in range(R):
+        assert_bits(f"acc[{r}]", f32(s.acc[r]), ref_acc[r], "f32")
+    grads, state, acc = host_copy(s)
+    gpu_step(s, hp, bucket_bytes=1 << 20, accum_k=k, use_acc=True)
+    torch.cuda.synchronize()
+    compare_all(s, state, oracle_step(grads, state, hp, acc=acc))
+
+
+def test_accumulation_equals_single_step_on_summed_integer_grads():
+    R, n, k = 8, 65_536 + 3, 4
+    micro = [wl.integer_grads(R, n, micro=j, device=DEV) for j in range(k)]
+    _, master, m, v = random_inputs(1, n, seed=77, step=10)
+    a = new_slabs(micro[k - 1], master.clone(), m.clone(), v.clone(), with_acc=True)
+    for j in range(k - 1):
+        capi.cc_accumulate_local(micro[j], a.acc, n, R, j == 0)
+    gpu_step(a, HP10, accum_k=k, use_acc=True)
+    summed = [sum(micro[j][r].float() for j in range(k)).to(torch.bfloat16)
+              for r in range(R)]
+    b = new_slabs(summed, master.clone(), m.clone(), v.clone())
+    gpu_step(b, HP10)
+    torch.cuda.synchronize()
+    for x, y in zip([a.master, a.m, a.v] + a.outs, [b.master, b.m, b.v] + b.outs):
+        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32
+                           else x.view(torch.int16),
+                           y.view(torch.int32) if y.dtype == torch.float32
+                           else y.view(torch.int16))
+
+
+def test_rejects_host_memory_and_short_allocations():
+    n = 4096
+    s = new_slabs(*random_inputs(2, n, seed=1))
+    host = torch.zeros(n)
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_fused_dp_step(s.grads, host, s.m, s.v, s.outs, n, 2, 0, **HP1)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    with pytest.raises(capi.CCError) as ei:   # n past the end of every slab
+        capi.cc_fused_dp_step(s.grads, s.master, s.m, s.v, s.outs, 1 << 30, 2, 0,
+                              **HP1)
+    assert ei.value.status == capi.CC_ERR_INVALID
+
+
+# ---------------------------------------------------------------------------
+# Full workload sizes, sampled elements, benchmark launch configuration
+# ---------------------------------------------------------------------------
+
+def sample_indices(n, boundaries, count, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    r = torch.randint(0, n, (count,), generator=g, device=DEV)
+    edges = []
+    for b in boundaries:
+        edges += [b - 9, b - 8, b - 1, b, b + 1, b + 7, b + 8]
+    edges += [0, 1, n - 1, n - 2, n - 9]
+    e = torch.tensor([x for x in edges if 0 <= x < n], device=DEV, dtype=torch.long)
+    return torch.unique(torch.cat([r, e]))
+
+
+def uniform_cuts(n, bucket_bytes):
+    per = max(8, bucket_bytes // 16 * 8)
+    return list(range(0, n, per))
+
+
+def check_sampled(s, hp, idx, bucket_bytes, use_acc=False, accum_k=1):
+    grads, state, acc = host_copy(s, idx)
+    gpu_step(s, hp, bucket_bytes, accum_k=accum_k, use_acc=use_acc)
+    torch.cuda.synchronize()
+    outs = oracle_step(grads, state, hp, acc=acc)
+    compare_all(s, state, outs, idx=idx)
+
+
+def test_full_size_bert_large_r8():
+    """336M parameters, R=8, 25 MiB buckets, step 10: the benchmark's step."""
+    w = wl.bert_large_r8()
+    s, offsets, n_slab = planned_workload_slabs(w)
+    cuts = uniform_cuts(n_slab, w.bucket_bytes) + offsets
+    idx = sample_indices(n_slab, cuts, 1 << 20, seed=1)
+    check_sampled(s, hp_of(w), idx, w.bucket_bytes)
+
+
+def test_full_size_gpt2_slice_r4():
+    """2.72e9 parameters (element indices past 2^31), R=4, loss scale 65536."""
+    w = wl.gpt2_slice_r4()
+    s, offsets, n_slab = planned_workload_slabs(w)
+    assert n_slab > (1 << 31)
+    cuts = uniform_cuts(n_slab, w.bucket_bytes)[::7] + offsets + [1 << 31, (1 << 31) + 8]
+    idx = sample_indices(n_slab, cuts, 1 << 20, seed=2)
+    assert (idx > (1 << 31)).sum() > 1000
+    check_sampled(s, hp_of(w), idx, w.bucket_bytes)
+
+
+def test_full_size_bert_large_accumulation_k4():
+    """k=4 on the 336M set at R=8: three local micro-steps, then the reducing
+    step, sampled against the oracle run through the same micro-steps."""
+    w = wl.bert_large_r8(accum_k=4)
+    s, offsets, n_slab = planned_workload_slabs(w, micro=0, with_acc=True)
+    idx = sample_indices(n_slab, uniform_cuts(n_slab, w.bucket_bytes) + offsets,
+                         1 << 19, seed=3)
+    ref_acc = None
+    for j in range(w.accum_k - 1):
+        if j > 0:
+            s.grads = workload_grads(w, offsets, n_slab, micro=j)
+        gj = [u16(g[idx]) for g in s.grads]
+        if ref_acc is None:
+            ref_acc = [np.empty(idx.numel(), np.float32) for _ in range(w.R)]
+        capi.cc_accumulate_local(s.grads, s.acc, n_slab, w.R, j == 0)
+        oracle.accumulate_local(gj, ref_acc, first=(j == 0))
+    torch.cuda.synchronize()
+    for r in range(w.R):
+        assert_bits(f"acc[{r}]", f32(s.acc[r][idx]), ref_acc[r], "f32")
+    s.grads = workload_grads(w, offsets, n_slab, micro=w.accum_k - 1)
+    check_sampled(s, hp_of(w), idx, w.bucket_bytes, use_acc=True, accum_k=w.accum_k)
