@@ -216,10 +216,32 @@ def test_rejects_host_memory_and_short_allocations():
     with pytest.raises(capi.CCError) as ei:
         capi.cc_fused_dp_step(s.grads, host, s.m, s.v, s.outs, n, 2, 0, **HP1)
     assert ei.value.status == capi.CC_ERR_INVALID
-    with pytest.raises(capi.CCError) as ei:   # n past the end of every slab
-        capi.cc_fused_dp_step(s.grads, s.master, s.m, s.v, s.outs, 1 << 30, 2, 0,
-                              **HP1)
-    assert ei.value.status == capi.CC_ERR_INVALID
+    # All slabs carved from one cudaMalloc allocation, master last, ending
+    # exactly at the allocation's end: n elements fit, n + 8 run 32 bytes past.
+    import ctypes
+    torch.cuda.synchronize()
+    rt = ctypes.CDLL("libcudart.so.13")
+    n = 1 << 20
+    pad = n + 64
+    total = 16 * pad + 4 * n
+    ptr = ctypes.c_void_p()
+    assert rt.cudaMalloc(ctypes.byref(ptr), ctypes.c_size_t(total)) == 0
+    try:
+        base = ptr.value
+        assert rt.cudaMemset(ctypes.c_void_p(base), 0, ctypes.c_size_t(total)) == 0
+        bf = [base + 2 * pad * i for i in range(4)]            # grads[0:2], outs[0:2]
+        fp = [base + 8 * pad + 4 * pad * i for i in range(2)]  # m, v
+        master = base + total - 4 * n
+        capi.cc_fused_dp_step(bf[:2], master, fp[0], fp[1], bf[2:], n, 2, 0,
+                              stream=0, **HP1)
+        assert rt.cudaDeviceSynchronize() == 0
+        with pytest.raises(capi.CCError) as ei:
+            capi.cc_fused_dp_step(bf[:2], master, fp[0], fp[1], bf[2:], n + 8, 2, 0,
+                                  stream=0, **HP1)
+        assert ei.value.status == capi.CC_ERR_INVALID
+    finally:
+        rt.cudaFree(ptr)
+    assert "past the end" in ei.value.reason
 
 
 # ---------------------------------------------------------------------------
