@@ -207,6 +207,22 @@ def build_workload(device, R_override=None, bucket_mib=25):
                 m=m, v=v, outs=outs)
 
 
+def build_small_workload(device, n, R=8):
+    """A flat R-replica slab of n elements with the same value recipe (one
+    bucket): the small case for profiler captures."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+
+    w = wl.bert_large_r8(bucket_bytes=0)
+    w.R, w.n, w.tensors = R, n, None
+    grads = wl.make_grads(R, n, w.grad_sigma, device=device)
+    master, m, v = wl.make_state(n, w.step, w.grad_sigma, device=device)
+    outs = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(R)]
+    torch.cuda.synchronize()
+    return dict(w=w, numel=[n], layer_of=[0], offsets=[0], buckets=[(0, n)],
+                n_slab=n, grads=grads, master=master, m=m, v=v, outs=outs)
+
+
 def step_args(wk, step):
     w = wk["w"]
     return dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps,
@@ -279,7 +295,11 @@ def run_ours(args):
     gbuild.build()
     capi.lib()
 
-    wk = build_workload(dev, bucket_mib=args.bucket_mib)
+    if args.small:
+        wk = build_small_workload(dev, args.small)
+        args.no_e2e = args.no_overlap = args.no_cpu_baseline = True
+    else:
+        wk = build_workload(dev, bucket_mib=args.bucket_mib)
     w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
     n_params = w.n
     bb = w.bucket_bytes
@@ -339,7 +359,9 @@ def run_ours(args):
             "bucket_bytes": bb, "launches_per_step": launches,
             "parallelism": f"replicas x{world} (R={R} emulated per GPU)",
             "l2": "inputs 14.8 GB per GPU, larger than the 129 MB L2: no flush",
-        },
+        } if not args.small else {
+            "workload": f"profile case: flat slab of {n_slab} elements, R={R}, one bucket",
+            "R": R, "n_slab": n_slab, "bucket_bytes": 0},
         "hbm_gbs": round(bytes_per_param * n_slab / (ms * 1e-3) / 1e9, 1),
         "hbm_pct_of_8tbs": round(100 * bytes_per_param * n_slab / (ms * 1e-3) / 8e12, 2),
         "roofline": roofline,
@@ -427,7 +449,7 @@ def run_overlap(args, wk, dev, mibs):
             ready_layers=ready, num_layers=24, gemms_per_layer=3, gemm_m=M,
             gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
             warmup=args.warmup, iters=args.overlap_iters,
-            max_ctas=args.overlap_ctas, side_priority_high=args.side_priority,
+            max_ctas=args.overlap_ctas, stream_priority=args.stream_priority,
             **step_args(wk, w.step))
         r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
         r["bucket_mib"] = mib
@@ -487,12 +509,16 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--bucket-mib", type=int, default=25)
+    p.add_argument("--small", type=int, default=0,
+                   help="profile case: a flat R=8 slab of this many elements, "
+                        "one bucket, device timing only")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-overlap", action="store_true")
     p.add_argument("--overlap-iters", type=int, default=20)
     p.add_argument("--overlap-ctas", type=int, default=0)
-    p.add_argument("--side-priority", action="store_true")
+    p.add_argument("--stream-priority", type=int, default=0, choices=(0, 1, 2),
+                   help="overlap: 0 equal, 1 side stream high, 2 compute high")
     p.add_argument("--sweep", action="store_true",
                    help="also run the 1/4/25/100/500 MiB bucket sweep")
     p.add_argument("--no-cpu-baseline", action="store_true")

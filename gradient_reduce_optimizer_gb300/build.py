@@ -57,14 +57,19 @@ def _stale(target: str, deps: List[str]) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False,
-          extra_flags: List[str] = ()) -> str:
-    """Compile (if stale) and link the library; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+          extra_flags: List[str] = (), build_dir: str = BUILD_DIR,
+          library: str = LIBRARY) -> str:
+    """Compile (if stale) and link the library; returns its path.
+
+    ``extra_flags`` (e.g. ``-DCC_DP_THREADS=512``) go to every nvcc call;
+    give such builds their own ``build_dir`` and ``library`` path.
+    """
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     objs, procs = [], []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [path, *HEADERS]):
             cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", path, "-o", obj]
@@ -83,15 +88,15 @@ def build(force: bool = False, verbose: bool = False,
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    if force or procs or _stale(LIBRARY, objs):
+    if force or procs or _stale(library, objs):
         rpath = ":".join(cuda_lib_dirs())
-        tmp = LIBRARY + ".tmp"
+        tmp = library + ".tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
                "-lcublas", f"-Xlinker=-rpath={rpath}"]
         cmd += [f"-L{d}" for d in cuda_lib_dirs()]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIBRARY)
-    return LIBRARY
+        os.replace(tmp, library)
+    return library
 
 
 if __name__ == "__main__":

@@ -206,7 +206,7 @@ int run_step(const Slabs &s, const AdamScalars &c, size_t n, size_t bucket_bytes
     const size_t per = bucket_elems(bucket_bytes, n);
     for (size_t b = 0; b < n; b += per) {
         const size_t e = std::min(n, b + per);
-        const cudaError_t err = launch_fused(s, c, b, e, 0, stream);
+        const cudaError_t err = launch_fused(s, c, b, e, 0, /*chain=*/b > 0, stream);
         if (err != cudaSuccess) return fail_cuda(err, "fused step launch");
     }
     return CC_OK;
@@ -287,7 +287,7 @@ int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
     st = validate_slabs(grads, acc, master, m, v, params_out, n, R, acc != nullptr, &s);
     if (st != CC_OK) return st;
     const cudaError_t e =
-        launch_fused(s, c, begin, end, max_ctas, static_cast<cudaStream_t>(stream));
+        launch_fused(s, c, begin, end, max_ctas, false, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused bucket launch");
 }
 

@@ -35,8 +35,12 @@ struct Slabs {
 // Enqueue the fused reduce + AdamW + redistribute kernel over elements
 // [begin, end) on `stream`.  Requires begin % CC_PAD_ELEMS == 0 and 16-byte
 // aligned slab bases (checked by the caller).  max_ctas > 0 caps the grid.
+// chain = true launches it as a programmatic dependent of the kernel just
+// before it on `stream`, which must be a fused-step launch on a disjoint
+// element range (the next bucket of the same step).
 cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
-                         size_t end, int max_ctas, cudaStream_t stream);
+                         size_t end, int max_ctas, bool chain,
+                         cudaStream_t stream);
 
 // Enqueue one local accumulation micro-step over [0, n).
 cudaError_t launch_accumulate(const void *const *grads, float *const *acc,

@@ -83,7 +83,7 @@ struct Bench {
             if (wait_ready) e = cudaStreamWaitEvent(s, res.layer[cfg.bucket_ready_layer[b]], 0);
             if (e == cudaSuccess)
                 e = launch_fused(slabs, scalars, cfg.bucket_begin[b], cfg.bucket_end[b],
-                                 max_ctas, s);
+                                 max_ctas, /*chain=*/!wait_ready && b > 0, s);
             if (e != cudaSuccess) return fail_cuda(e, "bucket launch");
         }
         return CC_OK;
@@ -157,6 +157,8 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     if (c.iters < 1 || c.iters > 1000 || c.warmup < 0 || c.warmup > 1000)
         return fail(CC_ERR_INVALID, "iters=%d must be in 1..1000, warmup in 0..1000", c.iters);
     if (c.max_ctas < 0) return fail(CC_ERR_INVALID, "max_ctas=%d must be >= 0", c.max_ctas);
+    if (c.stream_priority < 0 || c.stream_priority > 2)
+        return fail(CC_ERR_INVALID, "stream_priority=%d must be 0, 1 or 2", c.stream_priority);
     if (c.num_buckets < 1 || !c.bucket_begin || !c.bucket_end || !c.bucket_ready_layer)
         return fail(CC_ERR_INVALID, "need at least one bucket");
     for (int b = 0; b < c.num_buckets; ++b) {
@@ -192,10 +194,12 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     int lo = 0, hi = 0;
     if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess)
         return fail_cuda(e, "priority range");
-    if ((e = cudaStreamCreateWithPriority(&res.comp, cudaStreamNonBlocking, lo)) != cudaSuccess)
+    // Larger numbers are lower priorities: lo is the default, hi the top.
+    if ((e = cudaStreamCreateWithPriority(&res.comp, cudaStreamNonBlocking,
+                                          c.stream_priority == 2 ? hi : lo)) != cudaSuccess)
         return fail_cuda(e, "compute stream");
     if ((e = cudaStreamCreateWithPriority(&res.side, cudaStreamNonBlocking,
-                                          c.side_priority_high ? hi : lo)) != cudaSuccess)
+                                          c.stream_priority == 1 ? hi : lo)) != cudaSuccess)
         return fail_cuda(e, "side stream");
     if ((e = cudaEventCreate(&res.start)) != cudaSuccess ||
         (e = cudaEventCreate(&res.stop)) != cudaSuccess ||

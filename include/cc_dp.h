@@ -260,7 +260,7 @@ typedef struct cc_overlap_cfg {
     void *gemm_a, *gemm_b, *gemm_c;  /* bf16 device buffers */
     int warmup, iters;             /* iters in 1..1000 */
     int max_ctas;                  /* bucket kernels' CTA cap while overlapped; 0 = full */
-    int side_priority_high;        /* nonzero: side stream at the highest priority */
+    int stream_priority;           /* 0: equal; 1: side stream high; 2: compute stream high */
 } cc_overlap_cfg;
 
 typedef struct cc_overlap_result {
