@@ -43,8 +43,8 @@ if ROOT not in sys.path:
 METRIC = "fused DP step params/s and HBM GB/s (% of ~8 TB/s) at R=8; exposed ms/step"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCE = os.path.join(ROOT, "gradient_reduce_optimizer_gb300", "csrc",
-                             "cc_dp_kernels.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "gradient_reduce_optimizer_gb300", "csrc", f)
+                  for f in ("cc_dp_kernels.cu", "cc_dp_device.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_step_kernel_traffic.json")
 
 
@@ -105,8 +105,11 @@ def measured_hbm_peak():
 
 
 def kernel_sha() -> str:
-    with open(KERNEL_SOURCE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic_per_param(R: int):
@@ -229,6 +232,12 @@ def step_args(wk, step):
                 weight_decay=w.weight_decay, step=step, grad_scale=w.grad_scale)
 
 
+def uniform_buckets(n_slab, bucket_bytes):
+    """The cut cc_fused_dp_step makes: floor(bucket_bytes/16)*8 elements."""
+    per = max(8, bucket_bytes // 16 * 8) if bucket_bytes else n_slab
+    return [(b, min(n_slab, b + per)) for b in range(0, n_slab, per)]
+
+
 def launches_per_step(n_slab, bucket_bytes):
     per = max(8, bucket_bytes // 16 * 8) if bucket_bytes else n_slab
     return (n_slab + per - 1) // per
@@ -305,10 +314,20 @@ def run_ours(args):
     bb = w.bucket_bytes
     stream = torch.cuda.current_stream()
 
+    cuts = uniform_buckets(n_slab, bb)
+
     def one_step(step):
-        capi.cc_fused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"],
-                              wk["outs"], n_slab, R, bb, stream=stream,
-                              **step_args(wk, step))
+        if args.engine_ctas > 0:
+            # the bulk-copy engine on a budget of SMs, bucket by bucket
+            for b, e in cuts:
+                capi.cc_fused_dp_bucket(wk["grads"], None, wk["master"], wk["m"],
+                                        wk["v"], wk["outs"], n_slab, R, b, e,
+                                        max_ctas=args.engine_ctas, stream=stream,
+                                        **step_args(wk, step))
+        else:
+            capi.cc_fused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"],
+                                  wk["outs"], n_slab, R, bb, stream=stream,
+                                  **step_args(wk, step))
 
     for i in range(args.warmup):
         one_step(w.step + i)
@@ -336,13 +355,14 @@ def run_ours(args):
     launch_ms = ms_local / launches           # launches run back to back
     achieved = bytes_per_param * per_launch_elems / (launch_ms * 1e-3) / 1e9
     peak, peak_src = measured_hbm_peak()
-    tpp = profiled_traffic_per_param(R)
+    tpp = profiled_traffic_per_param(R) if args.engine_ctas == 0 else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": (round(tpp * per_launch_elems) if tpp else None),
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": round(bytes_per_param * per_launch_elems),
-                "kernel": f"fused_step_kernel<R={R}>",
+                "kernel": (f"fused_step_bulk_kernel<R={R}> on {args.engine_ctas} SMs"
+                           if args.engine_ctas > 0 else f"fused_step_kernel<R={R}>"),
                 "launches_per_step": launches}
 
     result = {
@@ -509,6 +529,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--bucket-mib", type=int, default=25)
+    p.add_argument("--engine-ctas", type=int, default=0,
+                   help="run each bucket on the bulk-copy engine with this many "
+                        "SMs (cc_fused_dp_bucket max_ctas); 0 = the plain kernel")
     p.add_argument("--small", type=int, default=0,
                    help="profile case: a flat R=8 slab of this many elements, "
                         "one bucket, device timing only")

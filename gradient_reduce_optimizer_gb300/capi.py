@@ -82,6 +82,7 @@ _SIGNATURES = {
     "cc_overlap_bench": ([ctypes.POINTER(cc_overlap_cfg),
                           ctypes.POINTER(cc_overlap_result)], _i),
     "cc_l2_flush": ([_vp, _sz, _vp], _i),
+    "cc_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
 }
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -257,6 +258,14 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
     _check(lib().cc_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
            "cc_overlap_bench")
     return {name: getattr(res, name) for name, _ in res._fields_}
+
+
+def cc_device_status(clear: bool = False) -> int:
+    """The bulk engine's status word (0 = no wait ever ran out)."""
+    st = ctypes.c_uint(0)
+    _check(lib().cc_device_status(ctypes.byref(st), int(bool(clear))),
+           "cc_device_status")
+    return st.value
 
 
 def cc_l2_flush(buf, nbytes: int, stream=None) -> None:

@@ -287,7 +287,7 @@ int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
     st = validate_slabs(grads, acc, master, m, v, params_out, n, R, acc != nullptr, &s);
     if (st != CC_OK) return st;
     const cudaError_t e =
-        launch_fused(s, c, begin, end, max_ctas, false, static_cast<cudaStream_t>(stream));
+        launch_step_range(s, c, begin, end, max_ctas, false, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused bucket launch");
 }
 
@@ -395,6 +395,14 @@ int cc_bucket_ready_layers(const size_t *numel, const int *layer_of,
     for (int b = 0; b < num_buckets; ++b)
         if (ready_layer_out[b] < 0) return fail(CC_ERR_INVALID, "bucket %d holds no tensor", b);
     return CC_OK;
+}
+
+int cc_device_status(unsigned *status, int clear) {
+    if (!status) return fail(CC_ERR_INVALID, "status is NULL");
+    int st = ensure_device();
+    if (st != CC_OK) return st;
+    const cudaError_t e = read_bulk_status(status, clear != 0);
+    return e == cudaSuccess ? CC_OK : fail_cuda(e, "status read");
 }
 
 int cc_l2_flush(void *buf, size_t bytes, void *stream) {

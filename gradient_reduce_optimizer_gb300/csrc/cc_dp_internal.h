@@ -42,6 +42,29 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
                          size_t end, int max_ctas, bool chain,
                          cudaStream_t stream);
 
+// Enqueue the bulk-copy engine of the same step over [begin, end) on at most
+// num_ctas SMs (one persistent CTA per SM; 0 = every SM).  Same arithmetic
+// and requirements as launch_fused.
+cudaError_t launch_fused_bulk(const Slabs &s, const AdamScalars &c, size_t begin,
+                              size_t end, int num_ctas, cudaStream_t stream);
+
+// The fused step over [begin, end) with the engine a CTA budget calls for:
+// max_ctas > 0 runs the bulk-copy engine on that many SMs, 0 the plain
+// kernel over the whole GPU (chained to the previous bucket if `chain`).
+inline cudaError_t launch_step_range(const Slabs &s, const AdamScalars &c, size_t begin,
+                                     size_t end, int max_ctas, bool chain,
+                                     cudaStream_t stream) {
+    return max_ctas > 0 ? launch_fused_bulk(s, c, begin, end, max_ctas, stream)
+                        : launch_fused(s, c, begin, end, 0, chain, stream);
+}
+
+// Read (and optionally clear) the bulk engine's status word: 0, or codes of
+// waits that ran out (1 consumer, 2 producer, 4 drain).  Synchronous.
+cudaError_t read_bulk_status(unsigned *status, bool clear);
+
+// Multiprocessor count of the current device (queried once per device).
+cudaError_t device_sm_count(int *count);
+
 // Enqueue one local accumulation micro-step over [0, n).
 cudaError_t launch_accumulate(const void *const *grads, float *const *acc,
                               int R, size_t n, bool first,

@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "cc_dp_device.cuh"
 #include "cc_dp_internal.h"
 
 // Launch shape (compile-time tuning parameters).
@@ -57,6 +58,8 @@
 namespace ccdp {
 namespace {
 
+using namespace dev;
+
 constexpr int kThreads = CC_DP_THREADS;
 
 struct FusedParams {
@@ -70,46 +73,6 @@ struct FusedParams {
     size_t tail_begin;             // first element of the partial vector
     int tail_len;                  // 0..7 elements after the full vectors
 };
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) {
-    return __uint_as_float(w << 16);
-}
-__device__ __forceinline__ float bf16_hi(uint32_t w) {
-    return __uint_as_float(w & 0xFFFF0000u);
-}
-__device__ __forceinline__ float bf16_at(const void *base, size_t i) {
-    const unsigned short h = static_cast<const unsigned short *>(base)[i];
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
-}
-
-__device__ __forceinline__ void widen8(const uint4 q, float t[8]) {
-    t[0] = bf16_lo(q.x); t[1] = bf16_hi(q.x);
-    t[2] = bf16_lo(q.y); t[3] = bf16_hi(q.y);
-    t[4] = bf16_lo(q.z); t[5] = bf16_hi(q.z);
-    t[6] = bf16_lo(q.w); t[7] = bf16_hi(q.w);
-}
-
-// Two fp32 -> bf16x2, round to nearest even; a lands in the low half.
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-// One AdamW step on one element, given the reduced gradient s.
-__device__ __forceinline__ void adamw(float s, float &p, float &m, float &v,
-                                      const AdamScalars &c) {
-    const float g = __fmul_rn(s, c.inv_scale);
-    const float m_new = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.one_minus_b1, g));
-    const float v_new = __fadd_rn(__fmul_rn(c.beta2, v),
-                                  __fmul_rn(c.one_minus_b2, __fmul_rn(g, g)));
-    const float m_hat = __fdiv_rn(m_new, c.bias_corr1);
-    const float v_hat = __fdiv_rn(v_new, c.bias_corr2);
-    const float denom = __fadd_rn(__fsqrt_rn(v_hat), c.eps);
-    const float update = __fmul_rn(c.lr, __fdiv_rn(m_hat, denom));
-    p = __fsub_rn(__fmul_rn(p, c.decay), update);
-    m = m_new;
-    v = v_new;
-}
 
 template <int R, bool ACC>
 __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
@@ -130,25 +93,26 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     const float4 v0 = __ldcs(p.v + 2 * vi), v1 = __ldcs(p.v + 2 * vi + 1);
 
     // Reduce in replica order.
-    float s[8], t[8];
-    widen8(gq[0], s);
+    float s[8];
     if constexpr (ACC) {
-        const float a0[8] = {aq[0][0].x, aq[0][0].y, aq[0][0].z, aq[0][0].w,
-                             aq[0][1].x, aq[0][1].y, aq[0][1].z, aq[0][1].w};
+        float a0[8] = {aq[0][0].x, aq[0][0].y, aq[0][0].z, aq[0][0].w,
+                       aq[0][1].x, aq[0][1].y, aq[0][1].z, aq[0][1].w};
+        add8_bf16(a0, gq[0]);                      // acc[0] + g[0]
 #pragma unroll
-        for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(a0[k], s[k]);
+        for (int k = 0; k < 8; ++k) s[k] = a0[k];
+    } else {
+        widen8(gq[0], s);
     }
 #pragma unroll
     for (int r = 1; r < R; ++r) {
-        widen8(gq[r], t);
         if constexpr (ACC) {
-            const float ar[8] = {aq[r][0].x, aq[r][0].y, aq[r][0].z, aq[r][0].w,
-                                 aq[r][1].x, aq[r][1].y, aq[r][1].z, aq[r][1].w};
+            float ar[8] = {aq[r][0].x, aq[r][0].y, aq[r][0].z, aq[r][0].w,
+                           aq[r][1].x, aq[r][1].y, aq[r][1].z, aq[r][1].w};
+            add8_bf16(ar, gq[r]);                  // acc[r] + g[r]
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], __fadd_rn(ar[k], t[k]));
+            for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], ar[k]);
         } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) s[k] = __fadd_rn(s[k], t[k]);
+            add8_bf16(s, gq[r]);
         }
     }
 
@@ -348,6 +312,13 @@ cudaError_t device_info(DeviceInfo **out) {
 size_t div_up(size_t a, size_t b) { return (a + b - 1) / b; }
 
 }  // namespace
+
+cudaError_t device_sm_count(int *count) {
+    DeviceInfo *d = nullptr;
+    const cudaError_t e = device_info(&d);
+    if (e == cudaSuccess) *count = d->sm_count;
+    return e;
+}
 
 cudaError_t check_device(int *major, int *minor) {
     DeviceInfo *d = nullptr;

@@ -82,8 +82,8 @@ struct Bench {
             cudaError_t e = cudaSuccess;
             if (wait_ready) e = cudaStreamWaitEvent(s, res.layer[cfg.bucket_ready_layer[b]], 0);
             if (e == cudaSuccess)
-                e = launch_fused(slabs, scalars, cfg.bucket_begin[b], cfg.bucket_end[b],
-                                 max_ctas, /*chain=*/!wait_ready && b > 0, s);
+                e = launch_step_range(slabs, scalars, cfg.bucket_begin[b], cfg.bucket_end[b],
+                                      max_ctas, /*chain=*/!wait_ready && b > 0, s);
             if (e != cudaSuccess) return fail_cuda(e, "bucket launch");
         }
         return CC_OK;

@@ -163,8 +163,12 @@ CC_API int cc_fused_dp_step_accum(const void *const *grads, const float *const *
  * bucket's gradients become ready (DDP bucketing, Communication Overlap).
  * Slab pointers and n describe the whole slabs, as for cc_fused_dp_step_accum
  * (acc may be NULL).  begin must be a multiple of CC_PAD_ELEMS (else
- * CC_ERR_MISALIGNED) and begin <= end <= n.  max_ctas > 0 caps the grid (a
- * CTA budget that leaves SMs to concurrent compute); 0 = fill the GPU.
+ * CC_ERR_MISALIGNED) and begin <= end <= n.
+ *   max_ctas  0: the plain kernel over the whole GPU.  > 0: a CTA budget that
+ *             leaves SMs to concurrent compute -- the bulk-copy engine runs
+ *             one persistent CTA on each of at most max_ctas SMs, streaming
+ *             tiles through shared memory with cp.async.bulk so that few SMs
+ *             reach HBM bandwidth.  Same values either way.
  */
 CC_API int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
                        float *master, float *m, float *v,
@@ -270,6 +274,16 @@ typedef struct cc_overlap_result {
 } cc_overlap_result;
 
 CC_API int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out);
+
+/*
+ * cc_device_status -- the bulk-copy engine's status word on the current
+ * device: 0, or an or of codes of pipeline waits that ran out (each wait is
+ * bounded to one second, after which the kernel abandons its pipeline and
+ * returns instead of hanging): 1 consumer, 2 producer, 4 drain of copies in
+ * flight.  A non-zero word means some bulk-engine launch did not finish its
+ * range.  Synchronises with the device; clear != 0 resets the word.
+ */
+CC_API int cc_device_status(unsigned *status, int clear);
 
 /*
  * cc_l2_flush -- overwrite `bytes` of the caller's device buffer `buf`

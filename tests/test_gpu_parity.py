@@ -314,3 +314,77 @@ def test_full_size_bert_large_accumulation_k4():
         assert_bits(f"acc[{r}]", f32(s.acc[r][idx]), ref_acc[r], "f32")
     s.grads = workload_grads(w, offsets, n_slab, micro=w.accum_k - 1)
     check_sampled(s, hp_of(w), idx, w.bucket_bytes, use_acc=True, accum_k=w.accum_k)
+
+
+# ---------------------------------------------------------------------------
+# The bulk-copy engine (a CTA budget: cc_fused_dp_bucket with max_ctas > 0)
+# ---------------------------------------------------------------------------
+
+def bulk_step(s, hp, max_ctas, begin=0, end=None, use_acc=False):
+    end = s.n if end is None else end
+    capi.cc_fused_dp_bucket(s.grads, s.acc if use_acc else None, s.master, s.m, s.v,
+                            s.outs, s.n, s.R, begin, end, max_ctas=max_ctas, **hp)
+
+
+def check_bulk(s, hp, max_ctas, use_acc=False, label=""):
+    grads, state, acc = host_copy(s)
+    bulk_step(s, hp, max_ctas, use_acc=use_acc)
+    torch.cuda.synchronize()
+    outs = oracle_step(grads, state, hp, acc=acc if use_acc else None)
+    compare_all(s, state, outs, label=label)
+    assert capi.cc_device_status() == 0
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 1023, 1024, 1025, 4096 + 3, 300_007])
+@pytest.mark.parametrize("R", [1, 3, 8, 16])
+def test_bulk_engine_ragged(R, n):
+    s = new_slabs(*random_inputs(R, n, seed=500 + R * 7 + n % 97, step=4))
+    check_bulk(s, dict(HP10, step=4), max_ctas=5, label=f"bulk R={R} n={n} ")
+
+
+@pytest.mark.parametrize("R", [1, 2, 8, 16])
+@pytest.mark.parametrize("max_ctas", [1, 3, 152, 1000])
+def test_bulk_engine_accumulators(R, max_ctas):
+    """With accumulators the tile shrinks to 512 (R=8) or 256 (R=16)."""
+    n = 100_003
+    s = new_slabs(*random_inputs(R, n, seed=R + max_ctas, step=3), with_acc=True)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(17)
+    for a in s.acc:
+        a.copy_(torch.randn(n, generator=g, device=DEV) * 1e-3)
+    check_bulk(s, dict(HP10, step=3), max_ctas, use_acc=True)
+
+
+def test_bulk_engine_subrange_leaves_the_rest_untouched():
+    n = 50_000
+    s = new_slabs(*random_inputs(4, n, seed=99, step=2))
+    before = [t.clone() for t in (s.master, s.m, s.v)] + [o.clone() for o in s.outs]
+    grads, state, _ = host_copy(s)
+    b, e = 8 * 1000, 8 * 4000 + 5
+    bulk_step(s, dict(HP10, step=2), 7, begin=b, end=e)
+    torch.cuda.synchronize()
+    sub = [x[b:e].copy() for x in state]
+    outs = oracle_step([g_[b:e].copy() for g_ in grads], sub, dict(HP10, step=2))
+    idx = torch.arange(b, e, device=DEV)
+    compare_all(s, sub, outs, idx=idx)
+    after = [s.master, s.m, s.v] + s.outs
+    for x, y in zip(after, before):
+        xb = x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32)
+        yb = y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32)
+        assert torch.equal(xb[:b], yb[:b]) and torch.equal(xb[e:], yb[e:])
+    assert capi.cc_device_status() == 0
+
+
+def test_full_size_bert_large_r8_bulk_engine():
+    """The 336M R=8 slab in its planned buckets on a 64-SM budget."""
+    w = wl.bert_large_r8()
+    s, offsets, n_slab = planned_workload_slabs(w)
+    _, buckets, _ = oracle.plan_buckets(w.numel(), w.bucket_bytes)
+    idx = sample_indices(n_slab, [b for b, _ in buckets] + offsets, 1 << 20, seed=4)
+    grads, state, _ = host_copy(s, idx)
+    for b, e in buckets:
+        capi.cc_fused_dp_bucket(s.grads, None, s.master, s.m, s.v, s.outs, n_slab,
+                                w.R, b, e, max_ctas=64, **hp_of(w))
+    torch.cuda.synchronize()
+    compare_all(s, state, oracle_step(grads, state, hp_of(w)), idx=idx)
+    assert capi.cc_device_status() == 0
