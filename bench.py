@@ -393,8 +393,18 @@ def run_ours(args):
         result["e2e"] = run_e2e(args, wk, stream, world, dev)
     if not args.no_overlap:
         result["overlap"] = run_overlap(args, wk, dev, [args.bucket_mib])
-        if args.sweep:
-            result["overlap_sweep"] = run_overlap(args, wk, dev, [1, 4, 25, 100, 500])
+        result["overlap_rank_share"] = run_overlap(args, wk, dev, [args.bucket_mib],
+                                                   rank_share=True)
+        if not args.no_sweep:
+            keep = ("bucket_mib", "num_buckets", "t_bwd_ms", "t_comm_ms",
+                    "t_step_overlap_ms", "t_step_seq_ms", "exposed_ms",
+                    "exposed_bound_ms")
+            sweep = {}
+            for share in (False, True):
+                rows = run_overlap(args, wk, dev, [1, 4, 25, 100, 500], rank_share=share)
+                sweep["rank_share" if share else "all_replicas"] = [
+                    {k: r[k] for k in keep} for r in rows]
+            result["overlap_sweep"] = sweep
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, passes, el = time_oracle(R, args.cpu_sample, 10.0, 30.0)
         result["cpu_baseline"] = {
@@ -445,9 +455,26 @@ def run_e2e(args, wk, stream, world, dev):
             "ms_per_step": round(ms, 3), "steps": steps}
 
 
-def run_overlap(args, wk, dev, mibs):
+def shard_range(begin, end, count, index):
+    """Shard `index` of `count` of the bucket [begin, end), cut in 8-element
+    units (sizes differ by at most 8 elements): the part of a bucket one
+    rank reduces and updates in the sharded (ReduceScatter-optimizer-
+    AllGather) form of the step."""
+    units = (end - begin) // 8
+    lo = begin + 8 * (units * index // count)
+    hi = begin + 8 * (units * (index + 1) // count) if index + 1 < count else end
+    return lo, hi
+
+
+def run_overlap(args, wk, dev, mibs, rank_share=False):
     """Exposed time of the bucketed step behind a proxy backward of 24 layers
-    x 3 bf16 GEMMs (M=8192, N=K=1024); buckets planned at each size."""
+    x 3 bf16 GEMMs (M=8192, N=K=1024); buckets planned at each size.
+
+    rank_share=False: one GPU carries all R replicas' traffic (the emulated
+    step).  rank_share=True: one rank's share of the sharded step -- each
+    bucket shrinks to rank 0's 1/R shard: it reads the R replicas' gradients
+    of the shard, updates the shard's master/m/v and writes the shard's
+    parameters to all R replica slabs, (4 + 24/R) bytes per parameter."""
     import torch
     from gradient_reduce_optimizer_gb300 import capi
 
@@ -463,6 +490,10 @@ def run_overlap(args, wk, dev, mibs):
         offsets, buckets, n_slab = capi.cc_plan_buckets(wk["numel"], mib << 20)
         assert n_slab == wk["n_slab"] and offsets == wk["offsets"]
         ready = capi.cc_bucket_ready_layers(wk["numel"], wk["layer_of"], offsets, buckets)
+        if rank_share:
+            pairs = [(shard_range(b, e, w.R, 0), rl) for (b, e), rl in zip(buckets, ready)]
+            pairs = [(br, rl) for br, rl in pairs if br[1] > br[0]]
+            buckets, ready = [br for br, _ in pairs], [rl for _, rl in pairs]
         r = capi.cc_overlap_bench(
             grads=wk["grads"], master=wk["master"], m=wk["m"], v=wk["v"],
             params_out=wk["outs"], n=n_slab, R=w.R, buckets=buckets,
@@ -473,6 +504,7 @@ def run_overlap(args, wk, dev, mibs):
             **step_args(wk, w.step))
         r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
         r["bucket_mib"] = mib
+        r["mode"] = "rank share (1/R of each bucket)" if rank_share else "all R replicas"
         r["exposed_pct_of_bwd"] = round(100 * r["exposed_ms"] / r["t_bwd_ms"], 1)
         r["bwd_tflops"] = round(24 * 3 * 2 * M * N * K / (r["t_bwd_ms"] * 1e-3) / 1e12, 1)
         out.append(r)
@@ -540,10 +572,10 @@ def parse_args(argv=None):
     p.add_argument("--no-overlap", action="store_true")
     p.add_argument("--overlap-iters", type=int, default=20)
     p.add_argument("--overlap-ctas", type=int, default=0)
-    p.add_argument("--stream-priority", type=int, default=0, choices=(0, 1, 2),
+    p.add_argument("--stream-priority", type=int, default=2, choices=(0, 1, 2),
                    help="overlap: 0 equal, 1 side stream high, 2 compute high")
-    p.add_argument("--sweep", action="store_true",
-                   help="also run the 1/4/25/100/500 MiB bucket sweep")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the 1/4/25/100/500 MiB bucket-size sweep")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1 << 22)
     p.add_argument("--ref-sample", type=int, default=1 << 20)
