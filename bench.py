@@ -389,6 +389,8 @@ def run_ours(args):
         "gpu_launches": launches * args.steps,
     }
 
+    if not args.no_unfused and not args.small:
+        result["unfused"] = run_unfused(args, wk, stream, ms)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wk, stream, world, dev)
     if not args.no_overlap:
@@ -414,6 +416,44 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(result), flush=True)
     return result
+
+
+def run_unfused(args, wk, stream, fused_ms):
+    """The same step in the unfused schedule (reduce into a workspace, AdamW,
+    broadcast copies): the separate-kernel baseline the fused step is
+    compared against.  Same workload, buckets and timing rules."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
+    bb = w.bucket_bytes
+    per = max(8, bb // 16 * 8) if bb else n_slab
+    ws = torch.empty(min(per, n_slab), dtype=torch.float32, device=wk["master"].device)
+
+    def step(i):
+        capi.cc_unfused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"],
+                                wk["outs"], ws, ws.numel() * 4, n_slab, R, bb,
+                                stream=stream, **step_args(wk, w.step + i))
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 100))
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    buckets = launches_per_step(n_slab, bb)
+    return {"ms_per_step": round(ms, 4), "value": round(w.n / (ms * 1e-3)),
+            "unit": UNIT, "steps": steps,
+            "bytes_per_param": 6 * R + 30,
+            "hbm_gbs": round((6 * R + 30) * n_slab / (ms * 1e-3) / 1e9, 1),
+            "launches_per_step": buckets * 2, "copies_per_step": buckets * (R - 1),
+            "fused_speedup": round(ms / fused_ms, 3)}
 
 
 def run_e2e(args, wk, stream, world, dev):
@@ -568,6 +608,8 @@ def parse_args(argv=None):
                    help="profile case: a flat R=8 slab of this many elements, "
                         "one bucket, device timing only")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-unfused", action="store_true",
+                   help="skip timing the unfused (reduce, AdamW, copies) schedule")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-overlap", action="store_true")
     p.add_argument("--overlap-iters", type=int, default=20)

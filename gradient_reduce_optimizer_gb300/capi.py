@@ -83,6 +83,8 @@ _SIGNATURES = {
                           ctypes.POINTER(cc_overlap_result)], _i),
     "cc_l2_flush": ([_vp, _sz, _vp], _i),
     "cc_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
+    "cc_unfused_dp_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _sz, _i, _sz,
+                            _f, _f, _f, _f, _f, _i, _f, _vp], _i),
 }
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -179,6 +181,18 @@ def cc_fused_dp_bucket(grads, acc, master, m, v, params_out, n: int, R: int,
         _addr(v), _addr_array(params_out), n, R, begin, end, lr, beta1, beta2,
         eps, weight_decay, step, grad_scale, max_ctas, _stream(stream)),
         "cc_fused_dp_bucket")
+
+
+def cc_unfused_dp_step(grads, master, m, v, params_out, workspace,
+                       workspace_bytes: int, n: int, R: int, bucket_bytes: int,
+                       lr: float, beta1: float, beta2: float, eps: float,
+                       weight_decay: float, step: int, grad_scale: float,
+                       stream=None) -> None:
+    _check(lib().cc_unfused_dp_step(
+        _addr_array(grads), _addr(master), _addr(m), _addr(v),
+        _addr_array(params_out), _addr(workspace), workspace_bytes, n, R,
+        bucket_bytes, lr, beta1, beta2, eps, weight_decay, step, grad_scale,
+        _stream(stream)), "cc_unfused_dp_step")
 
 
 def cc_accumulate_local(grads, acc, n: int, R: int, first: bool,

@@ -397,6 +397,49 @@ int cc_bucket_ready_layers(const size_t *numel, const int *layer_of,
     return CC_OK;
 }
 
+int cc_unfused_dp_step(const void *const *grads, float *master, float *m, float *v,
+                       void *const *params_out, float *workspace, size_t workspace_bytes,
+                       size_t n, int R, size_t bucket_bytes, float lr, float beta1,
+                       float beta2, float eps, float weight_decay, int step,
+                       float grad_scale, void *stream) {
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    AdamScalars c;
+    int st = make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
+    if (st != CC_OK) return st;
+    if (n == 0) return CC_OK;
+    const size_t per = bucket_elems(bucket_bytes, n);
+    const size_t need = 4 * (per < n ? per : n);
+    if (!workspace) return fail(CC_ERR_INVALID, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return fail(CC_ERR_MISALIGNED, "workspace=%p is not 16-byte aligned", workspace);
+    if (workspace_bytes < need)
+        return fail(CC_ERR_INVALID, "workspace of %zu bytes, the largest bucket needs %zu",
+                    workspace_bytes, need);
+    // The workspace is written: it may overlap no slab.
+    const uintptr_t wlo = reinterpret_cast<uintptr_t>(workspace), whi = wlo + need;
+    auto hits = [&](const void *p, size_t bytes) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        return p && lo < whi && wlo < lo + bytes;
+    };
+    if (!grads || !params_out) return fail(CC_ERR_INVALID, "grads/params_out arrays are NULL");
+    for (int r = 0; r < R; ++r)
+        if (hits(grads[r], 2 * n) || hits(params_out[r], 2 * n))
+            return fail(CC_ERR_ALIAS, "workspace overlaps replica %d's slabs", r);
+    if (hits(master, 4 * n) || hits(m, 4 * n) || hits(v, 4 * n))
+        return fail(CC_ERR_ALIAS, "workspace overlaps master/m/v");
+    Slabs s;
+    st = validate_slabs(grads, nullptr, master, m, v, params_out, n, R, false, &s);
+    if (st != CC_OK) return st;
+    if ((st = check_device_range(workspace, need, "workspace")) != CC_OK) return st;
+    for (size_t b = 0; b < n; b += per) {
+        const size_t e = std::min(n, b + per);
+        const cudaError_t err = launch_unfused_bucket(s, c, workspace, b, e,
+                                                      static_cast<cudaStream_t>(stream));
+        if (err != cudaSuccess) return fail_cuda(err, "unfused step launch");
+    }
+    return CC_OK;
+}
+
 int cc_device_status(unsigned *status, int clear) {
     if (!status) return fail(CC_ERR_INVALID, "status is NULL");
     int st = ensure_device();

@@ -58,6 +58,15 @@ inline cudaError_t launch_step_range(const Slabs &s, const AdamScalars &c, size_
                         : launch_fused(s, c, begin, end, 0, chain, stream);
 }
 
+// Enqueue the unfused schedule of one bucket: reduce into `workspace`
+// (fp32, at least end - begin elements), AdamW from it, then R-1 copies of
+// replica 0's parameters.  Same values as launch_fused.
+cudaError_t launch_unfused_bucket(const Slabs &s, const AdamScalars &c, float *workspace,
+                                  size_t begin, size_t end, cudaStream_t stream);
+
+// Elements per bucket for a bf16 byte size (0 = the whole slab).
+size_t bucket_elems(size_t bucket_bytes, size_t n);
+
 // Read (and optionally clear) the bulk engine's status word: 0, or codes of
 // waits that ran out (1 consumer, 2 producer, 4 drain).  Synchronous.
 cudaError_t read_bulk_status(unsigned *status, bool clear);

@@ -178,6 +178,31 @@ CC_API int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
                        float grad_scale, int max_ctas, void *stream);
 
 /*
+ * cc_unfused_dp_step -- the same step as cc_fused_dp_step (bit-identical
+ * results) in the unfused schedule a framework runs when the collective and
+ * the optimizer are separate library calls, kept for comparison ("LIT-735
+ * (CoCoNet)", Key takeaways: fusing the optimizer into the ReduceScatter/
+ * AllGather beats PyTorch DDP's bucketed AllReduce followed by a separate
+ * optimizer step).  Per bucket: a reduce kernel writes the fp32 sum of the
+ * R gradients into `workspace`, an AdamW kernel reads it back and writes
+ * master/m/v and replica 0's parameters, and R-1 device copies broadcast
+ * replica 0's parameters.  (6R + 30 bytes per parameter against 4R + 24.)
+ *
+ *   workspace        caller-owned fp32 device scratch of workspace_bytes
+ *                    >= 4 * (elements of the largest bucket) bytes, 16-byte
+ *                    aligned, overlapping no slab; reused by every bucket
+ *                    (the calls are stream-ordered).  Too small:
+ *                    CC_ERR_INVALID.
+ *   other arguments  as cc_fused_dp_step (no accumulators).
+ */
+CC_API int cc_unfused_dp_step(const void *const *grads, float *master, float *m,
+                              float *v, void *const *params_out, float *workspace,
+                              size_t workspace_bytes, size_t n, int R,
+                              size_t bucket_bytes, float lr, float beta1, float beta2,
+                              float eps, float weight_decay, int step,
+                              float grad_scale, void *stream);
+
+/*
  * cc_plan_buckets -- lay tensors out in reverse layer order and cut them into
  * buckets (Communication Overlap: backward produces the last layer's
  * gradients first, buckets hold a configurable size, default 25 MB, and the

@@ -210,3 +210,24 @@ def test_bucket_and_accumulate_validation():
     with pytest.raises(capi.CCError) as ei:
         capi.cc_accumulate_local(g, [acc[0], acc[1] + 4], 1000, 2, True, stream=0)
     assert ei.value.status == capi.CC_ERR_MISALIGNED
+
+
+def test_unfused_workspace_validation():
+    g, acc, p, m, v, o = fake_slabs(2, 1000)
+    ws = acc[0]                         # an unused, aligned fake range
+    kw = dict(ADAM, stream=0)
+    def status(workspace, nbytes, bucket_bytes=0):
+        try:
+            capi.cc_unfused_dp_step(g, p, m, v, o, workspace, nbytes, 1000, 2,
+                                    bucket_bytes, **kw)
+            return capi.CC_OK
+        except capi.CCError as err:
+            return err.status
+    assert status(0, 4000) == capi.CC_ERR_INVALID
+    assert status(ws + 4, 4000) == capi.CC_ERR_MISALIGNED
+    assert status(ws, 3999) == capi.CC_ERR_INVALID          # 4 * 1000 needed
+    assert status(ws, 64, bucket_bytes=32) in (capi.CC_ERR_UNSUPPORTED,
+                                              capi.CC_ERR_INVALID)  # 16 elements: enough
+    assert status(p + 1024, 4000) == capi.CC_ERR_ALIAS      # inside master
+    assert status(o[1], 4000) == capi.CC_ERR_ALIAS          # a parameter slab
+    assert status(ws, 4000) in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID)

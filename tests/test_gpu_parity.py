@@ -388,3 +388,41 @@ def test_full_size_bert_large_r8_bulk_engine():
     torch.cuda.synchronize()
     compare_all(s, state, oracle_step(grads, state, hp_of(w)), idx=idx)
     assert capi.cc_device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# The unfused schedule (reduce -> AdamW -> broadcast), for comparison
+# ---------------------------------------------------------------------------
+
+def unfused_step(s, hp, bucket_bytes=0):
+    per = max(8, bucket_bytes // 16 * 8) if bucket_bytes else s.n
+    ws = torch.empty(min(per, s.n), dtype=torch.float32, device=DEV)
+    capi.cc_unfused_dp_step(s.grads, s.master, s.m, s.v, s.outs, ws, ws.numel() * 4,
+                            s.n, s.R, bucket_bytes, **hp)
+    return ws
+
+
+@pytest.mark.parametrize("R", [1, 2, 5, 8, 16])
+@pytest.mark.parametrize("n", [1, 9, 4099, 300_007])
+def test_unfused_matches_oracle(R, n):
+    s = new_slabs(*random_inputs(R, n, seed=900 + R + n % 13, step=5))
+    grads, state, _ = host_copy(s)
+    ws = unfused_step(s, dict(HP10, step=5))
+    torch.cuda.synchronize()
+    compare_all(s, state, oracle_step(grads, state, dict(HP10, step=5)))
+    del ws
+
+
+@pytest.mark.parametrize("bucket_bytes", [16, 4096, 1 << 20])
+def test_unfused_equals_fused_bit_for_bit(bucket_bytes):
+    n = 3 * 1024 * 1024 + 5
+    base = random_inputs(8, n, seed=21, step=10)
+    a = new_slabs([g.clone() for g in base[0]], *[t.clone() for t in base[1:]])
+    b = new_slabs([g.clone() for g in base[0]], *[t.clone() for t in base[1:]])
+    gpu_step(a, HP10, bucket_bytes)
+    unfused_step(b, HP10, bucket_bytes)
+    torch.cuda.synchronize()
+    for x, y in zip([a.master, a.m, a.v] + a.outs, [b.master, b.m, b.v] + b.outs):
+        xv = x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32)
+        yv = y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32)
+        assert torch.equal(xv, yv)
