@@ -85,6 +85,8 @@ _SIGNATURES = {
     "cc_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
     "cc_unfused_dp_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _sz, _i, _sz,
                             _f, _f, _f, _f, _f, _i, _f, _vp], _i),
+    "cc_unfused_dp_step_noalloc": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _f, _f,
+                                    _f, _f, _f, _i, _f, _vp], _i),
 }
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -193,6 +195,19 @@ def cc_unfused_dp_step(grads, master, m, v, params_out, workspace,
         _addr_array(params_out), _addr(workspace), workspace_bytes, n, R,
         bucket_bytes, lr, beta1, beta2, eps, weight_decay, step, grad_scale,
         _stream(stream)), "cc_unfused_dp_step")
+
+
+def cc_unfused_dp_step_noalloc(grads, master, m, v, params_out, n: int, R: int,
+                               bucket_bytes: int, lr: float, beta1: float,
+                               beta2: float, eps: float, weight_decay: float,
+                               step: int, grad_scale: float, stream=None) -> None:
+    """The unfused step for callers that cannot allocate: its scratch is a
+    fixed 64 MiB array inside the library (buckets up to 16M elements)."""
+    _check(lib().cc_unfused_dp_step_noalloc(
+        _addr_array(grads), _addr(master), _addr(m), _addr(v),
+        _addr_array(params_out), n, R, bucket_bytes, lr, beta1, beta2, eps,
+        weight_decay, step, grad_scale, _stream(stream)),
+        "cc_unfused_dp_step_noalloc")
 
 
 def cc_accumulate_local(grads, acc, n: int, R: int, first: bool,

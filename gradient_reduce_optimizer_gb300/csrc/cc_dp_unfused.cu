@@ -21,6 +21,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "cc_dp_device.cuh"
 #include "cc_dp_internal.h"
 
@@ -187,3 +189,86 @@ cudaError_t launch_unfused_bucket(const Slabs &s, const AdamScalars &c, float *w
 }
 
 }  // namespace ccdp
+
+// ---------------------------------------------------------------------------
+// The unfused step without a caller-provided workspace.
+//
+// Some callers cannot hand the library a scratch buffer or call cudaMalloc
+// themselves: code that runs inside a framework whose caching allocator
+// owns nearly all of the device memory (a raw cudaMalloc outside it can fail
+// or fragment the pool), loops where an allocation or free would stall the
+// device (cudaFree synchronises), and plugins that are given buffers but no
+// right to allocate.  For them the reduced gradient of one bucket lives in a
+// fixed array in the library's own device memory, which every GPU that
+// loads the library holds until the process exits.
+// ---------------------------------------------------------------------------
+
+namespace ccdp {
+namespace {
+
+// Scratch of the allocation-free entry point: one bucket's fp32 reduced
+// gradient, CC_NOALLOC_SCRATCH_ELEMS elements (64 MiB).
+static __device__ __align__(256) float g_noalloc_scratch[CC_NOALLOC_SCRATCH_ELEMS];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+float *g_scratch_addr[kMaxScratchDevices] = {};
+
+// The device address of g_noalloc_scratch on the current device, looked up
+// once per device.  In host code the array's name is only a host-side
+// stand-in, so the address must come from cudaGetSymbolAddress.
+int scratch_address(float **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxScratchDevices)
+        return fail(CC_ERR_UNSUPPORTED, "device %d beyond the %d supported", dev,
+                    kMaxScratchDevices);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(scratch)");
+        g_scratch_addr[dev] = static_cast<float *>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return CC_OK;
+}
+
+}  // namespace
+}  // namespace ccdp
+
+extern "C" int cc_unfused_dp_step_noalloc(const void *const *grads, float *master, float *m,
+                                          float *v, void *const *params_out, size_t n, int R,
+                                          size_t bucket_bytes, float lr, float beta1,
+                                          float beta2, float eps, float weight_decay,
+                                          int step, float grad_scale, void *stream) {
+    using namespace ccdp;
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    AdamScalars c;
+    int st = make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
+    if (st != CC_OK) return st;
+    if (n == 0) return CC_OK;
+    const size_t per = bucket_elems(bucket_bytes, n);
+    const size_t largest = per < n ? per : n;
+    if (largest > CC_NOALLOC_SCRATCH_ELEMS)
+        return fail(CC_ERR_INVALID,
+                    "a bucket of %zu elements exceeds the fixed scratch of %u elements; "
+                    "use bucket_bytes <= %u (or cc_unfused_dp_step with a workspace)",
+                    largest, static_cast<unsigned>(CC_NOALLOC_SCRATCH_ELEMS),
+                    static_cast<unsigned>(2u * CC_NOALLOC_SCRATCH_ELEMS));
+    Slabs s;
+    st = validate_slabs(grads, nullptr, master, m, v, params_out, n, R, false, &s);
+    if (st != CC_OK) return st;
+    float *scratch = nullptr;
+    if ((st = scratch_address(&scratch)) != CC_OK) return st;
+    // The reduce kernel overwrites every scratch element a bucket uses before
+    // the AdamW kernel reads it, so nothing needs clearing between calls.
+    for (size_t b = 0; b < n; b += per) {
+        const size_t e = b + per < n ? b + per : n;
+        const cudaError_t err = launch_unfused_bucket(s, c, scratch, b, e,
+                                                      static_cast<cudaStream_t>(stream));
+        if (err != cudaSuccess) return fail_cuda(err, "allocation-free step launch");
+    }
+    return CC_OK;
+}

@@ -203,6 +203,38 @@ CC_API int cc_unfused_dp_step(const void *const *grads, float *master, float *m,
                               float grad_scale, void *stream);
 
 /*
+ * cc_unfused_dp_step_noalloc -- cc_unfused_dp_step for callers that cannot
+ * allocate device memory.  (The pages have no counterpart: this is a
+ * convenience of this library.)  Some callers cannot pass a workspace or
+ * call cudaMalloc: code whose device memory all belongs to a framework's
+ * caching allocator, hot loops where an allocation or free would stall the
+ * device, and plugins handed buffers but no right to allocate.  This entry
+ * point takes only the inputs and outputs; the reduced gradient of one bucket
+ * goes to a fixed array of CC_NOALLOC_SCRATCH_ELEMS fp32 elements (64 MiB)
+ * inside the library's own device memory, which every GPU that loads the
+ * library holds until the process exits.  It allocates nothing.
+ *
+ *  - A bucket (min(n, floor(bucket_bytes/16)*8 elements)) larger than the
+ *    array is rejected with CC_ERR_INVALID: keep bucket_bytes <=
+ *    2 * CC_NOALLOC_SCRATCH_ELEMS (32 MiB), or n within the array when
+ *    bucket_bytes is 0.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) for that device; make that first call before
+ *    any stream capture begins.
+ *  - Every call shares the one array, and each bucket overwrites the part
+ *    it uses before reading it, so no state carries over between calls.
+ *    Calls that overlap on the GPU (on different streams, or from different
+ *    threads without ordering) race on the array: order them.
+ *  - Arguments and results are as for cc_fused_dp_step (bit-identical).
+ */
+#define CC_NOALLOC_SCRATCH_ELEMS (16u * 1024u * 1024u)
+CC_API int cc_unfused_dp_step_noalloc(const void *const *grads, float *master, float *m,
+                                      float *v, void *const *params_out, size_t n, int R,
+                                      size_t bucket_bytes, float lr, float beta1,
+                                      float beta2, float eps, float weight_decay,
+                                      int step, float grad_scale, void *stream);
+
+/*
  * cc_plan_buckets -- lay tensors out in reverse layer order and cut them into
  * buckets (Communication Overlap: backward produces the last layer's
  * gradients first, buckets hold a configurable size, default 25 MB, and the
