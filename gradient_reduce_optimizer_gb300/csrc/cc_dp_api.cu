@@ -60,22 +60,77 @@ MemGetAddressRangeFn address_range_fn() {
 
 }  // namespace
 
+namespace {
+
+using PointerGetAttributeFn = CUresult (*)(void *, CUpointer_attribute, CUdeviceptr);
+
+PointerGetAttributeFn pointer_attribute_fn() {
+    static PointerGetAttributeFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PointerGetAttributeFn>(p);
+    }
+    return fn;
+}
+
+int check_within(const void *ptr, size_t bytes, uintptr_t base, size_t size,
+                 const char *name, const char *kind) {
+    const uintptr_t p = reinterpret_cast<uintptr_t>(ptr);
+    if (p < base || p - base > size || bytes > size - (p - base))
+        return fail(CC_ERR_INVALID,
+                    "%s: %zu bytes at %p run past the end of its %s allocation "
+                    "(%zu bytes at %p)", name, bytes, ptr, kind, size,
+                    reinterpret_cast<void *>(base));
+    return CC_OK;
+}
+
+// [ptr, ptr + bytes) inside one page-locked host allocation that the GPU
+// reaches at the same address (CUDA pinned memory under unified addressing:
+// kernels read and write it over the host link, NVLink-C2C on Grace).
+int check_host_range(const void *ptr, size_t bytes, const char *name) {
+    PointerGetAttributeFn fn = pointer_attribute_fn();
+    if (!fn) return fail(CC_ERR_UNSUPPORTED, "cuPointerGetAttribute unavailable");
+    const CUdeviceptr dp = reinterpret_cast<CUdeviceptr>(ptr);
+    unsigned int type = 0;
+    if (fn(&type, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, dp) != CUDA_SUCCESS ||
+        type != CU_MEMORYTYPE_HOST)
+        return fail(CC_ERR_INVALID,
+                    "%s=%p is neither device memory nor page-locked host memory", name, ptr);
+    CUdeviceptr mapped = 0;
+    if (fn(&mapped, CU_POINTER_ATTRIBUTE_DEVICE_POINTER, dp) != CUDA_SUCCESS || mapped != dp)
+        return fail(CC_ERR_INVALID,
+                    "%s=%p: page-locked host memory not mapped at the same device address",
+                    name, ptr);
+    CUdeviceptr start = 0;
+    size_t size = 0;
+    if (fn(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS ||
+        fn(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS)
+        return fail(CC_ERR_UNSUPPORTED, "%s=%p: cannot bound its host allocation", name, ptr);
+    return check_within(ptr, bytes, start, size, name, "page-locked host");
+}
+
+}  // namespace
+
 int check_device_range(const void *ptr, size_t bytes, const char *name) {
+    return check_slab_range(ptr, bytes, name, false);
+}
+
+int check_slab_range(const void *ptr, size_t bytes, const char *name, bool allow_host) {
     MemGetAddressRangeFn fn = address_range_fn();
     if (!fn) return fail(CC_ERR_UNSUPPORTED, "cuMemGetAddressRange unavailable");
     CUdeviceptr base = 0;
     size_t size = 0;
     const CUresult r = fn(&base, &size, reinterpret_cast<CUdeviceptr>(ptr));
-    if (r != CUDA_SUCCESS)
-        return fail(CC_ERR_INVALID, "%s=%p is not in a device allocation (CUresult %d)",
-                    name, ptr, static_cast<int>(r));
-    const uintptr_t p = reinterpret_cast<uintptr_t>(ptr);
-    if (p - base > size || bytes > size - (p - base))
-        return fail(CC_ERR_INVALID,
-                    "%s: %zu bytes at %p run past the end of its allocation "
-                    "(%zu bytes at %p)", name, bytes, ptr, size,
-                    reinterpret_cast<void *>(base));
-    return CC_OK;
+    if (r == CUDA_SUCCESS) return check_within(ptr, bytes, base, size, name, "device");
+    if (allow_host) return check_host_range(ptr, bytes, name);
+    return fail(CC_ERR_INVALID, "%s=%p is not in a device allocation (CUresult %d)",
+                name, ptr, static_cast<int>(r));
 }
 
 int ensure_device() {
@@ -136,6 +191,7 @@ struct Range {
     bool written;
     const char *name;
     int index;
+    bool host_ok;      // may be page-locked host memory (replica slabs)
 };
 
 bool overlap(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi; }
@@ -157,12 +213,12 @@ int validate_slabs(const void *const *grads, const float *const *acc,
     std::vector<Range> ranges;
     ranges.reserve(3 * CC_MAX_R + 3);
     auto add = [&](const void *p, size_t bytes, bool written, const char *name,
-                   int idx) -> int {
+                   int idx, bool host_ok = false) -> int {
         if (!p) return fail(CC_ERR_INVALID, "%s[%d] is NULL", name, idx);
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
             return fail(CC_ERR_MISALIGNED, "%s[%d]=%p is not 16-byte aligned", name, idx, p);
         const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-        ranges.push_back({lo, lo + bytes, written, name, idx});
+        ranges.push_back({lo, lo + bytes, written, name, idx, host_ok});
         return CC_OK;
     };
     int st;
@@ -170,8 +226,8 @@ int validate_slabs(const void *const *grads, const float *const *acc,
         s->grads[r] = grads[r];
         s->out[r] = params_out[r];
         s->acc[r] = need_acc ? acc[r] : nullptr;
-        if ((st = add(grads[r], 2 * n, false, "grads", r)) != CC_OK) return st;
-        if ((st = add(params_out[r], 2 * n, true, "params_out", r)) != CC_OK) return st;
+        if ((st = add(grads[r], 2 * n, false, "grads", r, true)) != CC_OK) return st;
+        if ((st = add(params_out[r], 2 * n, true, "params_out", r, true)) != CC_OK) return st;
         if (need_acc && (st = add(acc[r], 4 * n, false, "acc", r)) != CC_OK) return st;
     }
     for (int r = R; r < CC_MAX_R; ++r) {
@@ -189,8 +245,8 @@ int validate_slabs(const void *const *grads, const float *const *acc,
                             ranges[i].index, ranges[j].name, ranges[j].index);
     if ((st = ensure_device()) != CC_OK) return st;
     for (const Range &r : ranges)
-        if ((st = check_device_range(reinterpret_cast<const void *>(r.lo), r.hi - r.lo,
-                                     r.name)) != CC_OK)
+        if ((st = check_slab_range(reinterpret_cast<const void *>(r.lo), r.hi - r.lo,
+                                   r.name, r.host_ok)) != CC_OK)
             return st;
     return CC_OK;
 }
@@ -308,7 +364,7 @@ int cc_accumulate_local(const void *const *grads, float *const *acc, size_t n,
                 return fail(CC_ERR_MISALIGNED, "%s[%d]=%p is not 16-byte aligned",
                             names[k], r, ps[k]);
             const uintptr_t lo = reinterpret_cast<uintptr_t>(ps[k]);
-            ranges.push_back({lo, lo + bytes[k], k == 1, names[k], r});
+            ranges.push_back({lo, lo + bytes[k], k == 1, names[k], r, false});
         }
     }
     for (size_t i = 0; i < ranges.size(); ++i)

@@ -98,13 +98,18 @@ int ensure_device();
 // CC_OK if [ptr, ptr + bytes) lies inside one device allocation.
 int check_device_range(const void *ptr, size_t bytes, const char *name);
 
+// As check_device_range; with allow_host, a range inside one page-locked
+// host allocation mapped at the same device address is accepted too.
+int check_slab_range(const void *ptr, size_t bytes, const char *name, bool allow_host);
+
 // Validate and round the AdamW hyper-parameters to the kernel's scalars.
 int make_scalars(float lr, float beta1, float beta2, float eps,
                  float weight_decay, int step, float grad_scale,
                  AdamScalars *c);
 
 // Validate a slab set (R, pointers, alignment, aliasing, device ranges of n
-// elements) and fill `s`.  need_acc selects whether acc[] is used.
+// elements; gradient and parameter replica slabs may be page-locked host
+// memory) and fill `s`.  need_acc selects whether acc[] is used.
 int validate_slabs(const void *const *grads, const float *const *acc,
                    float *master, float *m, float *v, void *const *params_out,
                    size_t n, int R, bool need_acc, Slabs *s);

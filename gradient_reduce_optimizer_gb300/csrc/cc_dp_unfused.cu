@@ -181,8 +181,9 @@ cudaError_t launch_unfused_bucket(const Slabs &s, const AdamScalars &c, float *w
     const size_t bytes = 2 * (end - begin);
     const char *src = static_cast<const char *>(s.out[0]) + 2 * begin;
     for (int r = 1; r < s.R; ++r) {
+        // Default: replica slabs may be page-locked host memory.
         e = cudaMemcpyAsync(static_cast<char *>(s.out[r]) + 2 * begin, src, bytes,
-                            cudaMemcpyDeviceToDevice, stream);
+                            cudaMemcpyDefault, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

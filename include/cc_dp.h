@@ -39,6 +39,13 @@
  *  - Each device range [ptr, ptr + bytes) must lie inside one device
  *    allocation; a range that does not is rejected with CC_ERR_INVALID
  *    before any launch.
+ *  - Replica slabs (grads[r], params_out[r]) may instead live in page-locked
+ *    host memory allocated or registered with CUDA and mapped at the same
+ *    address (any pinned allocation under unified addressing).  The kernels
+ *    then read and write them directly over the host link (NVLink-C2C on
+ *    GB300), with no staging copy; the range must lie inside one such
+ *    allocation.  Pageable host memory is rejected (CC_ERR_INVALID).
+ *    master, m, v, accumulators and workspaces must be device memory.
  *  - Written ranges must not overlap one another nor any read range
  *    (CC_ERR_ALIAS); master, m and v are updated in place.  Read-only
  *    ranges (gradients, accumulators) may alias each other.

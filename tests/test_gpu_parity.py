@@ -426,3 +426,47 @@ def test_unfused_equals_fused_bit_for_bit(bucket_bytes):
         xv = x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32)
         yv = y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32)
         assert torch.equal(xv, yv)
+
+
+# ---------------------------------------------------------------------------
+# Replica slabs in page-locked host memory (read/written over the host link)
+# ---------------------------------------------------------------------------
+
+def test_replica_slabs_in_pinned_host_memory():
+    R, n = 4, 1_000_003
+    grads, master, m, v = random_inputs(R, n, seed=41, step=3)
+    host_grads = [g.cpu().pin_memory() for g in grads]
+    s = new_slabs(host_grads, master, m, v)
+    s.outs[0] = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+    s.outs[2] = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+    grads_h, state, _ = host_copy(s)
+    gpu_step(s, dict(HP10, step=3), bucket_bytes=1 << 20)
+    torch.cuda.synchronize()
+    compare_all(s, state, oracle_step(grads_h, state, dict(HP10, step=3)))
+    # the unfused schedule with host-resident replicas too
+    u = new_slabs(host_grads, *[t.clone() for t in random_inputs(R, n, seed=41, step=3)[1:]])
+    u.outs[1] = torch.empty(n, dtype=torch.bfloat16).pin_memory()
+    grads_h, state, _ = host_copy(u)
+    ws = torch.empty(n, dtype=torch.float32, device=DEV)
+    capi.cc_unfused_dp_step(u.grads, u.master, u.m, u.v, u.outs, ws, 4 * n, n, R, 0,
+                            **dict(HP10, step=3))
+    torch.cuda.synchronize()
+    compare_all(u, state, oracle_step(grads_h, state, dict(HP10, step=3)))
+
+
+def test_pageable_and_short_host_ranges_are_rejected():
+    R, n = 2, 1 << 20
+    s = new_slabs(*random_inputs(R, n, seed=43, step=1))
+    pageable = torch.zeros(n, dtype=torch.bfloat16)
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_fused_dp_step([pageable, s.grads[1]], s.master, s.m, s.v, s.outs, n, R, 0,
+                              **HP1)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    big = 1 << 22
+    dev = new_slabs(*random_inputs(R, big, seed=44, step=1))
+    short = torch.empty(n, dtype=torch.bfloat16).pin_memory()   # 2 MiB of pinned memory
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_fused_dp_step(dev.grads, dev.master, dev.m, dev.v, [short, dev.outs[1]],
+                              big, R, 0, **HP1)
+    assert ei.value.status in (capi.CC_ERR_INVALID, capi.CC_ERR_UNSUPPORTED)
+    assert "past the end" in ei.value.reason or "cannot bound" in ei.value.reason
