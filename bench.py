@@ -391,6 +391,8 @@ def run_ours(args):
 
     if not args.no_unfused and not args.small:
         result["unfused"] = run_unfused(args, wk, stream, ms)
+    if not args.no_accum and not args.small:
+        result["accumulation"] = run_accumulation(args, wk, stream)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wk, stream, world, dev)
     if not args.no_overlap:
@@ -416,6 +418,64 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(result), flush=True)
     return result
+
+
+def run_accumulation(args, wk, stream, k=4):
+    """Gradient accumulation with k micro-steps on the same workload: k-1
+    local micro-steps (first: acc = g, 6R bytes per parameter; later:
+    acc += g, 10R) and the reducing step, the fused kernel with the
+    accumulators (8R + 24).  "The reducing step, not the average step, is
+    the one to profile" (Overlapping Communication and Computation)."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
+    acc = [torch.empty(n_slab, dtype=torch.float32, device=wk["master"].device)
+           for _ in range(R)]
+    reps = max(3, min(args.steps, 20))
+
+    def timed(fn):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for i in range(reps):
+            fn(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1) / reps
+
+    def micro(first):
+        return lambda i: capi.cc_accumulate_local(wk["grads"], acc, n_slab, R, first,
+                                                  stream=stream)
+
+    def reducing(i):
+        capi.cc_fused_dp_step_accum(wk["grads"], acc, wk["master"], wk["m"], wk["v"],
+                                    wk["outs"], n_slab, R, w.bucket_bytes,
+                                    accum_k=k, stream=stream, **step_args(wk, w.step + i))
+
+    def whole(i):
+        for j in range(k - 1):
+            micro(j == 0)(i)
+        reducing(i)
+
+    out = {"accum_k": k}
+    for name, fn, bpp in (("micro_first", micro(True), 6 * R),
+                          ("micro_later", micro(False), 10 * R),
+                          ("reducing_step", reducing, 8 * R + 24)):
+        ms = timed(fn)
+        out[name] = {"ms": round(ms, 4), "bytes_per_param": bpp,
+                     "hbm_gbs": round(bpp * n_slab / (ms * 1e-3) / 1e9, 1)}
+    ms = timed(whole)
+    total = 6 * R + (k - 2) * 10 * R + 8 * R + 24
+    out["optimizer_step"] = {"ms": round(ms, 4), "bytes_per_param": total,
+                             "hbm_gbs": round(total * n_slab / (ms * 1e-3) / 1e9, 1),
+                             "params_per_s": round(w.n / (ms * 1e-3))}
+    del acc
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_unfused(args, wk, stream, fused_ms):
@@ -651,6 +711,8 @@ def parse_args(argv=None):
                    help="profile case: a flat R=8 slab of this many elements, "
                         "one bucket, device timing only")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-accum", action="store_true",
+                   help="skip timing gradient accumulation (k=4)")
     p.add_argument("--no-unfused", action="store_true",
                    help="skip timing the unfused (reduce, AdamW, copies) schedule")
     p.add_argument("--e2e-steps", type=int, default=20)

@@ -186,8 +186,11 @@ fused_step_kernel(const __grid_constant__ FusedParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Local accumulation micro-step: acc[r] = (first ? 0 : acc[r]) + g[r], where
-// "first" copies the gradient (no addition, so -0 stays -0).
+// Local accumulation micro-step: acc[r] = g[r] on the first micro-step (a
+// copy: no "0 +", so -0 stays -0), acc[r] + g[r] on later ones.  One thread
+// owns one 8-element vector across all R replicas and issues every load of
+// it before any add, like the fused kernel (R x 16 bytes in flight on the
+// first micro-step, R x 48 on later ones); one vector per thread.
 // ---------------------------------------------------------------------------
 struct AccumParams {
     const uint4 *g[CC_MAX_R];
@@ -197,35 +200,48 @@ struct AccumParams {
     int tail_len;
 };
 
-template <bool FIRST>
+template <int R, bool FIRST>
 __global__ void __launch_bounds__(kThreads)
 accumulate_kernel(const __grid_constant__ AccumParams p) {
-    const int r = blockIdx.y;
-    const uint4 *g = p.g[r];
-    float4 *acc = p.acc[r];
     const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
     for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
          i < p.num_vec; i += stride) {
-        const uint4 q = __ldcs(g + i);
-        float t[8];
-        widen8(q, t);
+        uint4 gq[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) gq[r] = __ldcs(p.g[r] + i);
         if constexpr (FIRST) {
-            __stcs(acc + 2 * i, make_float4(t[0], t[1], t[2], t[3]));
-            __stcs(acc + 2 * i + 1, make_float4(t[4], t[5], t[6], t[7]));
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float t[8];
+                widen8(gq[r], t);
+                __stcs(p.acc[r] + 2 * i, make_float4(t[0], t[1], t[2], t[3]));
+                __stcs(p.acc[r] + 2 * i + 1, make_float4(t[4], t[5], t[6], t[7]));
+            }
         } else {
-            const float4 a0 = __ldcs(acc + 2 * i), a1 = __ldcs(acc + 2 * i + 1);
-            __stcs(acc + 2 * i, make_float4(__fadd_rn(a0.x, t[0]), __fadd_rn(a0.y, t[1]),
-                                            __fadd_rn(a0.z, t[2]), __fadd_rn(a0.w, t[3])));
-            __stcs(acc + 2 * i + 1,
-                   make_float4(__fadd_rn(a1.x, t[4]), __fadd_rn(a1.y, t[5]),
-                               __fadd_rn(a1.z, t[6]), __fadd_rn(a1.w, t[7])));
+            float4 aq[R][2];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                aq[r][0] = __ldcs(p.acc[r] + 2 * i);
+                aq[r][1] = __ldcs(p.acc[r] + 2 * i + 1);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float a[8] = {aq[r][0].x, aq[r][0].y, aq[r][0].z, aq[r][0].w,
+                              aq[r][1].x, aq[r][1].y, aq[r][1].z, aq[r][1].w};
+                add8_bf16(a, gq[r]);
+                __stcs(p.acc[r] + 2 * i, make_float4(a[0], a[1], a[2], a[3]));
+                __stcs(p.acc[r] + 2 * i + 1, make_float4(a[4], a[5], a[6], a[7]));
+            }
         }
     }
     if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len) {
-        const size_t i = p.tail_begin + threadIdx.x;
-        float *a = reinterpret_cast<float *>(acc);
-        const float t = bf16_at(g, i);
-        a[i] = FIRST ? t : __fadd_rn(a[i], t);
+        const size_t e = p.tail_begin + threadIdx.x;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float *a = reinterpret_cast<float *>(p.acc[r]);
+            const float t = bf16_at(p.g[r], e);
+            a[e] = FIRST ? t : __fadd_rn(a[e], t);
+        }
     }
 }
 
@@ -372,13 +388,31 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     return cudaLaunchKernelEx(&cfg, fused_kernel_for(s.R, acc), p);
 }
 
+using AccumKernel = void (*)(AccumParams);
+
+template <int R>
+AccumKernel pick_accum(bool first) {
+    return first ? accumulate_kernel<R, true> : accumulate_kernel<R, false>;
+}
+
+AccumKernel accum_kernel_for(int R, bool first) {
+    switch (R) {
+        case 1: return pick_accum<1>(first);   case 2: return pick_accum<2>(first);
+        case 3: return pick_accum<3>(first);   case 4: return pick_accum<4>(first);
+        case 5: return pick_accum<5>(first);   case 6: return pick_accum<6>(first);
+        case 7: return pick_accum<7>(first);   case 8: return pick_accum<8>(first);
+        case 9: return pick_accum<9>(first);   case 10: return pick_accum<10>(first);
+        case 11: return pick_accum<11>(first); case 12: return pick_accum<12>(first);
+        case 13: return pick_accum<13>(first); case 14: return pick_accum<14>(first);
+        case 15: return pick_accum<15>(first); case 16: return pick_accum<16>(first);
+        default: return nullptr;
+    }
+}
+
 cudaError_t launch_accumulate(const void *const *grads, float *const *acc,
                               int R, size_t n, bool first,
                               cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
-    DeviceInfo *d = nullptr;
-    cudaError_t e = device_info(&d);
-    if (e != cudaSuccess) return e;
     AccumParams p{};
     for (int r = 0; r < R; ++r) {
         p.g[r] = static_cast<const uint4 *>(grads[r]);
@@ -388,14 +422,9 @@ cudaError_t launch_accumulate(const void *const *grads, float *const *acc,
     p.tail_begin = p.num_vec * CC_PAD_ELEMS;
     p.tail_len = static_cast<int>(n - p.tail_begin);
     size_t blocks = div_up(p.num_vec, kThreads);
-    const size_t cap = div_up(static_cast<size_t>(d->sm_count) * 8, R);
-    if (blocks > cap) blocks = cap;
+    if (blocks > 0x7FFFFFFFu) blocks = 0x7FFFFFFFu;   // grid-stride covers the rest
     if (blocks == 0) blocks = 1;
-    const dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(R));
-    if (first)
-        accumulate_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-    else
-        accumulate_kernel<false><<<grid, kThreads, 0, stream>>>(p);
+    accum_kernel_for(R, first)<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
