@@ -470,3 +470,26 @@ def test_pageable_and_short_host_ranges_are_rejected():
                               big, R, 0, **HP1)
     assert ei.value.status in (capi.CC_ERR_INVALID, capi.CC_ERR_UNSUPPORTED)
     assert "past the end" in ei.value.reason or "cannot bound" in ei.value.reason
+
+
+@pytest.mark.parametrize("use_acc", [False, True])
+def test_fp32_slabs_aligned_to_16_but_not_32_bytes(use_acc):
+    """fp32 slabs 16 bytes past a 32-byte boundary take the 128-bit path."""
+    R, n = 3, 100_003
+    grads, master, m, v = random_inputs(R, n, seed=61, step=4)
+    def offset16(t):
+        buf = torch.empty(t.numel() + 4, dtype=t.dtype, device=DEV)
+        view = buf[4:]
+        assert view.data_ptr() % 32 == 16
+        view.copy_(t)
+        return view
+    s = new_slabs(grads, offset16(master), offset16(m), offset16(v), with_acc=use_acc)
+    if use_acc:
+        g = torch.Generator(device=DEV)
+        g.manual_seed(62)
+        s.acc = [offset16(torch.randn(n, generator=g, device=DEV) * 1e-3) for _ in range(R)]
+    grads_h, state, acc = host_copy(s)
+    gpu_step(s, dict(HP10, step=4), bucket_bytes=64 << 10, accum_k=2 if use_acc else 1,
+             use_acc=use_acc)
+    torch.cuda.synchronize()
+    compare_all(s, state, oracle_step(grads_h, state, dict(HP10, step=4), acc=acc))
