@@ -493,3 +493,55 @@ def test_fp32_slabs_aligned_to_16_but_not_32_bytes(use_acc):
              use_acc=use_acc)
     torch.cuda.synchronize()
     compare_all(s, state, oracle_step(grads_h, state, dict(HP10, step=4), acc=acc))
+
+
+# ---------------------------------------------------------------------------
+# The ready-driven scheduler (cc_overlap_bench) steps every bucket exactly once
+# per arm
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("max_ctas,prio", [(0, 0), (0, 2), (24, 1)])
+def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio):
+    """With warmup 0 and one iteration the four arms step the slabs three
+    times (buckets alone, overlapped, sequential; the backward-only arm does
+    not step): the result must be three oracle steps, bit for bit."""
+    t = wl.bert_large_tensors(layers=4, hidden=256, ffn=1024, vocab=997, positions=64)
+    numel = [x[1] for x in t]
+    layer_of = [x[2] for x in t]
+    offsets, buckets, n_slab = oracle.plan_buckets(numel, 96 * 1024)
+    ready = oracle.bucket_ready_layers(numel, layer_of, offsets, buckets)
+    assert len(buckets) >= 8 and len(set(ready)) == 4
+    R = 4
+    s = new_slabs(*random_inputs(R, n_slab, seed=71, step=5))
+    grads, state, _ = host_copy(s)
+    hp = dict(HP10, step=5)
+    M = N = K = 256
+    A = torch.randn(M * K, device=DEV).to(torch.bfloat16)
+    B = torch.randn(K * N, device=DEV).to(torch.bfloat16)
+    C = torch.empty(M * N, dtype=torch.bfloat16, device=DEV)
+    r = capi.cc_overlap_bench(grads=s.grads, master=s.master, m=s.m, v=s.v,
+                              params_out=s.outs, n=n_slab, R=R, buckets=buckets,
+                              ready_layers=ready, num_layers=4, gemms_per_layer=2,
+                              gemm_m=M, gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B,
+                              gemm_c=C, warmup=0, iters=1, max_ctas=max_ctas,
+                              stream_priority=prio, **hp)
+    assert r["num_buckets"] == len(buckets) and r["t_bwd_ms"] > 0
+    torch.cuda.synchronize()
+    for _ in range(3):
+        outs = oracle_step(grads, state, hp)
+    compare_all(s, state, outs)
+    assert capi.cc_device_status() == 0
+
+
+def test_overlap_bench_rejects_bad_schedules():
+    s = new_slabs(*random_inputs(2, 4096, seed=72, step=1))
+    A = torch.empty(64 * 64, dtype=torch.bfloat16, device=DEV)
+    base = dict(grads=s.grads, master=s.master, m=s.m, v=s.v, params_out=s.outs,
+                n=4096, R=2, num_layers=2, gemms_per_layer=1, gemm_m=64, gemm_n=64,
+                gemm_k=64, gemm_a=A, gemm_b=A, gemm_c=A, warmup=0, iters=1, **HP1)
+    for buckets, ready, status in (([(0, 4096)], [2], capi.CC_ERR_INVALID),   # no layer 2
+                                   ([(4, 4096)], [0], capi.CC_ERR_MISALIGNED),
+                                   ([(0, 5000)], [0], capi.CC_ERR_INVALID)):
+        with pytest.raises(capi.CCError) as ei:
+            capi.cc_overlap_bench(buckets=buckets, ready_layers=ready, **base)
+        assert ei.value.status == status
