@@ -44,6 +44,7 @@ __all__ = [
     "accumulate_local",
     "plan_buckets",
     "bucket_ready_layers",
+    "tp_allreduce",
     "MAX_R",
 ]
 
@@ -65,6 +66,8 @@ def _lib() -> ctypes.CDLL:
         lib.oracle_fused_dp_step.argtypes = [
             vp, vp, vp, vp, vp, vp, sz, i, f, f, f, f, f, i, f]
         lib.oracle_fused_dp_step.restype = i
+        lib.oracle_tp_allreduce.argtypes = [vp, vp, sz, i]
+        lib.oracle_tp_allreduce.restype = i
         _LIB = lib
     return _LIB
 
@@ -149,6 +152,21 @@ def fused_dp_step(grads: Sequence[np.ndarray], master: np.ndarray,
         int(step), grad_scale)
     if rc != 0:
         raise ValueError("oracle_fused_dp_step rejected its arguments")
+    return outs
+
+
+def tp_allreduce(partials: Sequence[np.ndarray]) -> list:
+    """The tensor-parallel AllReduce of R fp32 partial products: their sum
+    in rank order, rounded to bf16, one uint16 array per rank."""
+    R = len(partials)
+    if not 1 <= R <= MAX_R:
+        raise ValueError("R must be in 1..16")
+    n = partials[0].size
+    for r in range(R):
+        _check(partials[r], np.float32, n, f"partials[{r}]")
+    outs = [np.empty(n, dtype=np.uint16) for _ in range(R)]
+    if _lib().oracle_tp_allreduce(_ptr_array(partials), _ptr_array(outs), n, R) != 0:
+        raise ValueError("oracle_tp_allreduce rejected its arguments")
     return outs
 
 

@@ -36,6 +36,11 @@
  *   each replica's local total acc[r] + g[r] and then reduces across
  *   replicas as above.
  *
+ * The tensor-parallel AllReduce ("LIT-735", Key takeaways: the model-
+ * parallel MatMul-then-AllReduce, overlapped in chunks): R ranks each hold a
+ * partial fp32 product; every rank receives their sum, replica 0 first, in
+ * that order, rounded once to bf16 (oracle_tp_allreduce).
+ *
  * Parity pins (tests/test_oracle_pins.py): closed form at step 1, R=1 against
  * torch.optim.AdamW on CPU, exact integer sums, replica identity, k-step
  * accumulation against the single step on summed gradients, the bf16 cast
@@ -171,6 +176,22 @@ int oracle_fused_dp_step(const uint16_t *const *grads, const float *const *acc,
 
         const uint16_t b = oracle_bf16_round(p_new);
         for (int r = 0; r < R; ++r) params_out[r][i] = b;
+    }
+    return 0;
+}
+
+/*
+ * The sum over R partial products, in rank order r = 0..R-1 starting from
+ * partial[0] itself, rounded to bf16 and handed to every rank.
+ */
+int oracle_tp_allreduce(const float *const *partials, uint16_t *const *out,
+                        size_t n, int R) {
+    if (R < 1 || R > ORACLE_MAX_R) return -1;
+    for (size_t i = 0; i < n; ++i) {
+        float s = partials[0][i];
+        for (int r = 1; r < R; ++r) s = s + partials[r][i];
+        const uint16_t b = oracle_bf16_round(s);
+        for (int r = 0; r < R; ++r) out[r][i] = b;
     }
     return 0;
 }

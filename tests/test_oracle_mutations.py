@@ -65,6 +65,15 @@ MUTATIONS = {
     "accumulator ignored for r > 0":
         ("float local = acc[r][i] + oracle_bf16_widen(grads[r][i]);",
          "float local = oracle_bf16_widen(grads[r][i]);"),
+    "all-reduce drops the last rank":
+        ("        for (int r = 1; r < R; ++r) s = s + partials[r][i];",
+         "        for (int r = 1; r < R - 1; ++r) s = s + partials[r][i];"),
+    "all-reduce sums in reverse rank order":
+        ("        float s = partials[0][i];\n        for (int r = 1; r < R; ++r) s = s + partials[r][i];",
+         "        float s = partials[R - 1][i];\n        for (int r = R - 2; r >= 0; --r) s = s + partials[r][i];"),
+    "all-reduce truncates to bf16":
+        ("        const uint16_t b = oracle_bf16_round(s);\n        for (int r = 0; r < R; ++r) out[r][i] = b;",
+         "        uint32_t u_; memcpy(&u_, &s, 4);\n        const uint16_t b = (uint16_t)(u_ >> 16);\n        for (int r = 0; r < R; ++r) out[r][i] = b;"),
     "only replica 0 receives parameters":
         ("for (int r = 0; r < R; ++r) params_out[r][i] = b;",
          "params_out[0][i] = b; for (int r = 1; r < R; ++r) params_out[r][i] = 0;"),

@@ -395,3 +395,41 @@ def test_brute_force_float64_tiny(n, R):
         # the cast of the fp32 master is to the nearest bf16 (<= half a step)
         q = widen(out[0][i:i + 1])[0]
         assert abs(q - float(P[i])) <= abs(float(P[i])) * 2.0 ** -8
+
+
+# ---------------------------------------------------------------------------
+# The tensor-parallel AllReduce
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R", [1, 2, 4, 16])
+def test_tp_allreduce_integer_sums_exact_and_identical(R):
+    """Integer partials sum exactly; small integers are exact in bf16, so the
+    result is the integer sum, the same on every rank."""
+    n = 5000
+    ints = [RNG.integers(-15, 16, n) for _ in range(R)]
+    out = oracle.tp_allreduce([i.astype(np.float32) for i in ints])
+    s = np.sum(ints, axis=0)
+    np.testing.assert_array_equal(widen(out[0]), s.astype(np.float64))
+    for r in range(1, R):
+        np.testing.assert_array_equal(out[r], out[0])
+
+
+def test_tp_allreduce_rank_order():
+    """Rank order is observable after the bf16 cast: (1 + 2^-24) rounds to 1
+    (a tie, to even), so [1, 2^-24, -1] gives 0, while [-1, 2^-24, 1] keeps
+    the 2^-24 (exact in bf16)."""
+    parts = [np.array([x], np.float32) for x in (1.0, 2.0 ** -24, -1.0)]
+    assert widen(oracle.tp_allreduce(parts)[0])[0] == 0.0
+    assert widen(oracle.tp_allreduce(parts[::-1])[0])[0] == 2.0 ** -24
+
+
+def test_tp_allreduce_matches_float64_sum_within_bound():
+    """Random partials: the result is the float64 sum rounded to the bf16 grid,
+    up to the fp32 summation error (R ulps of the partial sums)."""
+    R, n = 8, 20000
+    parts = [(RNG.standard_normal(n) * 10).astype(np.float32) for _ in range(R)]
+    got = widen(oracle.tp_allreduce(parts)[0])
+    exact = np.sum([p.astype(np.float64) for p in parts], axis=0)
+    bound = np.abs(exact) * 2.0 ** -8 + R * 2.0 ** -24 * np.sum(
+        [np.abs(p.astype(np.float64)) for p in parts], axis=0) * 2
+    assert np.all(np.abs(got - exact) <= bound)
