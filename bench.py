@@ -391,6 +391,8 @@ def run_ours(args):
 
     if not args.no_unfused and not args.small:
         result["unfused"] = run_unfused(args, wk, stream, ms)
+    if not args.no_tp and not args.small:
+        result["tp_matmul_allreduce"] = run_tp(args, dev)
     if not args.no_accum and not args.small:
         result["accumulation"] = run_accumulation(args, wk, stream)
     if not args.no_e2e:
@@ -418,6 +420,41 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(result), flush=True)
     return result
+
+
+def run_tp(args, dev, R=8, m=8192, n=3072, k=12288, chunk_list=(1, 2, 4, 8, 16)):
+    """The tensor-parallel MatMul-then-AllReduce of a GPT-2 8.3B MLP output
+    projection (row-parallel: k = 12288 -> n = 3072 over m = 8192 tokens) at
+    tensor-parallel degree R = 8, sequential and overlapped in chunks of rows
+    ("LIT-735", Key takeaways: hides most of the MatMul, up to 1.36x)."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    kr = k // R
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    # each operand one buffer cut into R equal shards (batched GEMM per chunk)
+    x = list(torch.randn(R * m * kr, generator=g, device=dev).to(torch.bfloat16).view(R, -1))
+    w = list((torch.randn(R * kr * n, generator=g, device=dev) * 0.02)
+             .to(torch.bfloat16).view(R, -1))
+    partials = list(torch.empty(R, m * n, device=dev))
+    outs = [torch.empty(m * n, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    rows = []
+    for chunks in chunk_list:
+        t = capi.cc_tp_overlap_bench(R=R, m=m, n=n, k=k, chunks=chunks, x=x, w=w,
+                                     partials=partials, out=outs, warmup=args.warmup,
+                                     iters=args.overlap_iters,
+                                     stream_priority=args.stream_priority)
+        hidden = (t["t_sequential_ms"] - t["t_overlap_ms"]) / t["t_allreduce_ms"]
+        rows.append({"chunks": chunks, **{key: round(v, 4) for key, v in t.items()},
+                     "allreduce_hidden_pct": round(100 * hidden, 1),
+                     "speedup_vs_sequential": round(t["t_sequential_ms"] / t["t_overlap_ms"], 3)})
+    ar = rows[0]["t_allreduce_ms"]
+    return {"shape": {"R": R, "m": m, "n": n, "k": k},
+            "gemm_tflops": round(2 * m * n * k / (rows[0]["t_gemm_ms"] * 1e-3) / 1e12, 1),
+            "allreduce_bytes": 6 * R * m * n,
+            "allreduce_hbm_gbs": round(6 * R * m * n / (ar * 1e-3) / 1e9, 1),
+            "chunks": rows}
 
 
 def run_accumulation(args, wk, stream, k=4):
@@ -711,6 +748,8 @@ def parse_args(argv=None):
                    help="profile case: a flat R=8 slab of this many elements, "
                         "one bucket, device timing only")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-tp", action="store_true",
+                   help="skip the tensor-parallel MatMul-then-AllReduce overlap")
     p.add_argument("--no-accum", action="store_true",
                    help="skip timing gradient accumulation (k=4)")
     p.add_argument("--no-unfused", action="store_true",

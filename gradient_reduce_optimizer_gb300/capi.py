@@ -67,6 +67,19 @@ class cc_overlap_result(ctypes.Structure):
     ]
 
 
+class cc_tp_cfg(ctypes.Structure):
+    _fields_ = [
+        ("R", _i), ("m", _i), ("n", _i), ("k", _i), ("chunks", _i),
+        ("x", _vp), ("w", _vp), ("partials", _vp), ("out", _vp),
+        ("warmup", _i), ("iters", _i), ("stream_priority", _i),
+    ]
+
+
+class cc_tp_result(ctypes.Structure):
+    _fields_ = [("t_gemm_ms", _f), ("t_allreduce_ms", _f),
+                ("t_sequential_ms", _f), ("t_overlap_ms", _f)]
+
+
 _SIGNATURES = {
     "cc_status_string": ([_i], ctypes.c_char_p),
     "cc_last_error": ([], ctypes.c_char_p),
@@ -87,6 +100,8 @@ _SIGNATURES = {
                             _f, _f, _f, _f, _f, _i, _f, _vp], _i),
     "cc_unfused_dp_step_noalloc": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _f, _f,
                                     _f, _f, _f, _i, _f, _vp], _i),
+    "cc_tp_allreduce": ([_vp, _vp, _sz, _i, _vp], _i),
+    "cc_tp_overlap_bench": ([ctypes.POINTER(cc_tp_cfg), ctypes.POINTER(cc_tp_result)], _i),
 }
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -295,6 +310,25 @@ def cc_device_status(clear: bool = False) -> int:
     _check(lib().cc_device_status(ctypes.byref(st), int(bool(clear))),
            "cc_device_status")
     return st.value
+
+
+def cc_tp_allreduce(partials, out, n: int, R: int, stream=None) -> None:
+    _check(lib().cc_tp_allreduce(_addr_array(partials), _addr_array(out), n, R,
+                                 _stream(stream)), "cc_tp_allreduce")
+
+
+def cc_tp_overlap_bench(*, R: int, m: int, n: int, k: int, chunks: int, x, w,
+                        partials, out, warmup: int = 3, iters: int = 20,
+                        stream_priority: int = 0) -> Dict[str, float]:
+    keep = [_addr_array(a) for a in (x, w, partials, out)]
+    cfg = cc_tp_cfg(R=R, m=m, n=n, k=k, chunks=chunks,
+                    x=ctypes.cast(keep[0], _vp), w=ctypes.cast(keep[1], _vp),
+                    partials=ctypes.cast(keep[2], _vp), out=ctypes.cast(keep[3], _vp),
+                    warmup=warmup, iters=iters, stream_priority=stream_priority)
+    res = cc_tp_result()
+    _check(lib().cc_tp_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
+           "cc_tp_overlap_bench")
+    return {name: getattr(res, name) for name, _ in res._fields_}
 
 
 def cc_l2_flush(buf, nbytes: int, stream=None) -> None:

@@ -340,6 +340,53 @@ typedef struct cc_overlap_result {
 CC_API int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out);
 
 /*
+ * cc_tp_allreduce -- the AllReduce of a tensor-parallel row-parallel layer,
+ * for R emulated ranks ("LIT-735 (CoCoNet)", Key takeaways: the
+ * model-parallel MatMul and the AllReduce that follows it).  Every rank's
+ * output becomes the bf16 rounding of the fp32 sum of the R partial products
+ * in rank order r = 0..R-1 (one rounding).
+ *
+ *   partials[R]  fp32[n] each, read: rank r's partial product.
+ *   out[R]       bf16[n] each, written: every rank's copy of the sum.
+ *   n, R, stream as for cc_fused_dp_step.  Device memory only.
+ */
+CC_API int cc_tp_allreduce(const float *const *partials, void *const *out, size_t n,
+                           int R, void *stream);
+
+/*
+ * cc_tp_overlap_bench -- the MatMul-then-AllReduce of a row-parallel layer,
+ * sequential and overlapped in chunks of rows (LIT-735, Key takeaways:
+ * overlapping the two in chunks hides most of the MatMul).  Rank r holds
+ * x[r] (bf16, m x k/R, row-major) and w[r] (bf16, k/R x n, row-major) and
+ * computes partials[r] = x[r] w[r] (fp32, m x n, cuBLAS with fp32
+ * accumulation); out[r] receives the AllReduce (cc_tp_allreduce).  The rows
+ * are cut into `chunks` equal chunks; in the overlapped arm each chunk's
+ * AllReduce runs on a side stream as soon as that chunk's R GEMMs finish.
+ * Four arms, each the median of `iters` runs after `warmup`: the GEMMs
+ * alone, the AllReduce alone, GEMMs then AllReduce on one stream, and the
+ * chunked overlap.  Requires k % R == 0, m % chunks == 0, (m/chunks)*n and
+ * k/R multiples of 8.  When the R shards of x, w and partials lie at equal
+ * strides (one buffer cut into R slabs), a chunk's R products run as one
+ * strided-batched GEMM.  Buffers are caller-owned device memory; the call
+ * synchronises its own streams and allocates nothing beyond cuBLAS's handle.
+ */
+typedef struct cc_tp_cfg {
+    int R, m, n, k, chunks;
+    const void *const *x;          /* [R] bf16 m x k/R */
+    const void *const *w;          /* [R] bf16 k/R x n */
+    float *const *partials;        /* [R] fp32 m x n */
+    void *const *out;              /* [R] bf16 m x n */
+    int warmup, iters;
+    int stream_priority;           /* 0 equal, 1 side stream high, 2 compute high */
+} cc_tp_cfg;
+
+typedef struct cc_tp_result {
+    float t_gemm_ms, t_allreduce_ms, t_sequential_ms, t_overlap_ms;
+} cc_tp_result;
+
+CC_API int cc_tp_overlap_bench(const cc_tp_cfg *cfg, cc_tp_result *out);
+
+/*
  * cc_device_status -- the bulk-copy engine's status word on the current
  * device: 0, or an or of codes of pipeline waits that ran out (each wait is
  * bounded to one second, after which the kernel abandons its pipeline and

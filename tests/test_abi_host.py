@@ -231,3 +231,18 @@ def test_unfused_workspace_validation():
     assert status(p + 1024, 4000) == capi.CC_ERR_ALIAS      # inside master
     assert status(o[1], 4000) == capi.CC_ERR_ALIAS          # a parameter slab
     assert status(ws, 4000) in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID)
+
+
+def test_tp_allreduce_validation():
+    g, acc, p, m, v, o = fake_slabs(3, 1000)
+    def status(parts, outs, R=3):
+        try:
+            capi.cc_tp_allreduce(parts, outs, 1000, R, stream=0)
+            return capi.CC_OK
+        except capi.CCError as err:
+            return err.status
+    assert status(acc, o, R=0) == capi.CC_ERR_INVALID
+    assert status(acc, [o[0], o[1] + 2, o[2]]) == capi.CC_ERR_MISALIGNED
+    assert status(acc, [o[0], acc[1], o[2]]) == capi.CC_ERR_ALIAS    # writes over a partial
+    assert status(acc, [o[0], o[0], o[2]]) == capi.CC_ERR_ALIAS      # two outputs share memory
+    assert status(acc, o) in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID)

@@ -545,3 +545,78 @@ def test_overlap_bench_rejects_bad_schedules():
         with pytest.raises(capi.CCError) as ei:
             capi.cc_overlap_bench(buckets=buckets, ready_layers=ready, **base)
         assert ei.value.status == status
+
+
+# ---------------------------------------------------------------------------
+# The tensor-parallel MatMul-then-AllReduce
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("n", [1, 9, 4099, 262_147])
+def test_tp_allreduce_matches_oracle(R, n):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(R * 1000 + n % 1000)
+    parts = [torch.randn(n, generator=g, device=DEV) * 10 for _ in range(R)]
+    if n > 100:   # a few special values
+        specials = torch.tensor([float("inf"), -float("inf"), float("nan"), 0.0, -0.0,
+                                 3e38, 1e-40], device=DEV)
+        parts[0][:7] = specials
+    outs = [torch.full((n,), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+            for _ in range(R)]
+    capi.cc_tp_allreduce(parts, outs, n, R)
+    torch.cuda.synchronize()
+    ref = oracle.tp_allreduce([f32(p).copy() for p in parts])
+    for r in range(R):
+        assert_bits(f"out[{r}]", u16(outs[r]), ref[r], "bf16")
+
+
+@pytest.mark.parametrize("batched", [False, True])
+def test_tp_overlap_bench_outputs(batched):
+    R, m, n, k, chunks = 4, 256, 128, 512, 4
+    kr = k // R
+    g = torch.Generator(device=DEV)
+    g.manual_seed(81)
+    if batched:   # one buffer per operand, R equal shards
+        x = list(torch.randn(R * m * kr, generator=g, device=DEV).to(torch.bfloat16).view(R, -1))
+        w = list((torch.randn(R * kr * n, generator=g, device=DEV) * 0.05)
+                 .to(torch.bfloat16).view(R, -1))
+        partials = list(torch.empty(R, m * n, device=DEV))
+    else:
+        x = [(torch.randn(m * kr, generator=g, device=DEV)).to(torch.bfloat16)
+             for _ in range(R)]
+        w = [(torch.randn(kr * n, generator=g, device=DEV) * 0.05).to(torch.bfloat16)
+             for _ in range(R)]
+        partials = [torch.empty(m * n, device=DEV) for _ in range(R)]
+    outs = [torch.empty(m * n, dtype=torch.bfloat16, device=DEV) for _ in range(R)]
+    t = capi.cc_tp_overlap_bench(R=R, m=m, n=n, k=k, chunks=chunks, x=x, w=w,
+                                 partials=partials, out=outs, warmup=0, iters=1,
+                                 stream_priority=2)
+    assert all(v > 0 for v in t.values())
+    torch.cuda.synchronize()
+    P = [f32(p).copy() for p in partials]
+    # the AllReduce of what the GEMMs produced: bit for bit
+    ref = oracle.tp_allreduce(P)
+    for r in range(R):
+        assert_bits(f"out[{r}]", u16(outs[r]), ref[r], "bf16")
+    # the GEMMs (cuBLAS, fp32 accumulation) against a float64 matmul
+    for r in range(R):
+        X = x[r].float().cpu().numpy().astype(np.float64).reshape(m, kr)
+        W = w[r].float().cpu().numpy().astype(np.float64).reshape(kr, n)
+        exact = X @ W
+        bound = kr * 2.0 ** -23 * (np.abs(X) @ np.abs(W)) + 1e-30
+        assert np.all(np.abs(P[r].reshape(m, n) - exact) <= bound)
+
+
+def test_tp_overlap_bench_rejects_bad_shapes():
+    R = 2
+    x = [torch.empty(64 * 32, dtype=torch.bfloat16, device=DEV) for _ in range(R)]
+    w = [torch.empty(32 * 64, dtype=torch.bfloat16, device=DEV) for _ in range(R)]
+    p = [torch.empty(64 * 64, device=DEV) for _ in range(R)]
+    o = [torch.empty(64 * 64, dtype=torch.bfloat16, device=DEV) for _ in range(R)]
+    for kw, status in ((dict(k=63, chunks=1), capi.CC_ERR_INVALID),
+                       (dict(k=64, chunks=3), capi.CC_ERR_INVALID),
+                       (dict(k=36, chunks=1), capi.CC_ERR_MISALIGNED)):
+        with pytest.raises(capi.CCError) as ei:
+            capi.cc_tp_overlap_bench(R=R, m=64, n=64, x=x, w=w, partials=p, out=o,
+                                     warmup=0, iters=1, **kw)
+        assert ei.value.status == status
