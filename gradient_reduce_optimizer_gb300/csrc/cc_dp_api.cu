@@ -43,18 +43,21 @@ bool finite(float x) { return std::isfinite(x); }
 
 using MemGetAddressRangeFn = CUresult (*)(CUdeviceptr *, size_t *, CUdeviceptr);
 
+// Driver entry points, looked up once (thread-safe static initialisation)
+// through the runtime so that the library needs no link-time libcuda.
+void *driver_entry_point(const char *symbol) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(symbol, &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return p;
+    return nullptr;
+}
+
 MemGetAddressRangeFn address_range_fn() {
-    static MemGetAddressRangeFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<MemGetAddressRangeFn>(p);
-    }
+    static const MemGetAddressRangeFn fn =
+        reinterpret_cast<MemGetAddressRangeFn>(driver_entry_point("cuMemGetAddressRange"));
     return fn;
 }
 
@@ -65,17 +68,8 @@ namespace {
 using PointerGetAttributeFn = CUresult (*)(void *, CUpointer_attribute, CUdeviceptr);
 
 PointerGetAttributeFn pointer_attribute_fn() {
-    static PointerGetAttributeFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PointerGetAttributeFn>(p);
-    }
+    static const PointerGetAttributeFn fn =
+        reinterpret_cast<PointerGetAttributeFn>(driver_entry_point("cuPointerGetAttribute"));
     return fn;
 }
 

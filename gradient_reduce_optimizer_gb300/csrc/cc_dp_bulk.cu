@@ -39,6 +39,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "cc_dp_device.cuh"
 #include "cc_dp_internal.h"
 
@@ -364,6 +366,7 @@ void choose_tiling(int R, bool acc, int *tile, int *stages) {
 
 constexpr int kMaxDevices = 64;
 bool g_smem_attr_set[kMaxDevices][CC_MAX_R + 1][2];
+std::mutex g_smem_attr_mutex;
 
 }  // namespace
 
@@ -380,11 +383,14 @@ cudaError_t launch_fused_bulk(const Slabs &s, const AdamScalars &c, size_t begin
     int T = 0, S = 0;
     choose_tiling(s.R, acc, &T, &S);
     const unsigned smem = static_cast<unsigned>(S) * stage_layout(s.R, acc, T).bytes;
-    if (!g_smem_attr_set[dev][s.R][acc ? 1 : 0]) {
-        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-        if (e != cudaSuccess) return e;
-        g_smem_attr_set[dev][s.R][acc ? 1 : 0] = true;
+    {
+        std::lock_guard<std::mutex> lock(g_smem_attr_mutex);
+        if (!g_smem_attr_set[dev][s.R][acc ? 1 : 0]) {
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+            if (e != cudaSuccess) return e;
+            g_smem_attr_set[dev][s.R][acc ? 1 : 0] = true;
+        }
     }
     BulkParams p{};
     for (int r = 0; r < s.R; ++r) {

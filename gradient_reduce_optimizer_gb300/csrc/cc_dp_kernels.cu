@@ -35,6 +35,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "cc_dp_device.cuh"
 #include "cc_dp_internal.h"
 
@@ -297,6 +300,7 @@ struct DeviceInfo {
 };
 
 DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
 
 cudaError_t device_info(DeviceInfo **out) {
     int dev = 0;
@@ -304,6 +308,7 @@ cudaError_t device_info(DeviceInfo **out) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     DeviceInfo &d = g_devices[dev];
+    std::lock_guard<std::mutex> lock(g_devices_mutex);
     if (!d.ready) {
         cudaDeviceProp prop;
         e = cudaGetDeviceProperties(&prop, dev);
@@ -434,8 +439,8 @@ cudaError_t launch_l2_flush(void *buf, size_t bytes, cudaStream_t stream) {
     DeviceInfo *d = nullptr;
     cudaError_t e = device_info(&d);
     if (e != cudaSuccess) return e;
-    static uint32_t salt = 0x9E3779B9u;
-    salt = salt * 1664525u + 1013904223u;
+    static std::atomic<uint32_t> counter{0};
+    const uint32_t salt = 0x9E3779B9u * (counter.fetch_add(1) + 1u);
     size_t blocks = div_up(nv, kThreads);
     const size_t cap = static_cast<size_t>(d->sm_count) * 8;
     if (blocks > cap) blocks = cap;
