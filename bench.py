@@ -748,6 +748,8 @@ def parse_args(argv=None):
                    help="profile case: a flat R=8 slab of this many elements, "
                         "one bucket, device timing only")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--tp-only", type=int, default=0,
+                   help="profile case: only the tensor-parallel path, with this many rows")
     p.add_argument("--no-tp", action="store_true",
                    help="skip the tensor-parallel MatMul-then-AllReduce overlap")
     p.add_argument("--no-accum", action="store_true",
@@ -772,6 +774,16 @@ def parse_args(argv=None):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.tp_only:
+        # profile case: the tensor-parallel path alone, m rows
+        import torch
+        torch.cuda.set_device(0)
+        from gradient_reduce_optimizer_gb300 import build as gbuild
+        gbuild.build()
+        print(json.dumps({"tp_matmul_allreduce": run_tp(args, torch.device("cuda", 0),
+                                                        m=args.tp_only, chunk_list=(1, 4))}),
+              flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

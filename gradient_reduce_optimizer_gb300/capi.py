@@ -101,6 +101,7 @@ _SIGNATURES = {
     "cc_unfused_dp_step_noalloc": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _f, _f,
                                     _f, _f, _f, _i, _f, _vp], _i),
     "cc_tp_allreduce": ([_vp, _vp, _sz, _i, _vp], _i),
+    "cc_inject_launch_failure": ([_i], _i),
     "cc_tp_overlap_bench": ([ctypes.POINTER(cc_tp_cfg), ctypes.POINTER(cc_tp_result)], _i),
 }
 
@@ -329,6 +330,12 @@ def cc_tp_overlap_bench(*, R: int, m: int, n: int, k: int, chunks: int, x, w,
     _check(lib().cc_tp_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
            "cc_tp_overlap_bench")
     return {name: getattr(res, name) for name, _ in res._fields_}
+
+
+def cc_inject_launch_failure(after_launches: int) -> None:
+    """Arm (or with -1 disarm) a one-shot injected launch failure on this
+    thread, for testing error propagation."""
+    _check(lib().cc_inject_launch_failure(after_launches), "cc_inject_launch_failure")
 
 
 def cc_l2_flush(buf, nbytes: int, stream=None) -> None:

@@ -251,11 +251,29 @@ size_t bucket_elems(size_t bucket_bytes, size_t n) {
     return e < CC_PAD_ELEMS ? CC_PAD_ELEMS : e;
 }
 
+namespace {
+// One-shot injected launch failure for this thread (cc_inject_launch_failure):
+// -1 disarmed, otherwise the number of bucket launches still allowed.
+thread_local int g_fail_after = -1;
+}  // namespace
+
+bool injected_failure() {
+    if (g_fail_after < 0) return false;
+    if (g_fail_after == 0) {
+        g_fail_after = -1;
+        return true;
+    }
+    --g_fail_after;
+    return false;
+}
+
 int run_step(const Slabs &s, const AdamScalars &c, size_t n, size_t bucket_bytes,
              cudaStream_t stream) {
     const size_t per = bucket_elems(bucket_bytes, n);
     for (size_t b = 0; b < n; b += per) {
         const size_t e = std::min(n, b + per);
+        if (injected_failure())
+            return fail(CC_ERR_CUDA, "injected launch failure before the bucket at element %zu", b);
         const cudaError_t err = launch_fused(s, c, b, e, 0, /*chain=*/b > 0, stream);
         if (err != cudaSuccess) return fail_cuda(err, "fused step launch");
     }
@@ -483,10 +501,19 @@ int cc_unfused_dp_step(const void *const *grads, float *master, float *m, float 
     if ((st = check_device_range(workspace, need, "workspace")) != CC_OK) return st;
     for (size_t b = 0; b < n; b += per) {
         const size_t e = std::min(n, b + per);
+        if (injected_failure())
+            return fail(CC_ERR_CUDA, "injected launch failure before the bucket at element %zu", b);
         const cudaError_t err = launch_unfused_bucket(s, c, workspace, b, e,
                                                       static_cast<cudaStream_t>(stream));
         if (err != cudaSuccess) return fail_cuda(err, "unfused step launch");
     }
+    return CC_OK;
+}
+
+int cc_inject_launch_failure(int after_launches) {
+    if (after_launches < -1) return fail(CC_ERR_INVALID, "after_launches=%d must be >= -1",
+                                         after_launches);
+    g_fail_after = after_launches;
     return CC_OK;
 }
 

@@ -397,6 +397,17 @@ CC_API int cc_tp_overlap_bench(const cc_tp_cfg *cfg, cc_tp_result *out);
 CC_API int cc_device_status(unsigned *status, int clear);
 
 /*
+ * cc_inject_launch_failure -- failure injection on the host, for testing how
+ * errors propagate (no GPU fault is involved).  Arms a one-shot failure for
+ * the calling thread: after `after_launches` more bucket launches by
+ * cc_fused_dp_step, cc_fused_dp_step_accum or cc_unfused_dp_step, the next
+ * bucket is not launched and the call returns CC_ERR_CUDA ("injected launch
+ * failure ...") -- the documented partial-launch case: earlier buckets of
+ * that call were enqueued, later ones were not.  -1 disarms.
+ */
+CC_API int cc_inject_launch_failure(int after_launches);
+
+/*
  * cc_l2_flush -- overwrite `bytes` of the caller's device buffer `buf`
  * (16-byte aligned) so that a timed kernel that follows finds none of its
  * data in L2.  Measurement helper; not part of the step.

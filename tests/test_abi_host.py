@@ -246,3 +246,11 @@ def test_tp_allreduce_validation():
     assert status(acc, [o[0], acc[1], o[2]]) == capi.CC_ERR_ALIAS    # writes over a partial
     assert status(acc, [o[0], o[0], o[2]]) == capi.CC_ERR_ALIAS      # two outputs share memory
     assert status(acc, o) in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID)
+
+
+def test_inject_launch_failure_arguments():
+    capi.cc_inject_launch_failure(5)
+    capi.cc_inject_launch_failure(-1)
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_inject_launch_failure(-2)
+    assert ei.value.status == capi.CC_ERR_INVALID

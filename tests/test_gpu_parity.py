@@ -620,3 +620,41 @@ def test_tp_overlap_bench_rejects_bad_shapes():
             capi.cc_tp_overlap_bench(R=R, m=64, n=64, x=x, w=w, partials=p, out=o,
                                      warmup=0, iters=1, **kw)
         assert ei.value.status == status
+
+
+# ---------------------------------------------------------------------------
+# Error propagation: an injected launch failure partway through a step
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("schedule", ["fused", "unfused"])
+def test_injected_launch_failure_leaves_earlier_buckets_applied(schedule):
+    """Failure after 3 of 8 buckets: CC_ERR_CUDA with the reason; buckets 0-2
+    were stepped, 3-7 untouched; the next call works normally."""
+    R, n, bb = 2, 8 * 4096, 8192          # 4096-element buckets, 8 of them
+    s = new_slabs(*random_inputs(R, n, seed=91, step=2))
+    before = [f32(t).copy() for t in (s.master, s.m, s.v)]
+    grads, state, _ = host_copy(s)
+    hp = dict(HP10, step=2)
+    ws = torch.empty(4096, dtype=torch.float32, device=DEV)
+
+    def step():
+        if schedule == "fused":
+            capi.cc_fused_dp_step(s.grads, s.master, s.m, s.v, s.outs, n, R, bb, **hp)
+        else:
+            capi.cc_unfused_dp_step(s.grads, s.master, s.m, s.v, s.outs, ws, 4 * 4096,
+                                    n, R, bb, **hp)
+
+    capi.cc_inject_launch_failure(3)
+    with pytest.raises(capi.CCError) as ei:
+        step()
+    assert ei.value.status == capi.CC_ERR_CUDA and "injected" in ei.value.reason
+    torch.cuda.synchronize()
+    outs = oracle_step(grads, state, hp)
+    done, rest = 3 * 4096, slice(3 * 4096, n)
+    for name, t, ref, old in zip(("master", "m", "v"), (s.master, s.m, s.v), state, before):
+        got = f32(t)
+        assert_bits(name, got[:done], ref[:done], "f32")
+        assert_bits(name + " untouched", got[rest], old[rest], "f32")
+    step()                                  # disarmed: a normal full step
+    torch.cuda.synchronize()
+    capi.cc_inject_launch_failure(-1)
