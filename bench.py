@@ -401,6 +401,12 @@ def run_ours(args):
         result["overlap"] = run_overlap(args, wk, dev, [args.bucket_mib])
         result["overlap_rank_share"] = run_overlap(args, wk, dev, [args.bucket_mib],
                                                    rank_share=True)
+        # the overlapped arm on a static SM partition (green contexts), at the
+        # partition sizes measured best for each mode
+        result["overlap_partitioned"] = {
+            "all_replicas_96_sms": run_overlap(args, wk, dev, [args.bucket_mib], comm_sms=96),
+            "rank_share_48_sms": run_overlap(args, wk, dev, [args.bucket_mib],
+                                             rank_share=True, comm_sms=48)}
         if not args.no_sweep:
             keep = ("bucket_mib", "num_buckets", "t_bwd_ms", "t_comm_ms",
                     "t_step_overlap_ms", "t_step_seq_ms", "exposed_ms",
@@ -646,7 +652,7 @@ def shard_range(begin, end, count, index):
     return lo, hi
 
 
-def run_overlap(args, wk, dev, mibs, rank_share=False):
+def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0):
     """Exposed time of the bucketed step behind a proxy backward of 24 layers
     x 3 bf16 GEMMs (M=8192, N=K=1024); buckets planned at each size.
 
@@ -681,7 +687,7 @@ def run_overlap(args, wk, dev, mibs, rank_share=False):
             gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
             warmup=args.warmup, iters=args.overlap_iters,
             max_ctas=args.overlap_ctas, stream_priority=args.stream_priority,
-            **step_args(wk, w.step))
+            comm_sms=comm_sms, **step_args(wk, w.step))
         r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
         r["bucket_mib"] = mib
         r["mode"] = "rank share (1/R of each bucket)" if rank_share else "all R replicas"

@@ -55,7 +55,7 @@ class cc_overlap_cfg(ctypes.Structure):
         ("gemm_m", _i), ("gemm_n", _i), ("gemm_k", _i),
         ("gemm_a", _vp), ("gemm_b", _vp), ("gemm_c", _vp),
         ("warmup", _i), ("iters", _i), ("max_ctas", _i),
-        ("stream_priority", _i),
+        ("stream_priority", _i), ("comm_sms", _i),
     ]
 
 
@@ -63,7 +63,7 @@ class cc_overlap_result(ctypes.Structure):
     _fields_ = [
         ("t_bwd_ms", _f), ("t_comm_ms", _f), ("t_step_overlap_ms", _f),
         ("t_step_seq_ms", _f), ("exposed_ms", _f), ("exposed_bound_ms", _f),
-        ("num_buckets", _i),
+        ("num_buckets", _i), ("comm_sms", _i), ("compute_sms", _i),
     ]
 
 
@@ -276,7 +276,7 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
                      grad_scale: float, num_layers: int, gemms_per_layer: int,
                      gemm_m: int, gemm_n: int, gemm_k: int, gemm_a, gemm_b,
                      gemm_c, warmup: int = 3, iters: int = 20,
-                     max_ctas: int = 0, stream_priority: int = 0,
+                     max_ctas: int = 0, stream_priority: int = 0, comm_sms: int = 0,
                      acc=None) -> Dict[str, float]:
     B = len(buckets)
     keep = dict(
@@ -298,7 +298,7 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
         gemms_per_layer=gemms_per_layer, gemm_m=gemm_m, gemm_n=gemm_n,
         gemm_k=gemm_k, gemm_a=_addr(gemm_a), gemm_b=_addr(gemm_b),
         gemm_c=_addr(gemm_c), warmup=warmup, iters=iters, max_ctas=max_ctas,
-        stream_priority=stream_priority)
+        stream_priority=stream_priority, comm_sms=comm_sms)
     res = cc_overlap_result()
     _check(lib().cc_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
            "cc_overlap_bench")

@@ -11,8 +11,17 @@
 // synchronous schedule (backward, then reduction and optimizer, in strict
 // phases) is the sequential arm.  Stream ordering uses events only: no
 // kernel waits on a flag.
+//
+// The reduction is an SM kernel that needs most SMs to stream at HBM speed,
+// and cuBLAS's GEMMs occupy every SM, so left to the block scheduler the two
+// take turns.  With comm_sms > 0 the overlapped arm runs on a spatial
+// partition instead: two green contexts with disjoint SM sets, the buckets'
+// stream on comm_sms SMs and the GEMMs' stream on the rest.  The other arms
+// keep the whole GPU, so exposed time is still measured against the
+// unpartitioned backward.
 
 #include <cublas_v2.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -23,16 +32,66 @@
 namespace ccdp {
 namespace {
 
+// Green-context driver calls, resolved through the runtime (no link-time
+// libcuda).
+struct GreenApi {
+    decltype(&cuDeviceGetDevResource) get_resource = nullptr;
+    decltype(&cuDevSmResourceSplitByCount) split = nullptr;
+    decltype(&cuDevResourceGenerateDesc) make_desc = nullptr;
+    decltype(&cuGreenCtxCreate) create = nullptr;
+    decltype(&cuGreenCtxDestroy) destroy = nullptr;
+    decltype(&cuGreenCtxStreamCreate) stream_create = nullptr;
+    decltype(&cuStreamDestroy) stream_destroy = nullptr;
+    bool ok = false;
+};
+
+template <typename F>
+bool resolve(F *fn, const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 13000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return false;
+    *fn = reinterpret_cast<F>(p);
+    return true;
+}
+
+const GreenApi &green_api() {
+    static const GreenApi api = [] {
+        GreenApi a;
+        a.ok = resolve(&a.get_resource, "cuDeviceGetDevResource") &&
+               resolve(&a.split, "cuDevSmResourceSplitByCount") &&
+               resolve(&a.make_desc, "cuDevResourceGenerateDesc") &&
+               resolve(&a.create, "cuGreenCtxCreate") &&
+               resolve(&a.destroy, "cuGreenCtxDestroy") &&
+               resolve(&a.stream_create, "cuGreenCtxStreamCreate") &&
+               resolve(&a.stream_destroy, "cuStreamDestroy");
+        return a;
+    }();
+    return api;
+}
+
 struct Resources {
     cudaStream_t comp = nullptr, side = nullptr;
     cudaEvent_t start = nullptr, stop = nullptr, side_done = nullptr;
     std::vector<cudaEvent_t> layer;
     cublasHandle_t blas = nullptr;
+    // the spatial partition of the overlapped arm (comm_sms > 0)
+    CUgreenCtx green_comp = nullptr, green_side = nullptr;
+    CUstream gcomp = nullptr, gside = nullptr;
+    int comm_sms = 0, compute_sms = 0;
 
     ~Resources() {
         if (comp) cudaStreamSynchronize(comp);
         if (side) cudaStreamSynchronize(side);
+        const GreenApi &g = green_api();
+        if (gcomp) cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(gcomp));
+        if (gside) cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(gside));
         if (blas) cublasDestroy(blas);
+        if (gcomp) g.stream_destroy(gcomp);
+        if (gside) g.stream_destroy(gside);
+        if (green_comp) g.destroy(green_comp);
+        if (green_side) g.destroy(green_side);
         for (cudaEvent_t e : layer)
             if (e) cudaEventDestroy(e);
         if (start) cudaEventDestroy(start);
@@ -42,6 +101,44 @@ struct Resources {
         if (side) cudaStreamDestroy(side);
     }
 };
+
+// Split the current device's SMs into comm_sms (rounded up by the driver to
+// its partition granularity) for the buckets and the rest for the GEMMs.
+int make_partition(int want, int prio_comp, int prio_side, Resources &res) {
+    const GreenApi &g = green_api();
+    if (!g.ok) return fail(CC_ERR_UNSUPPORTED, "green contexts unavailable in this driver");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    CUdevResource all{}, part{}, rest{};
+    if (g.get_resource(static_cast<CUdevice>(dev), &all, CU_DEV_RESOURCE_TYPE_SM) != CUDA_SUCCESS)
+        return fail(CC_ERR_CUDA, "cuDeviceGetDevResource failed");
+    if (want >= static_cast<int>(all.sm.smCount))
+        return fail(CC_ERR_INVALID, "comm_sms=%d must be below the %u SMs", want,
+                    all.sm.smCount);
+    unsigned groups = 1;
+    CUresult r = g.split(&part, &groups, &all, &rest, 0, static_cast<unsigned>(want));
+    if (r != CUDA_SUCCESS || groups != 1 || rest.sm.smCount == 0)
+        return fail(CC_ERR_INVALID, "cannot split %u SMs into %d + rest (CUresult %d)",
+                    all.sm.smCount, want, static_cast<int>(r));
+    CUdevResourceDesc dpart = nullptr, drest = nullptr;
+    if (g.make_desc(&dpart, &part, 1) != CUDA_SUCCESS ||
+        g.make_desc(&drest, &rest, 1) != CUDA_SUCCESS)
+        return fail(CC_ERR_CUDA, "cuDevResourceGenerateDesc failed");
+    if (g.create(&res.green_side, dpart, static_cast<CUdevice>(dev),
+                 CU_GREEN_CTX_DEFAULT_STREAM) != CUDA_SUCCESS ||
+        g.create(&res.green_comp, drest, static_cast<CUdevice>(dev),
+                 CU_GREEN_CTX_DEFAULT_STREAM) != CUDA_SUCCESS)
+        return fail(CC_ERR_CUDA, "cuGreenCtxCreate failed");
+    if (g.stream_create(&res.gside, res.green_side, CU_STREAM_NON_BLOCKING, prio_side) !=
+            CUDA_SUCCESS ||
+        g.stream_create(&res.gcomp, res.green_comp, CU_STREAM_NON_BLOCKING, prio_comp) !=
+            CUDA_SUCCESS)
+        return fail(CC_ERR_CUDA, "cuGreenCtxStreamCreate failed");
+    res.comm_sms = static_cast<int>(part.sm.smCount);
+    res.compute_sms = static_cast<int>(rest.sm.smCount);
+    return CC_OK;
+}
 
 struct Bench {
     const cc_overlap_cfg &cfg;
@@ -64,13 +161,17 @@ struct Bench {
         return CUBLAS_STATUS_SUCCESS;
     }
 
+    // Streams of the arm being run (the partitioned pair for the overlapped
+    // arm when a partition exists, else the whole-GPU pair).
+    cudaStream_t comp = nullptr, side = nullptr;
+
     int backward(bool record_layers) {
         for (int l = cfg.num_layers - 1; l >= 0; --l) {
             const cublasStatus_t st = gemms();
             if (st != CUBLAS_STATUS_SUCCESS)
                 return fail(CC_ERR_CUDA, "cublasGemmEx failed (status %d)", static_cast<int>(st));
             if (record_layers) {
-                const cudaError_t e = cudaEventRecord(res.layer[l], res.comp);
+                const cudaError_t e = cudaEventRecord(res.layer[l], comp);
                 if (e != cudaSuccess) return fail_cuda(e, "layer event record");
             }
         }
@@ -91,7 +192,12 @@ struct Bench {
 
     // Runs one arm once and returns its elapsed milliseconds in *ms.
     int arm(int which, float *ms) {
-        cudaError_t e = cudaEventRecord(res.start, res.comp);
+        const bool part = which == 2 && res.gcomp;
+        comp = part ? reinterpret_cast<cudaStream_t>(res.gcomp) : res.comp;
+        side = part ? reinterpret_cast<cudaStream_t>(res.gside) : res.side;
+        if (cublasSetStream(res.blas, comp) != CUBLAS_STATUS_SUCCESS)
+            return fail(CC_ERR_CUDA, "cublasSetStream failed");
+        cudaError_t e = cudaEventRecord(res.start, comp);
         if (e != cudaSuccess) return fail_cuda(e, "start event");
         int st = CC_OK;
         switch (which) {
@@ -99,26 +205,26 @@ struct Bench {
                 st = backward(false);
                 break;
             case 1:  // all buckets alone, on the compute stream
-                st = buckets(res.comp, false, 0);
+                st = buckets(comp, false, 0);
                 break;
             case 2: {  // overlapped: ready-driven buckets on the side stream
-                if ((e = cudaStreamWaitEvent(res.side, res.start, 0)) != cudaSuccess)
+                if ((e = cudaStreamWaitEvent(side, res.start, 0)) != cudaSuccess)
                     return fail_cuda(e, "side wait");
                 if ((st = backward(true)) != CC_OK) return st;
-                if ((st = buckets(res.side, true, cfg.max_ctas)) != CC_OK) return st;
-                if ((e = cudaEventRecord(res.side_done, res.side)) != cudaSuccess)
+                if ((st = buckets(side, true, part ? 0 : cfg.max_ctas)) != CC_OK) return st;
+                if ((e = cudaEventRecord(res.side_done, side)) != cudaSuccess)
                     return fail_cuda(e, "side done event");
-                if ((e = cudaStreamWaitEvent(res.comp, res.side_done, 0)) != cudaSuccess)
+                if ((e = cudaStreamWaitEvent(comp, res.side_done, 0)) != cudaSuccess)
                     return fail_cuda(e, "join wait");
                 break;
             }
             case 3:  // naive synchronous: backward, then every bucket
                 if ((st = backward(false)) != CC_OK) return st;
-                st = buckets(res.comp, false, 0);
+                st = buckets(comp, false, 0);
                 break;
         }
         if (st != CC_OK) return st;
-        if ((e = cudaEventRecord(res.stop, res.comp)) != cudaSuccess) return fail_cuda(e, "stop event");
+        if ((e = cudaEventRecord(res.stop, comp)) != cudaSuccess) return fail_cuda(e, "stop event");
         if ((e = cudaEventSynchronize(res.stop)) != cudaSuccess) return fail_cuda(e, "arm sync");
         if ((e = cudaEventElapsedTime(ms, res.start, res.stop)) != cudaSuccess)
             return fail_cuda(e, "elapsed time");
@@ -159,6 +265,7 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     if (c.max_ctas < 0) return fail(CC_ERR_INVALID, "max_ctas=%d must be >= 0", c.max_ctas);
     if (c.stream_priority < 0 || c.stream_priority > 2)
         return fail(CC_ERR_INVALID, "stream_priority=%d must be 0, 1 or 2", c.stream_priority);
+    if (c.comm_sms < 0) return fail(CC_ERR_INVALID, "comm_sms=%d must be >= 0", c.comm_sms);
     if (c.num_buckets < 1 || !c.bucket_begin || !c.bucket_end || !c.bucket_ready_layer)
         return fail(CC_ERR_INVALID, "need at least one bucket");
     for (int b = 0; b < c.num_buckets; ++b) {
@@ -211,8 +318,10 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
             return fail_cuda(e, "layer event create");
     if (cublasCreate(&res.blas) != CUBLAS_STATUS_SUCCESS)
         return fail(CC_ERR_CUDA, "cublasCreate failed");
-    if (cublasSetStream(res.blas, res.comp) != CUBLAS_STATUS_SUCCESS)
-        return fail(CC_ERR_CUDA, "cublasSetStream failed");
+    if (c.comm_sms > 0 &&
+        (st = make_partition(c.comm_sms, c.stream_priority == 2 ? hi : lo,
+                             c.stream_priority == 1 ? hi : lo, res)) != CC_OK)
+        return st;
 
     Bench bench{c, slabs, sc, res};
     cc_overlap_result r{};
@@ -223,6 +332,8 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     r.exposed_ms = r.t_step_overlap_ms - r.t_bwd_ms;
     r.exposed_bound_ms = std::max(0.0f, r.t_comm_ms - r.t_bwd_ms);
     r.num_buckets = c.num_buckets;
+    r.comm_sms = res.comm_sms;
+    r.compute_sms = res.compute_sms;
     *out = r;
     return CC_OK;
 }

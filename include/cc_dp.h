@@ -329,12 +329,16 @@ typedef struct cc_overlap_cfg {
     int warmup, iters;             /* iters in 1..1000 */
     int max_ctas;                  /* bucket kernels' CTA cap while overlapped; 0 = full */
     int stream_priority;           /* 0: equal; 1: side stream high; 2: compute stream high */
+    int comm_sms;                  /* > 0: overlapped arm on a spatial partition (green
+                                      contexts): buckets on comm_sms SMs (rounded up to the
+                                      driver's granularity), GEMMs on the rest; 0: none */
 } cc_overlap_cfg;
 
 typedef struct cc_overlap_result {
     float t_bwd_ms, t_comm_ms, t_step_overlap_ms, t_step_seq_ms;
     float exposed_ms, exposed_bound_ms;
     int num_buckets;
+    int comm_sms, compute_sms;     /* the partition's SM counts (0 without one) */
 } cc_overlap_result;
 
 CC_API int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out);
