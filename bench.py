@@ -17,7 +17,10 @@ C ABI.  Printed as one JSON line (rank 0):
   overlap    the step-time decomposition of the bucketed step behind a
              proxy backward of bf16 GEMMs: T_bwd, T_comm, overlapped and
              sequential step times, exposed ms
-  cpu_baseline  the oracle (single-threaded C) on a bounded sample
+  launch_floor  the small L2-resident case (R=2, 1M parameters): single
+             launches after an L2 flush, back to back, and in a CUDA graph
+  cpu_baseline  the oracle (single-threaded C) on a bounded sample, and
+             split over every host core
 
 `--impl reference` times the oracle alone on the host cores (the reference
 arm).  Under torchrun (N > 1) every rank runs its own independent step on
@@ -275,16 +278,59 @@ def oracle_sample_inputs(R, sample, seed_offset=0):
     return g16, st, hp, sample
 
 
-def time_oracle(R, sample, min_seconds, max_seconds):
-    import oracle
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleRunner:
+    """The oracle's step over a sample, on one thread or split into
+    contiguous element chunks over `threads` host threads.  Each chunk is
+    one unchanged oracle call (the step is elementwise, so the bits do not
+    depend on the split); ctypes releases the GIL for the C call, so the
+    chunks run in parallel."""
+
+    def __init__(self, g16, st, hp, threads: int):
+        self.hp, self.threads = hp, max(1, threads)
+        n = st[0].size
+        cuts = [n * k // self.threads // 8 * 8 for k in range(self.threads)] + [n]
+        self.chunks = [([g[a:b] for g in g16], [x[a:b] for x in st])
+                       for a, b in zip(cuts, cuts[1:]) if b > a]
+        self.pool = None
+        if len(self.chunks) > 1:
+            from concurrent.futures import ThreadPoolExecutor
+            self.pool = ThreadPoolExecutor(max_workers=len(self.chunks))
+
+    def step(self):
+        import oracle
+        if self.pool is None:
+            for g, st in self.chunks:
+                oracle.fused_dp_step(g, *st, **self.hp)
+            return
+        futs = [self.pool.submit(oracle.fused_dp_step, g, *st, **self.hp)
+                for g, st in self.chunks]
+        for f in futs:
+            f.result()
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.shutdown()
+
+
+def time_oracle(R, sample, min_seconds, max_seconds, threads=1):
     g16, st, hp, sample = oracle_sample_inputs(R, sample)
+    runner = OracleRunner(g16, st, hp, threads)
+    runner.step()                                  # warm the pool and pages
     passes, t0 = 0, time.perf_counter()
     while True:
-        oracle.fused_dp_step(g16, *st, **hp)
+        runner.step()
         passes += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or el >= max_seconds:
             break
+    runner.close()
     return sample * passes / el, sample, passes, el
 
 
@@ -393,6 +439,8 @@ def run_ours(args):
         result["unfused"] = run_unfused(args, wk, stream, ms)
     if not args.no_tp and not args.small:
         result["tp_matmul_allreduce"] = run_tp(args, dev)
+    if not args.no_launch_floor and not args.small:
+        result["launch_floor"] = run_launch_floor(args, dev)
     if not args.no_accum and not args.small:
         result["accumulation"] = run_accumulation(args, wk, stream)
     if not args.no_e2e:
@@ -423,9 +471,104 @@ def run_ours(args):
             "value": round(v), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"first {sample:,} slab elements of the same workload (R={R}), "
                        f"{passes} passes in {el:.1f} s, single-threaded C oracle")}
+        cores = host_cores()
+        if cores > 1:
+            va, sa, pa, ela = time_oracle(R, args.cpu_sample * 4, 5.0, 15.0, threads=cores)
+            result["cpu_baseline"]["all_cores"] = {
+                "value": round(va), "unit": UNIT, "cores": cores,
+                "sample": (f"first {sa:,} slab elements, {pa} passes in {ela:.1f} s, "
+                           f"split into {cores} contiguous chunks, one oracle call "
+                           "per chunk on its own thread")}
     if rank == 0:
         print(json.dumps(result), flush=True)
     return result
+
+
+def run_launch_floor(args, dev, reps=100, samples=50):
+    """The small flat case: R = 2, 1,048,576 parameters, one bucket, step 1
+    from m = v = 0.  Its 33.5 MB per step ((4R + 24) bytes per parameter)
+    fit in the 129 MB L2, so this measures the launch and L2 floor, three
+    ways:
+      flushed  one launch at a time, a 512 MiB write before each (the
+               step's inputs come from HBM), median over `samples`
+      warm     `reps` launches back to back from the stream (L2-resident)
+      graph    the same `reps` launches captured once in a CUDA graph and
+               replayed, median over `samples` replays."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+
+    w = wl.flat_1m_r2()
+    R, n = w.R, w.n
+    grads = wl.make_grads(R, n, w.grad_sigma, device=dev)
+    master, m, v = wl.make_state(n, w.step, w.grad_sigma, device=dev)
+    outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    hp = {k: getattr(w, k) for k in ("lr", "beta1", "beta2", "eps",
+                                     "weight_decay", "step", "grad_scale")}
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    step_bytes = (4 * R + 24) * n
+
+    def step(stream):
+        capi.cc_fused_dp_step(grads, master, m, v, outs, n, R, 0, stream=stream, **hp)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step(stream)
+    torch.cuda.synchronize()
+
+    pairs = []
+    for _ in range(samples):
+        capi.cc_l2_flush(flush, flush.numel(), stream=stream)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        step(stream)
+        e1.record(stream)
+        pairs.append((e0, e1))
+    torch.cuda.synchronize()
+    flushed_us = statistics.median(a.elapsed_time(b) for a, b in pairs) * 1e3
+
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(reps):
+        step(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    warm_us = e0.elapsed_time(e1) * 1e3 / reps
+
+    out = {"workload": f"flat slab of {n:,} parameters, R={R}, one bucket, step 1, "
+                       "m = v = 0, wd 0",
+           "bytes_per_step": step_bytes,
+           "flushed_us": round(flushed_us, 2),
+           "flushed_gbs": round(step_bytes / (flushed_us * 1e-6) / 1e9, 1),
+           "warm_us": round(warm_us, 2),
+           "warm_gbs": round(step_bytes / (warm_us * 1e-6) / 1e9, 1),
+           "reps": reps}
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream()
+            for _ in range(reps):
+                step(cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        pairs = []
+        for _ in range(samples):
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            pairs.append((e0, e1))
+        torch.cuda.synchronize()
+        graph_us = statistics.median(a.elapsed_time(b) for a, b in pairs) * 1e3 / reps
+        out.update(graph_us=round(graph_us, 2),
+                   graph_gbs=round(step_bytes / (graph_us * 1e-6) / 1e9, 1))
+        del graph
+    except RuntimeError as e:        # capture refused: report, keep the run
+        out["graph_error"] = str(e).splitlines()[0][:200]
+    return out
 
 
 def run_tp(args, dev, R=8, m=8192, n=3072, k=12288, chunk_list=(1, 2, 4, 8, 16)):
@@ -712,16 +855,22 @@ def run_reference(args):
     obuild.build()
     import oracle
     R = 8
+    threads = args.ref_threads or host_cores()
     g16, st, hp, sample = oracle_sample_inputs(R, args.ref_sample)
+    runner = OracleRunner(g16, st, hp, threads)
     for _ in range(args.warmup):
-        oracle.fused_dp_step(g16, *st, **hp)
+        runner.step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.fused_dp_step(g16, *st, **hp)
+        runner.step()
     el = time.perf_counter() - t0
+    runner.close()
+    threads = len(runner.chunks)
     value = sample * args.steps / el
     desc = (f"first {sample:,} slab elements of the BERT-large R=8 workload per "
-            "step, single-threaded C oracle")
+            + ("step, single-threaded C oracle" if threads == 1 else
+               f"step, split into {threads} contiguous chunks, one C oracle call "
+               "per chunk on its own host thread"))
     result = {
         "metric": METRIC, "value": round(value), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -730,7 +879,7 @@ def run_reference(args):
         "data": "synthetic", "impl": "reference",
         "config": {"workload": "BERT-large parameter list, R=8, 25 MiB buckets "
                    "(bounded sample per step)", "R": R, "sample_elements": sample},
-        "cpu_baseline": {"value": round(value), "unit": UNIT, "cores": 1,
+        "cpu_baseline": {"value": round(value), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -758,6 +907,8 @@ def parse_args(argv=None):
                    help="profile case: only the tensor-parallel path, with this many rows")
     p.add_argument("--no-tp", action="store_true",
                    help="skip the tensor-parallel MatMul-then-AllReduce overlap")
+    p.add_argument("--no-launch-floor", action="store_true",
+                   help="skip the small L2-resident case (single launches, CUDA graph)")
     p.add_argument("--no-accum", action="store_true",
                    help="skip timing gradient accumulation (k=4)")
     p.add_argument("--no-unfused", action="store_true",
@@ -772,7 +923,9 @@ def parse_args(argv=None):
                    help="skip the 1/4/25/100/500 MiB bucket-size sweep")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample", type=int, default=1 << 22)
-    p.add_argument("--ref-sample", type=int, default=1 << 20)
+    p.add_argument("--ref-sample", type=int, default=1 << 22)
+    p.add_argument("--ref-threads", type=int, default=0,
+                   help="reference arm: host threads (0 = every core this process may use)")
     a = p.parse_args(argv)
     a.warmup = max(3, a.warmup)     # at least 3 untimed warm-up steps
     return a

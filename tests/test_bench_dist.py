@@ -74,3 +74,24 @@ def test_shard_ranges_partition_each_bucket():
             sizes = [b - a for a, b in parts[:-1]]
             if sizes:
                 assert max(sizes) - min(sizes) <= 8
+
+
+def test_oracle_split_over_threads_gives_the_same_bits():
+    """The CPU baseline's threaded form (contiguous chunks, one oracle call
+    each) leaves master/m/v bit-identical to one call over the sample."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    runs = []
+    for threads in (1, 3, 8):
+        g16, st, hp, n = bench.oracle_sample_inputs(4, 10_007)
+        runner = bench.OracleRunner(g16, st, hp, threads)
+        assert len(runner.chunks) == threads
+        assert sum(c[1][0].size for c in runner.chunks) == n
+        runner.step()
+        runner.step()
+        runner.close()
+        runs.append([x.view(np.uint32).copy() for x in st])
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            assert np.array_equal(a, b)

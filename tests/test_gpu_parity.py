@@ -116,6 +116,29 @@ def test_bucket_entry_point_over_planned_buckets(max_ctas):
     compare_all(s, state, oracle_step(grads, state, hp))
 
 
+def test_consecutive_steps_captured_in_a_cuda_graph():
+    """Two consecutive multi-bucket steps captured in one CUDA graph and
+    replayed twice: inside a step the buckets chain by programmatic launch,
+    and a step's first bucket waits for all of the previous step.  Same bits
+    as four oracle steps."""
+    n = 1024 * 1024 + 8 * 13 + 3
+    s = new_slabs(*random_inputs(4, n, seed=31, step=2))
+    hp = dict(HP10, step=2)
+    gpu_step(s, hp, bucket_bytes=256 << 10)      # per-device state set up
+    torch.cuda.synchronize()
+    grads, state, _ = host_copy(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in (3, 4):
+            gpu_step(s, dict(hp, step=t), bucket_bytes=256 << 10)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for t in (3, 4, 3, 4):
+        outs = oracle_step(grads, state, dict(hp, step=t))
+    compare_all(s, state, outs, label="graph ")
+
+
 @pytest.mark.parametrize("R", [1, 2, 3, 8, 16])
 def test_integer_gradients_sum_exactly(R):
     n = 100_003
