@@ -361,9 +361,19 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     cuts = uniform_buckets(n_slab, bb)
+    acc = None
+    if args.small and args.reducing:
+        # the reducing step of an accumulated step: fp32 accumulators that
+        # stand for three earlier micro-steps
+        acc = [g.float() * 3.0 for g in wk["grads"]]
+        torch.cuda.synchronize()
 
     def one_step(step):
-        if args.engine_ctas > 0:
+        if acc is not None:
+            capi.cc_fused_dp_step_accum(wk["grads"], acc, wk["master"], wk["m"], wk["v"],
+                                        wk["outs"], n_slab, R, bb, accum_k=4,
+                                        stream=stream, **step_args(wk, step))
+        elif args.engine_ctas > 0:
             # the bulk-copy engine on a budget of SMs, bucket by bucket
             for b, e in cuts:
                 capi.cc_fused_dp_bucket(wk["grads"], None, wk["master"], wk["m"],
@@ -395,19 +405,20 @@ def run_ours(args):
     ms_local = ev0.elapsed_time(ev1) / args.steps
     ms, value = aggregate(ms_local, float(n_params), world, device=dev)
 
-    bytes_per_param = 4 * R + 24
+    bytes_per_param = 4 * R + 24 if acc is None else 8 * R + 24
     launches = launches_per_step(n_slab, bb)
     per_launch_elems = n_slab / launches
     launch_ms = ms_local / launches           # launches run back to back
     achieved = bytes_per_param * per_launch_elems / (launch_ms * 1e-3) / 1e9
     peak, peak_src = measured_hbm_peak()
-    tpp = profiled_traffic_per_param(R) if args.engine_ctas == 0 else None
+    tpp = profiled_traffic_per_param(R) if args.engine_ctas == 0 and acc is None else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": (round(tpp * per_launch_elems) if tpp else None),
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": round(bytes_per_param * per_launch_elems),
-                "kernel": (f"fused_step_bulk_kernel<R={R}> on {args.engine_ctas} SMs"
+                "kernel": (f"fused_step_kernel<R={R}, accumulators>" if acc is not None else
+                           f"fused_step_bulk_kernel<R={R}> on {args.engine_ctas} SMs"
                            if args.engine_ctas > 0 else f"fused_step_kernel<R={R}>"),
                 "launches_per_step": launches}
 
@@ -426,7 +437,8 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (R={R} emulated per GPU)",
             "l2": "inputs 14.8 GB per GPU, larger than the 129 MB L2: no flush",
         } if not args.small else {
-            "workload": f"profile case: flat slab of {n_slab} elements, R={R}, one bucket",
+            "workload": (f"profile case: flat slab of {n_slab} elements, R={R}, one bucket"
+                         + (", reducing step with fp32 accumulators" if acc is not None else "")),
             "R": R, "n_slab": n_slab, "bucket_bytes": 0},
         "hbm_gbs": round(bytes_per_param * n_slab / (ms * 1e-3) / 1e9, 1),
         "hbm_pct_of_8tbs": round(100 * bytes_per_param * n_slab / (ms * 1e-3) / 8e12, 2),
@@ -902,6 +914,8 @@ def parse_args(argv=None):
     p.add_argument("--small", type=int, default=0,
                    help="profile case: a flat R=8 slab of this many elements, "
                         "one bucket, device timing only")
+    p.add_argument("--reducing", action="store_true",
+                   help="with --small: time the reducing step with fp32 accumulators")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--tp-only", type=int, default=0,
                    help="profile case: only the tensor-parallel path, with this many rows")

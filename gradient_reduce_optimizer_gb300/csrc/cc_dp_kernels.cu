@@ -8,7 +8,8 @@
 //   * one thread owns 8 consecutive elements, so each replica's gradient and
 //     parameter is one 16-byte access and each fp32 array two; a warp
 //     touches 512 contiguous bytes per bf16 stream and 1 KiB per fp32
-//     stream;
+//     stream.  The reducing step with fp32 accumulators takes 4 elements
+//     per thread instead (its loads are three times larger);
 //   * all of a thread's loads (R + 6 vectors, R = 8 gives 224 bytes) are
 //     issued before any arithmetic, so each thread has them all in flight;
 //   * streaming cache hints (ld/st .cs, evict-first) keep the single-use
@@ -56,6 +57,9 @@
 #endif
 #ifndef CC_DP_PDL
 #define CC_DP_PDL 1            // chain consecutive buckets with programmatic launch
+#endif
+#ifndef CC_DP_ACC_HALF
+#define CC_DP_ACC_HALF 1       // accumulator variant: 4 elements per thread
 #endif
 
 namespace ccdp {
@@ -140,6 +144,54 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     for (int r = 0; r < R; ++r) __stcs(p.out[r] + vi, o);
 }
 
+// The reducing step with accumulators on half vectors: one thread owns 4
+// consecutive elements.  The R fp32 accumulators triple a thread's loads
+// (R = 8: 480 bytes for a full vector), and holding a full vector in flight
+// takes 142 registers, one 256-thread block per SM, whose warps then move
+// through load, arithmetic and store together.  Half a vector (240 bytes in
+// flight, 8-byte gradient and parameter accesses, still whole 32-byte
+// sectors per warp) leaves room for several independent blocks per SM.
+template <int R>
+__device__ __forceinline__ void fused_half_acc(const FusedParams &p, size_t hv) {
+    uint2 gq[R];
+    float4 aq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) gq[r] = __ldcs(reinterpret_cast<const uint2 *>(p.g[r]) + hv);
+#pragma unroll
+    for (int r = 0; r < R; ++r) aq[r] = __ldcs(p.acc[r] + hv);
+    const float4 w = __ldcs(p.master + hv);
+    const float4 m = __ldcs(p.m + hv);
+    const float4 v = __ldcs(p.v + hv);
+
+    // acc[0] + g[0], then s + (acc[r] + g[r]) in replica order.
+    float s[4] = {add_bf16_lo(aq[0].x, gq[0].x), add_bf16_hi(aq[0].y, gq[0].x),
+                  add_bf16_lo(aq[0].z, gq[0].y), add_bf16_hi(aq[0].w, gq[0].y)};
+#pragma unroll
+    for (int r = 1; r < R; ++r) {
+        s[0] = __fadd_rn(s[0], add_bf16_lo(aq[r].x, gq[r].x));
+        s[1] = __fadd_rn(s[1], add_bf16_hi(aq[r].y, gq[r].x));
+        s[2] = __fadd_rn(s[2], add_bf16_lo(aq[r].z, gq[r].y));
+        s[3] = __fadd_rn(s[3], add_bf16_hi(aq[r].w, gq[r].y));
+    }
+
+    float pw[4] = {w.x, w.y, w.z, w.w};
+    float mm[4] = {m.x, m.y, m.z, m.w};
+    float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) adamw(s[k], pw[k], mm[k], vv[k], p.c);
+
+    __stcs(p.master + hv, make_float4(pw[0], pw[1], pw[2], pw[3]));
+    __stcs(p.m + hv, make_float4(mm[0], mm[1], mm[2], mm[3]));
+    __stcs(p.v + hv, make_float4(vv[0], vv[1], vv[2], vv[3]));
+    const uint2 o = make_uint2(pack_bf16x2(pw[0], pw[1]), pack_bf16x2(pw[2], pw[3]));
+#pragma unroll
+    for (int r = 0; r < R; ++r) __stcs(reinterpret_cast<uint2 *>(p.out[r]) + hv, o);
+}
+
+// Threads per 8-element vector of the fused kernel.
+template <bool ACC>
+__host__ __device__ constexpr int threads_per_vector() { return (ACC && CC_DP_ACC_HALF) ? 2 : 1; }
+
 // One element of the partial last vector (scalar accesses).
 template <int R, bool ACC>
 __device__ __forceinline__ void fused_scalar(const FusedParams &p, size_t i) {
@@ -180,9 +232,14 @@ __global__ void __launch_bounds__(kThreads, CC_DP_MIN_BLOCKS)
 fused_step_kernel(const __grid_constant__ FusedParams p) {
     allow_dependents_to_launch();
     const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
-    for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
-         i < p.num_vec; i += stride)
-        fused_vector<R, ACC>(p, p.vec_begin + i);
+    const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if constexpr (threads_per_vector<ACC>() == 2) {
+        for (size_t i = first; i < 2 * p.num_vec; i += stride)
+            fused_half_acc<R>(p, 2 * p.vec_begin + i);
+    } else {
+        for (size_t i = first; i < p.num_vec; i += stride)
+            fused_vector<R, ACC>(p, p.vec_begin + i);
+    }
     if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len)
         fused_scalar<R, ACC>(p, p.tail_begin + threadIdx.x);
     wait_for_predecessor_grid();
@@ -203,39 +260,51 @@ struct AccumParams {
     int tail_len;
 };
 
+template <int R>
+__device__ __forceinline__ void accumulate_first(const AccumParams &p, size_t vi) {
+    uint4 gq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) gq[r] = __ldcs(p.g[r] + vi);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float t[8];
+        widen8(gq[r], t);
+        __stcs(p.acc[r] + 2 * vi, make_float4(t[0], t[1], t[2], t[3]));
+        __stcs(p.acc[r] + 2 * vi + 1, make_float4(t[4], t[5], t[6], t[7]));
+    }
+}
+
+template <int R>
+__device__ __forceinline__ void accumulate_later(const AccumParams &p, size_t vi) {
+    uint4 gq[R];
+    float4 aq[R][2];
+#pragma unroll
+    for (int r = 0; r < R; ++r) gq[r] = __ldcs(p.g[r] + vi);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        aq[r][0] = __ldcs(p.acc[r] + 2 * vi);
+        aq[r][1] = __ldcs(p.acc[r] + 2 * vi + 1);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float a[8] = {aq[r][0].x, aq[r][0].y, aq[r][0].z, aq[r][0].w,
+                      aq[r][1].x, aq[r][1].y, aq[r][1].z, aq[r][1].w};
+        add8_bf16(a, gq[r]);
+        __stcs(p.acc[r] + 2 * vi, make_float4(a[0], a[1], a[2], a[3]));
+        __stcs(p.acc[r] + 2 * vi + 1, make_float4(a[4], a[5], a[6], a[7]));
+    }
+}
+
 template <int R, bool FIRST>
 __global__ void __launch_bounds__(kThreads)
 accumulate_kernel(const __grid_constant__ AccumParams p) {
     const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
-    for (size_t i = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
-         i < p.num_vec; i += stride) {
-        uint4 gq[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) gq[r] = __ldcs(p.g[r] + i);
-        if constexpr (FIRST) {
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float t[8];
-                widen8(gq[r], t);
-                __stcs(p.acc[r] + 2 * i, make_float4(t[0], t[1], t[2], t[3]));
-                __stcs(p.acc[r] + 2 * i + 1, make_float4(t[4], t[5], t[6], t[7]));
-            }
-        } else {
-            float4 aq[R][2];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                aq[r][0] = __ldcs(p.acc[r] + 2 * i);
-                aq[r][1] = __ldcs(p.acc[r] + 2 * i + 1);
-            }
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                float a[8] = {aq[r][0].x, aq[r][0].y, aq[r][0].z, aq[r][0].w,
-                              aq[r][1].x, aq[r][1].y, aq[r][1].z, aq[r][1].w};
-                add8_bf16(a, gq[r]);
-                __stcs(p.acc[r] + 2 * i, make_float4(a[0], a[1], a[2], a[3]));
-                __stcs(p.acc[r] + 2 * i + 1, make_float4(a[4], a[5], a[6], a[7]));
-            }
-        }
+    const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    for (size_t i = first; i < p.num_vec; i += stride) {
+        if constexpr (FIRST)
+            accumulate_first<R>(p, i);
+        else
+            accumulate_later<R>(p, i);
     }
     if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len) {
         const size_t e = p.tail_begin + threadIdx.x;
@@ -372,7 +441,9 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     p.tail_begin = begin + p.num_vec * CC_PAD_ELEMS;
     p.tail_len = static_cast<int>(end - p.tail_begin);
 
-    size_t blocks = div_up(p.num_vec, kThreads);
+    const size_t units = p.num_vec * (acc ? threads_per_vector<true>()
+                                          : threads_per_vector<false>());
+    size_t blocks = div_up(units, kThreads);
     const size_t per_sm = CC_DP_BLOCKS_PER_SM > 0
                               ? static_cast<size_t>(CC_DP_BLOCKS_PER_SM)
                               : static_cast<size_t>(d->fused_blocks_per_sm[s.R][acc ? 1 : 0]);
