@@ -17,6 +17,8 @@ C ABI.  Printed as one JSON line (rank 0):
   overlap    the step-time decomposition of the bucketed step behind a
              proxy backward of bf16 GEMMs: T_bwd, T_comm, overlapped and
              sequential step times, exposed ms
+  gpt2_slice_r4  the same step on 24 GPT-2 8.3B layers (2.7B parameters)
+             at R=4, 76 GB resident
   launch_floor  the small L2-resident case (R=2, 1M parameters): single
              launches after an L2 flush, back to back, and in a CUDA graph
   cpu_baseline  the oracle (single-threaded C) on a bounded sample, and
@@ -188,23 +190,29 @@ class ClockSampler:
 # Workload
 # ---------------------------------------------------------------------------
 
-def build_workload(device, R_override=None, bucket_mib=25):
+def build_workload(device, R_override=None, bucket_mib=25, preset=None):
+    """Device slabs of a planned workload (BERT-large R=8 unless `preset`
+    names another): gradients scaled per layer where the preset says so,
+    pre-multiplied by its loss scale, zero on padding."""
     import torch
     from gradient_reduce_optimizer_gb300 import capi
     from gradient_reduce_optimizer_gb300 import workloads as wl
 
-    w = wl.bert_large_r8(bucket_bytes=bucket_mib * wl.MiB)
+    w = preset or wl.bert_large_r8(bucket_bytes=bucket_mib * wl.MiB)
     if R_override:
         w.R = R_override
     numel, layer_of = w.numel(), w.layer_of()
     offsets, buckets, n_slab = capi.cc_plan_buckets(numel, w.bucket_bytes)
     lay = wl.element_layer_map(numel, layer_of, offsets, n_slab, device=device)
-    per_layer = wl.layer_scales(max(layer_of) + 1, *w.layer_scale, device=device)
-    scale = per_layer[lay.clamp(min=0).long()]
+    scale = None
+    if w.layer_scale is not None:
+        per_layer = wl.layer_scales(max(layer_of) + 1, *w.layer_scale, device=device)
+        scale = per_layer[lay.clamp(min=0).long()]
     grads = wl.make_grads(w.R, n_slab, w.grad_sigma, device=device,
-                          elem_scale=scale, mask=lay >= 0)
+                          elem_scale=scale, mask=lay >= 0, premultiply=w.grad_scale)
     del lay, scale
-    master, m, v = wl.make_state(n_slab, w.step, w.grad_sigma, device=device)
+    master, m, v = wl.make_state(n_slab, w.step, w.grad_sigma,
+                                 master_sigma=w.master_sigma, device=device)
     outs = [torch.empty(n_slab, dtype=torch.bfloat16, device=device)
             for _ in range(w.R)]
     torch.cuda.synchronize()
@@ -453,6 +461,8 @@ def run_ours(args):
         result["tp_matmul_allreduce"] = run_tp(args, dev)
     if not args.no_launch_floor and not args.small:
         result["launch_floor"] = run_launch_floor(args, dev)
+    if not args.no_gpt2_slice and not args.small:
+        result["gpt2_slice_r4"] = run_gpt2_slice(args, dev)
     if not args.no_accum and not args.small:
         result["accumulation"] = run_accumulation(args, wk, stream)
     if not args.no_e2e:
@@ -494,6 +504,49 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(result), flush=True)
     return result
+
+
+def run_gpt2_slice(args, dev, steps=20):
+    """The fused step on 24 GPT-2 8.3B layers (2,718,867,456 parameters, 288
+    tensors) at R = 4 with loss scale 65536 and 25 MiB buckets: (4R + 24) =
+    40 bytes per parameter, 108.8 GB per step, 76 GB resident in HBM."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+
+    wk = build_workload(dev, preset=wl.gpt2_slice_r4())
+    w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        capi.cc_fused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"], wk["outs"],
+                              n_slab, R, w.bucket_bytes, stream=stream,
+                              **step_args(wk, w.step + i))
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(args.warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    bpp = 4 * R + 24
+    peak, src = measured_hbm_peak()
+    gbs = bpp * n_slab / (ms * 1e-3) / 1e9
+    out = {"workload": ("24 GPT-2 8.3B layers (hidden 3072, FFN 12288), R=4, "
+                        "loss scale 65536, 25 MiB buckets in reverse layer order"),
+           "n_params": w.n, "n_slab": n_slab, "R": R,
+           "launches_per_step": launches_per_step(n_slab, w.bucket_bytes),
+           "ms_per_step": round(ms, 3), "params_per_s": round(w.n / (ms * 1e-3)),
+           "bytes_per_param": bpp, "hbm_gbs": round(gbs, 1),
+           "frac": round(gbs / peak, 4), "peak_source": src, "steps": steps}
+    del wk
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_launch_floor(args, dev, reps=100, samples=50):
@@ -921,6 +974,8 @@ def parse_args(argv=None):
                    help="profile case: only the tensor-parallel path, with this many rows")
     p.add_argument("--no-tp", action="store_true",
                    help="skip the tensor-parallel MatMul-then-AllReduce overlap")
+    p.add_argument("--no-gpt2-slice", action="store_true",
+                   help="skip the 2.7B-parameter GPT-2 slice at R=4 (76 GB)")
     p.add_argument("--no-launch-floor", action="store_true",
                    help="skip the small L2-resident case (single launches, CUDA graph)")
     p.add_argument("--no-accum", action="store_true",
