@@ -3,7 +3,7 @@
 Bar: bit-identical master/m/v and bf16 parameters on every case (NaN
 payloads excepted: a NaN must meet a NaN).  The operation order is fixed in
 include/cc_dp.h and both sides round every binary32 operation separately, so
-the benchmark spec's tolerance (1e-5 relative on fp32 state, 1 bf16 ulp on
+the looser floating-point bar (1e-5 relative on fp32 state, 1 bf16 ulp on
 parameters) is never needed; bit equality is asserted instead.
 
 Element by element at sizes the oracle finishes in seconds (spanning many
