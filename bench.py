@@ -370,14 +370,17 @@ def run_ours(args):
 
     cuts = uniform_buckets(n_slab, bb)
     acc = None
-    if args.small and args.reducing:
-        # the reducing step of an accumulated step: fp32 accumulators that
-        # stand for three earlier micro-steps
+    if args.small and (args.reducing or args.micro):
+        # fp32 accumulators that stand for three earlier micro-steps
         acc = [g.float() * 3.0 for g in wk["grads"]]
         torch.cuda.synchronize()
 
     def one_step(step):
-        if acc is not None:
+        if args.small and args.micro:
+            # profile case: one local micro-step (acc = g, or acc += g)
+            capi.cc_accumulate_local(wk["grads"], acc, n_slab, R, args.micro == "first",
+                                     stream=stream)
+        elif acc is not None:
             capi.cc_fused_dp_step_accum(wk["grads"], acc, wk["master"], wk["m"], wk["v"],
                                         wk["outs"], n_slab, R, bb, accum_k=4,
                                         stream=stream, **step_args(wk, step))
@@ -413,7 +416,9 @@ def run_ours(args):
     ms_local = ev0.elapsed_time(ev1) / args.steps
     ms, value = aggregate(ms_local, float(n_params), world, device=dev)
 
-    bytes_per_param = 4 * R + 24 if acc is None else 8 * R + 24
+    bytes_per_param = (4 * R + 24 if acc is None else
+                       (6 * R if args.micro == "first" else 10 * R) if args.micro else
+                       8 * R + 24)
     launches = launches_per_step(n_slab, bb)
     per_launch_elems = n_slab / launches
     launch_ms = ms_local / launches           # launches run back to back
@@ -425,7 +430,9 @@ def run_ours(args):
                 "traffic": (round(tpp * per_launch_elems) if tpp else None),
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": round(bytes_per_param * per_launch_elems),
-                "kernel": (f"fused_step_kernel<R={R}, accumulators>" if acc is not None else
+                "kernel": (f"accumulate_kernel<R={R}, first={args.micro == 'first'}>"
+                           if args.micro else
+                           f"fused_step_kernel<R={R}, accumulators>" if acc is not None else
                            f"fused_step_bulk_kernel<R={R}> on {args.engine_ctas} SMs"
                            if args.engine_ctas > 0 else f"fused_step_kernel<R={R}>"),
                 "launches_per_step": launches}
@@ -446,7 +453,8 @@ def run_ours(args):
             "l2": "inputs 14.8 GB per GPU, larger than the 129 MB L2: no flush",
         } if not args.small else {
             "workload": (f"profile case: flat slab of {n_slab} elements, R={R}, one bucket"
-                         + (", reducing step with fp32 accumulators" if acc is not None else "")),
+                         + (f", {args.micro} local micro-step" if args.micro else
+                            ", reducing step with fp32 accumulators" if acc is not None else "")),
             "R": R, "n_slab": n_slab, "bucket_bytes": 0},
         "hbm_gbs": round(bytes_per_param * n_slab / (ms * 1e-3) / 1e9, 1),
         "hbm_pct_of_8tbs": round(100 * bytes_per_param * n_slab / (ms * 1e-3) / 8e12, 2),
@@ -969,6 +977,8 @@ def parse_args(argv=None):
                         "one bucket, device timing only")
     p.add_argument("--reducing", action="store_true",
                    help="with --small: time the reducing step with fp32 accumulators")
+    p.add_argument("--micro", choices=("first", "later"), default=None,
+                   help="with --small: time one local micro-step (acc = g, or acc += g)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--tp-only", type=int, default=0,
                    help="profile case: only the tensor-parallel path, with this many rows")

@@ -9,7 +9,8 @@
 //     parameter is one 16-byte access and each fp32 array two; a warp
 //     touches 512 contiguous bytes per bf16 stream and 1 KiB per fp32
 //     stream.  The reducing step with fp32 accumulators takes 4 elements
-//     per thread instead (its loads are three times larger);
+//     per thread instead (its loads are three times larger), and so does
+//     the first accumulation micro-step (a store-heavy widening copy);
 //   * all of a thread's loads (R + 6 vectors, R = 8 gives 224 bytes) are
 //     issued before any arithmetic, so each thread has them all in flight;
 //   * streaming cache hints (ld/st .cs, evict-first) keep the single-use
@@ -60,6 +61,12 @@
 #endif
 #ifndef CC_DP_ACC_HALF
 #define CC_DP_ACC_HALF 1       // accumulator variant: 4 elements per thread
+#endif
+#ifndef CC_DP_PLAIN_HALF
+#define CC_DP_PLAIN_HALF 0     // plain variant: 4 elements per thread (measured: no gain)
+#endif
+#ifndef CC_DP_ACCUM_FIRST_HALF
+#define CC_DP_ACCUM_FIRST_HALF 1  // first micro-step: 4 elements per thread
 #endif
 
 namespace ccdp {
@@ -144,34 +151,56 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     for (int r = 0; r < R; ++r) __stcs(p.out[r] + vi, o);
 }
 
-// The reducing step with accumulators on half vectors: one thread owns 4
-// consecutive elements.  The R fp32 accumulators triple a thread's loads
-// (R = 8: 480 bytes for a full vector), and holding a full vector in flight
-// takes 142 registers, one 256-thread block per SM, whose warps then move
-// through load, arithmetic and store together.  Half a vector (240 bytes in
-// flight, 8-byte gradient and parameter accesses, still whole 32-byte
-// sectors per warp) leaves room for several independent blocks per SM.
-template <int R>
-__device__ __forceinline__ void fused_half_acc(const FusedParams &p, size_t hv) {
+// Half vectors: one thread owns 4 consecutive elements.  A warp's fp32
+// accesses are then one 16-byte access per thread, 512 contiguous bytes per
+// instruction, every 32-byte sector written whole by one store; with 8
+// elements per thread each fp32 store instruction half-fills 32 sectors
+// and the next one fills the other halves.  The bf16 accesses become 8
+// bytes per thread (256 contiguous bytes per warp instruction).  For the
+// reducing step with accumulators it also halves the registers that the
+// loads in flight take (R = 8: 480 bytes for a full vector, 142 registers
+// and one 256-thread block per SM).
+template <int R, bool ACC>
+__device__ __forceinline__ void fused_half(const FusedParams &p, size_t hv) {
     uint2 gq[R];
-    float4 aq[R];
+    float4 aq[ACC ? R : 1];
 #pragma unroll
     for (int r = 0; r < R; ++r) gq[r] = __ldcs(reinterpret_cast<const uint2 *>(p.g[r]) + hv);
+    if constexpr (ACC) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) aq[r] = __ldcs(p.acc[r] + hv);
+        for (int r = 0; r < R; ++r) aq[r] = __ldcs(p.acc[r] + hv);
+    }
     const float4 w = __ldcs(p.master + hv);
     const float4 m = __ldcs(p.m + hv);
     const float4 v = __ldcs(p.v + hv);
 
-    // acc[0] + g[0], then s + (acc[r] + g[r]) in replica order.
-    float s[4] = {add_bf16_lo(aq[0].x, gq[0].x), add_bf16_hi(aq[0].y, gq[0].x),
-                  add_bf16_lo(aq[0].z, gq[0].y), add_bf16_hi(aq[0].w, gq[0].y)};
+    // Plain: g[0], then s + g[r].  Accumulated: acc[0] + g[0], then
+    // s + (acc[r] + g[r]).  Replica order either way.
+    float s[4];
+    if constexpr (ACC) {
+        s[0] = add_bf16_lo(aq[0].x, gq[0].x);
+        s[1] = add_bf16_hi(aq[0].y, gq[0].x);
+        s[2] = add_bf16_lo(aq[0].z, gq[0].y);
+        s[3] = add_bf16_hi(aq[0].w, gq[0].y);
+    } else {
+        s[0] = bf16_lo(gq[0].x);
+        s[1] = bf16_hi(gq[0].x);
+        s[2] = bf16_lo(gq[0].y);
+        s[3] = bf16_hi(gq[0].y);
+    }
 #pragma unroll
     for (int r = 1; r < R; ++r) {
-        s[0] = __fadd_rn(s[0], add_bf16_lo(aq[r].x, gq[r].x));
-        s[1] = __fadd_rn(s[1], add_bf16_hi(aq[r].y, gq[r].x));
-        s[2] = __fadd_rn(s[2], add_bf16_lo(aq[r].z, gq[r].y));
-        s[3] = __fadd_rn(s[3], add_bf16_hi(aq[r].w, gq[r].y));
+        if constexpr (ACC) {
+            s[0] = __fadd_rn(s[0], add_bf16_lo(aq[r].x, gq[r].x));
+            s[1] = __fadd_rn(s[1], add_bf16_hi(aq[r].y, gq[r].x));
+            s[2] = __fadd_rn(s[2], add_bf16_lo(aq[r].z, gq[r].y));
+            s[3] = __fadd_rn(s[3], add_bf16_hi(aq[r].w, gq[r].y));
+        } else {
+            s[0] = add_bf16_lo(s[0], gq[r].x);
+            s[1] = add_bf16_hi(s[1], gq[r].x);
+            s[2] = add_bf16_lo(s[2], gq[r].y);
+            s[3] = add_bf16_hi(s[3], gq[r].y);
+        }
     }
 
     float pw[4] = {w.x, w.y, w.z, w.w};
@@ -190,7 +219,9 @@ __device__ __forceinline__ void fused_half_acc(const FusedParams &p, size_t hv) 
 
 // Threads per 8-element vector of the fused kernel.
 template <bool ACC>
-__host__ __device__ constexpr int threads_per_vector() { return (ACC && CC_DP_ACC_HALF) ? 2 : 1; }
+__host__ __device__ constexpr int threads_per_vector() {
+    return (ACC ? CC_DP_ACC_HALF : CC_DP_PLAIN_HALF) ? 2 : 1;
+}
 
 // One element of the partial last vector (scalar accesses).
 template <int R, bool ACC>
@@ -235,7 +266,7 @@ fused_step_kernel(const __grid_constant__ FusedParams p) {
     const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     if constexpr (threads_per_vector<ACC>() == 2) {
         for (size_t i = first; i < 2 * p.num_vec; i += stride)
-            fused_half_acc<R>(p, 2 * p.vec_begin + i);
+            fused_half<R, ACC>(p, 2 * p.vec_begin + i);
     } else {
         for (size_t i = first; i < p.num_vec; i += stride)
             fused_vector<R, ACC>(p, p.vec_begin + i);
@@ -248,9 +279,13 @@ fused_step_kernel(const __grid_constant__ FusedParams p) {
 // ---------------------------------------------------------------------------
 // Local accumulation micro-step: acc[r] = g[r] on the first micro-step (a
 // copy: no "0 +", so -0 stays -0), acc[r] + g[r] on later ones.  One thread
-// owns one 8-element vector across all R replicas and issues every load of
-// it before any add, like the fused kernel (R x 16 bytes in flight on the
-// first micro-step, R x 48 on later ones); one vector per thread.
+// owns one vector across all R replicas and issues every load of it before
+// any add, like the fused kernel; one vector per thread.  Later micro-steps
+// take 8-element vectors (R x 48 bytes in flight).  The first micro-step is
+// a widening copy that writes twice what it reads; it takes 4-element half
+// vectors so that each fp32 store instruction writes whole sectors (with 8
+// elements per thread each store half-fills 32 sectors and stalls on the
+// store queue: 2.54 against 2.30 ms for the 336M-parameter R=8 slab).
 // ---------------------------------------------------------------------------
 struct AccumParams {
     const uint4 *g[CC_MAX_R];
@@ -272,6 +307,25 @@ __device__ __forceinline__ void accumulate_first(const AccumParams &p, size_t vi
         __stcs(p.acc[r] + 2 * vi, make_float4(t[0], t[1], t[2], t[3]));
         __stcs(p.acc[r] + 2 * vi + 1, make_float4(t[4], t[5], t[6], t[7]));
     }
+}
+
+// Half vector hv (elements 4*hv .. 4*hv+3): one 8-byte load and one
+// 16-byte store per replica, whole sectors per warp instruction.
+template <int R>
+__device__ __forceinline__ void accumulate_first_half(const AccumParams &p, size_t hv) {
+    uint2 gq[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) gq[r] = __ldcs(reinterpret_cast<const uint2 *>(p.g[r]) + hv);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        __stcs(p.acc[r] + hv, make_float4(bf16_lo(gq[r].x), bf16_hi(gq[r].x),
+                                          bf16_lo(gq[r].y), bf16_hi(gq[r].y)));
+}
+
+// Threads per 8-element vector of the accumulation kernel.
+template <bool FIRST>
+__host__ __device__ constexpr int accum_threads_per_vector() {
+    return (FIRST && CC_DP_ACCUM_FIRST_HALF) ? 2 : 1;
 }
 
 template <int R>
@@ -300,11 +354,15 @@ __global__ void __launch_bounds__(kThreads)
 accumulate_kernel(const __grid_constant__ AccumParams p) {
     const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
     const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
-    for (size_t i = first; i < p.num_vec; i += stride) {
-        if constexpr (FIRST)
-            accumulate_first<R>(p, i);
-        else
-            accumulate_later<R>(p, i);
+    if constexpr (accum_threads_per_vector<FIRST>() == 2) {
+        for (size_t i = first; i < 2 * p.num_vec; i += stride) accumulate_first_half<R>(p, i);
+    } else {
+        for (size_t i = first; i < p.num_vec; i += stride) {
+            if constexpr (FIRST)
+                accumulate_first<R>(p, i);
+            else
+                accumulate_later<R>(p, i);
+        }
     }
     if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len) {
         const size_t e = p.tail_begin + threadIdx.x;
@@ -497,7 +555,9 @@ cudaError_t launch_accumulate(const void *const *grads, float *const *acc,
     p.num_vec = n / CC_PAD_ELEMS;
     p.tail_begin = p.num_vec * CC_PAD_ELEMS;
     p.tail_len = static_cast<int>(n - p.tail_begin);
-    size_t blocks = div_up(p.num_vec, kThreads);
+    const size_t units = p.num_vec * (first ? accum_threads_per_vector<true>()
+                                            : accum_threads_per_vector<false>());
+    size_t blocks = div_up(units, kThreads);
     if (blocks > 0x7FFFFFFFu) blocks = 0x7FFFFFFFu;   // grid-stride covers the rest
     if (blocks == 0) blocks = 1;
     accum_kernel_for(R, first)<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
