@@ -90,6 +90,8 @@ _SIGNATURES = {
                                 _f, _f, _f, _f, _f, _i, _f, _i, _vp], _i),
     "cc_fused_dp_bucket": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _sz,
                             _f, _f, _f, _f, _f, _i, _f, _i, _vp], _i),
+    "cc_fused_dp_shard": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _sz, _sz,
+                           _f, _f, _f, _f, _f, _i, _f, _vp], _i),
     "cc_plan_buckets": ([_vp, _i, _sz, _vp, _vp, _vp, _i, _vp, _vp], _i),
     "cc_bucket_ready_layers": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _vp], _i),
     "cc_overlap_bench": ([ctypes.POINTER(cc_overlap_cfg),
@@ -199,6 +201,18 @@ def cc_fused_dp_bucket(grads, acc, master, m, v, params_out, n: int, R: int,
         _addr(v), _addr_array(params_out), n, R, begin, end, lr, beta1, beta2,
         eps, weight_decay, step, grad_scale, max_ctas, _stream(stream)),
         "cc_fused_dp_bucket")
+
+
+def cc_fused_dp_shard(grads, acc, master, m, v, params_out, n: int, R: int,
+                      shard_begin: int, shard_end: int, bucket_bytes: int,
+                      lr: float, beta1: float, beta2: float, eps: float,
+                      weight_decay: float, step: int, grad_scale: float,
+                      stream=None) -> None:
+    _check(lib().cc_fused_dp_shard(
+        _addr_array(grads), _addr_array(acc), _addr(master), _addr(m),
+        _addr(v), _addr_array(params_out), n, R, shard_begin, shard_end,
+        bucket_bytes, lr, beta1, beta2, eps, weight_decay, step, grad_scale,
+        _stream(stream)), "cc_fused_dp_shard")
 
 
 def cc_unfused_dp_step(grads, master, m, v, params_out, workspace,

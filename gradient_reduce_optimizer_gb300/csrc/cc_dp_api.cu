@@ -359,6 +359,44 @@ int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused bucket launch");
 }
 
+int cc_fused_dp_shard(const void *const *grads, const float *const *acc,
+                      float *master, float *m, float *v,
+                      void *const *params_out, size_t n, int R,
+                      size_t shard_begin, size_t shard_end, size_t bucket_bytes,
+                      float lr, float beta1, float beta2, float eps,
+                      float weight_decay, int step, float grad_scale,
+                      void *stream) {
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    if (shard_begin > shard_end || shard_end > n)
+        return fail(CC_ERR_INVALID, "shard [%zu, %zu) not inside [0, %zu)", shard_begin,
+                    shard_end, n);
+    if (shard_begin % CC_PAD_ELEMS != 0)
+        return fail(CC_ERR_MISALIGNED, "shard_begin=%zu is not a multiple of %d", shard_begin,
+                    CC_PAD_ELEMS);
+    if (shard_begin == shard_end) {
+        AdamScalars c;
+        return make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
+    }
+    if (!grads || !params_out) return fail(CC_ERR_INVALID, "grads/params_out arrays are NULL");
+    // The shard's view of the replica slabs: the same step over
+    // len = shard_end - shard_begin elements, with the state arrays as they
+    // are.  shard_begin is a multiple of 8, so the views keep the 16-byte
+    // alignment of the slabs.
+    const void *g[CC_MAX_R];
+    void *o[CC_MAX_R];
+    const float *a[CC_MAX_R];
+    for (int r = 0; r < R; ++r) {
+        if (!grads[r] || !params_out[r] || (acc && !acc[r]))
+            return fail(CC_ERR_INVALID, "replica %d slab is NULL", r);
+        g[r] = static_cast<const char *>(grads[r]) + 2 * shard_begin;
+        o[r] = static_cast<char *>(params_out[r]) + 2 * shard_begin;
+        a[r] = acc ? acc[r] + shard_begin : nullptr;
+    }
+    return cc_fused_dp_step_accum(g, acc ? a : nullptr, master, m, v, o,
+                                  shard_end - shard_begin, R, bucket_bytes, lr, beta1,
+                                  beta2, eps, weight_decay, step, grad_scale, 1, stream);
+}
+
 int cc_accumulate_local(const void *const *grads, float *const *acc, size_t n,
                         int R, int first, void *stream) {
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);

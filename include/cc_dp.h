@@ -185,6 +185,38 @@ CC_API int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
                        float grad_scale, int max_ctas, void *stream);
 
 /*
+ * cc_fused_dp_shard -- one rank's share of the sharded step, with the
+ * optimizer state sharded ("LIT-735 (CoCoNet)", Key takeaways: the fused
+ * ReduceScatter-optimizer-AllGather fits larger micro-batches by sharding
+ * optimizer state).  The rank owns the master weights and Adam moments of
+ * the slab elements [shard_begin, shard_end) only: it reduces the R
+ * replicas' gradients of that range (its ReduceScatter share), updates its
+ * state shard, and writes the range's bf16 parameters to all R replica
+ * slabs (its AllGather share).  The R ranks' calls over a partition of
+ * [0, n) give exactly the values of one cc_fused_dp_step_accum over [0, n).
+ *
+ *   grads[R], params_out[R]   whole replica slabs of n bf16 elements; only
+ *                  [shard_begin, shard_end) is read / written.
+ *   acc[R]         NULL, or whole fp32[n] accumulator slabs (read in the
+ *                  range): the reducing step of gradient accumulation.
+ *   master, m, v   fp32[shard_end - shard_begin]: element i is slab element
+ *                  shard_begin + i.  Read and written in place.
+ *   shard_begin    a multiple of CC_PAD_ELEMS (else CC_ERR_MISALIGNED);
+ *                  shard_begin <= shard_end <= n (else CC_ERR_INVALID).  An
+ *                  empty shard is a no-op returning CC_OK.
+ *   bucket_bytes   the shard is cut into buckets as cc_fused_dp_step cuts
+ *                  [0, n), counted from shard_begin.
+ *   the rest       as cc_fused_dp_step.  Allocates nothing.
+ */
+CC_API int cc_fused_dp_shard(const void *const *grads, const float *const *acc,
+                      float *master, float *m, float *v,
+                      void *const *params_out, size_t n, int R,
+                      size_t shard_begin, size_t shard_end, size_t bucket_bytes,
+                      float lr, float beta1, float beta2, float eps,
+                      float weight_decay, int step, float grad_scale,
+                      void *stream);
+
+/*
  * cc_unfused_dp_step -- the same step as cc_fused_dp_step (bit-identical
  * results) in the unfused schedule a framework runs when the collective and
  * the optimizer are separate library calls, kept for comparison ("LIT-735

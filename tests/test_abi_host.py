@@ -212,6 +212,37 @@ def test_bucket_and_accumulate_validation():
     assert ei.value.status == capi.CC_ERR_MISALIGNED
 
 
+def test_shard_validation():
+    g, acc, p, m, v, o = fake_slabs(2, 1000)
+
+    def status(begin, end, grads=g, outs=o, state=(p, m, v), accs=None, **kw):
+        hp = dict(ADAM)
+        hp.update(kw)
+        try:
+            capi.cc_fused_dp_shard(grads, accs, *state, outs, 1000, 2, begin, end, 0,
+                                   stream=0, **hp)
+            return capi.CC_OK
+        except capi.CCError as err:
+            return err.status
+
+    assert status(4, 100) == capi.CC_ERR_MISALIGNED
+    assert status(8, 1001) == capi.CC_ERR_INVALID
+    assert status(16, 8) == capi.CC_ERR_INVALID
+    # an empty shard checks the hyper-parameters and touches no pointer
+    assert status(64, 64, grads=None, outs=None, state=(0, 0, 0)) == capi.CC_OK
+    assert status(64, 64, grads=None, outs=None, state=(0, 0, 0), lr=-1.0) == \
+        capi.CC_ERR_INVALID
+    assert status(8, 100, grads=[g[0], 0]) == capi.CC_ERR_INVALID
+    assert status(8, 100, accs=[acc[0], None]) == capi.CC_ERR_INVALID
+    # the shard's state written over a gradient slab's shard range
+    assert status(8, 100, state=(g[1] + 16, m, v)) == capi.CC_ERR_ALIAS
+    # master is shard-sized: m may start right after a 92-element master
+    assert status(8, 100, state=(p, p + 4 * 92, v)) in (capi.CC_ERR_UNSUPPORTED,
+                                                        capi.CC_ERR_INVALID)
+    assert status(8, 100, state=(p, p + 4 * 88, v)) == capi.CC_ERR_ALIAS
+    assert status(8, 100, state=(p + 4, m, v)) == capi.CC_ERR_MISALIGNED
+
+
 def test_unfused_workspace_validation():
     g, acc, p, m, v, o = fake_slabs(2, 1000)
     ws = acc[0]                         # an unused, aligned fake range

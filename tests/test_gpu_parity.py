@@ -116,6 +116,38 @@ def test_bucket_entry_point_over_planned_buckets(max_ctas):
     compare_all(s, state, oracle_step(grads, state, hp))
 
 
+@pytest.mark.parametrize("R,n,use_acc", [(4, 100_003, False), (8, 1 << 20, True),
+                                         (3, 8 * 1000 + 5, False), (16, 4099, True),
+                                         (2, 7, False)])
+def test_sharded_state_ranks_partition_the_step(R, n, use_acc):
+    """Each of R ranks owns only its shard of master/m/v (arrays of the
+    shard's length) and calls cc_fused_dp_shard on its range of the replica
+    slabs.  Together they give the single fused step bit for bit: every
+    replica's parameters, and each rank's state shard."""
+    s = new_slabs(*random_inputs(R, n, seed=40 + R, step=6), with_acc=use_acc)
+    if use_acc:
+        g = torch.Generator(device=DEV).manual_seed(41)
+        for a in s.acc:
+            a.copy_(torch.randn(n, generator=g, device=DEV) * 3e-3)
+    grads, state, acc = host_copy(s)
+    hp = dict(HP10, step=6)
+    units = n // 8
+    cuts = [8 * (units * k // R) for k in range(R)] + [n]
+    owned = []
+    for k in range(R):
+        b, e = cuts[k], cuts[k + 1]
+        shard = [t[b:e].clone() for t in (s.master, s.m, s.v)]
+        capi.cc_fused_dp_shard(s.grads, s.acc, *shard, s.outs, n, R, b, e, 64 << 10, **hp)
+        owned.append((b, e, shard))
+    torch.cuda.synchronize()
+    outs = oracle_step(grads, state, hp, acc=acc)
+    for r, (t, ref) in enumerate(zip(s.outs, outs)):
+        assert_bits(f"params_out[{r}]", u16(t), ref, "bf16")
+    for k, (b, e, shard) in enumerate(owned):
+        for name, t, ref in zip(("master", "m", "v"), shard, state):
+            assert_bits(f"rank {k} {name}", f32(t), ref[b:e], "f32")
+
+
 def test_consecutive_steps_captured_in_a_cuda_graph():
     """Two consecutive multi-bucket steps captured in one CUDA graph and
     replayed twice: inside a step the buckets chain by programmatic launch,
