@@ -148,6 +148,26 @@ def test_sharded_state_ranks_partition_the_step(R, n, use_acc):
             assert_bits(f"rank {k} {name}", f32(t), ref[b:e], "f32")
 
 
+def test_fifty_consecutive_steps_do_not_drift():
+    """Steps t = 1..50 from m = v = 0, fresh gradients every step, the GPU
+    state and the oracle state each fed back into itself: still the same
+    bits after 50 steps (a single differently rounded operation anywhere
+    would compound)."""
+    R, n = 4, 262_147
+    s = new_slabs(*random_inputs(R, n, seed=77, step=1))
+    _, state, _ = host_copy(s)
+    gen = torch.Generator(device=DEV).manual_seed(78)
+    for t in range(1, 51):
+        for gr in s.grads:
+            gr.copy_((torch.randn(n, generator=gen, device=DEV) * 1e-3).to(torch.bfloat16))
+        host_grads = [u16(gr) for gr in s.grads]
+        hp = dict(HP10, step=t)
+        gpu_step(s, hp, bucket_bytes=96 << 10)
+        outs = oracle_step(host_grads, state, hp)
+    torch.cuda.synchronize()
+    compare_all(s, state, outs, label="step 50 ")
+
+
 def test_consecutive_steps_captured_in_a_cuda_graph():
     """Two consecutive multi-bucket steps captured in one CUDA graph and
     replayed twice: inside a step the buckets chain by programmatic launch,
