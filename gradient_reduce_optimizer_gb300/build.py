@@ -25,7 +25,7 @@ LIBRARY = os.path.join(PKG, "libcc_dp.so")
 SOURCES = ["cc_dp_kernels.cu", "cc_dp_bulk.cu", "cc_dp_unfused.cu", "cc_dp_api.cu",
            "cc_overlap.cu", "cc_tp.cu"]
 HEADERS = [os.path.join(CSRC, "cc_dp_internal.h"), os.path.join(CSRC, "cc_dp_device.cuh"),
-           os.path.join(INCLUDE, "cc_dp.h")]
+           os.path.join(CSRC, "cc_trace.h"), os.path.join(INCLUDE, "cc_dp.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [

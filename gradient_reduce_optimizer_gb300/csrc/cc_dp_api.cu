@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "cc_dp_internal.h"
+#include "cc_trace.h"
 
 namespace ccdp {
 
@@ -274,6 +275,7 @@ int run_step(const Slabs &s, const AdamScalars &c, size_t n, size_t bucket_bytes
         const size_t e = std::min(n, b + per);
         if (injected_failure())
             return fail(CC_ERR_CUDA, "injected launch failure before the bucket at element %zu", b);
+        TraceRange bucket("bucket", b);
         const cudaError_t err = launch_fused(s, c, b, e, 0, /*chain=*/b > 0, stream);
         if (err != cudaSuccess) return fail_cuda(err, "fused step launch");
     }
@@ -308,6 +310,7 @@ int cc_fused_dp_step_accum(const void *const *grads, const float *const *acc,
                            float beta2, float eps, float weight_decay,
                            int step, float grad_scale, int accum_k,
                            void *stream) {
+    TraceRange call(acc ? "cc_fused_dp_step_accum" : "cc_fused_dp_step", n);
     if (accum_k < 1) return fail(CC_ERR_INVALID, "accum_k=%d must be >= 1", accum_k);
     if (accum_k > 1 && !acc)
         return fail(CC_ERR_INVALID, "accum_k=%d needs the accumulators (acc is NULL)", accum_k);
@@ -341,6 +344,7 @@ int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
                        size_t end, float lr, float beta1, float beta2,
                        float eps, float weight_decay, int step,
                        float grad_scale, int max_ctas, void *stream) {
+    TraceRange call("cc_fused_dp_bucket", begin);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     if (begin > end || end > n)
         return fail(CC_ERR_INVALID, "range [%zu, %zu) not inside [0, %zu)", begin, end, n);
@@ -366,6 +370,7 @@ int cc_fused_dp_shard(const void *const *grads, const float *const *acc,
                       float lr, float beta1, float beta2, float eps,
                       float weight_decay, int step, float grad_scale,
                       void *stream) {
+    TraceRange call("cc_fused_dp_shard", shard_begin);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     if (shard_begin > shard_end || shard_end > n)
         return fail(CC_ERR_INVALID, "shard [%zu, %zu) not inside [0, %zu)", shard_begin,
@@ -399,6 +404,7 @@ int cc_fused_dp_shard(const void *const *grads, const float *const *acc,
 
 int cc_accumulate_local(const void *const *grads, float *const *acc, size_t n,
                         int R, int first, void *stream) {
+    TraceRange call(first ? "cc_accumulate_local(first)" : "cc_accumulate_local", n);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     if (n == 0) return CC_OK;
     if (!grads || !acc) return fail(CC_ERR_INVALID, "grads/acc arrays are NULL");
@@ -508,6 +514,7 @@ int cc_unfused_dp_step(const void *const *grads, float *master, float *m, float 
                        size_t n, int R, size_t bucket_bytes, float lr, float beta1,
                        float beta2, float eps, float weight_decay, int step,
                        float grad_scale, void *stream) {
+    TraceRange call("cc_unfused_dp_step", n);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     AdamScalars c;
     int st = make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
@@ -541,6 +548,7 @@ int cc_unfused_dp_step(const void *const *grads, float *master, float *m, float 
         const size_t e = std::min(n, b + per);
         if (injected_failure())
             return fail(CC_ERR_CUDA, "injected launch failure before the bucket at element %zu", b);
+        TraceRange bucket("bucket", b);
         const cudaError_t err = launch_unfused_bucket(s, c, workspace, b, e,
                                                       static_cast<cudaStream_t>(stream));
         if (err != cudaSuccess) return fail_cuda(err, "unfused step launch");

@@ -28,6 +28,7 @@
 #include <vector>
 
 #include "cc_dp_internal.h"
+#include "cc_trace.h"
 
 namespace ccdp {
 namespace {
@@ -167,6 +168,7 @@ struct Bench {
 
     int backward(bool record_layers) {
         for (int l = cfg.num_layers - 1; l >= 0; --l) {
+            TraceRange layer("proxy backward layer", static_cast<uint64_t>(l));
             const cublasStatus_t st = gemms();
             if (st != CUBLAS_STATUS_SUCCESS)
                 return fail(CC_ERR_CUDA, "cublasGemmEx failed (status %d)", static_cast<int>(st));
@@ -180,6 +182,7 @@ struct Bench {
 
     int buckets(cudaStream_t s, bool wait_ready, int max_ctas) {
         for (int b = 0; b < cfg.num_buckets; ++b) {
+            TraceRange bucket("bucket", cfg.bucket_begin[b]);
             cudaError_t e = cudaSuccess;
             if (wait_ready) e = cudaStreamWaitEvent(s, res.layer[cfg.bucket_ready_layer[b]], 0);
             if (e == cudaSuccess)
@@ -192,6 +195,9 @@ struct Bench {
 
     // Runs one arm once and returns its elapsed milliseconds in *ms.
     int arm(int which, float *ms) {
+        static const char *const kArmNames[4] = {"arm: backward alone", "arm: buckets alone",
+                                                 "arm: overlapped", "arm: sequential"};
+        TraceRange range(kArmNames[which], static_cast<uint64_t>(which));
         const bool part = which == 2 && res.gcomp;
         comp = part ? reinterpret_cast<cudaStream_t>(res.gcomp) : res.comp;
         side = part ? reinterpret_cast<cudaStream_t>(res.gside) : res.side;

@@ -23,6 +23,7 @@
 
 #include "cc_dp_device.cuh"
 #include "cc_dp_internal.h"
+#include "cc_trace.h"
 
 namespace ccdp {
 namespace {
@@ -293,6 +294,7 @@ using namespace ccdp;
 
 extern "C" int cc_tp_allreduce(const float *const *partials, void *const *out, size_t n,
                                int R, void *stream) {
+    TraceRange call("cc_tp_allreduce", n);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     if (n == 0) return CC_OK;
     if (n > SIZE_MAX / 8) return fail(CC_ERR_INVALID, "n=%zu too large", n);
