@@ -183,11 +183,15 @@ struct Bench {
     int buckets(cudaStream_t s, bool wait_ready, int max_ctas) {
         for (int b = 0; b < cfg.num_buckets; ++b) {
             TraceRange bucket("bucket", cfg.bucket_begin[b]);
+            // Past the budgeted buckets, a bucket waits for the end of the
+            // backward (layer 0's event) and takes the whole GPU.
+            const bool wide = wait_ready && cfg.budget_buckets > 0 && b >= cfg.budget_buckets;
+            const int ready = wide ? 0 : cfg.bucket_ready_layer[b];
             cudaError_t e = cudaSuccess;
-            if (wait_ready) e = cudaStreamWaitEvent(s, res.layer[cfg.bucket_ready_layer[b]], 0);
+            if (wait_ready) e = cudaStreamWaitEvent(s, res.layer[ready], 0);
             if (e == cudaSuccess)
                 e = launch_step_range(slabs, scalars, cfg.bucket_begin[b], cfg.bucket_end[b],
-                                      max_ctas, /*chain=*/!wait_ready && b > 0, s);
+                                      wide ? 0 : max_ctas, /*chain=*/!wait_ready && b > 0, s);
             if (e != cudaSuccess) return fail_cuda(e, "bucket launch");
         }
         return CC_OK;
@@ -272,6 +276,8 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     if (c.stream_priority < 0 || c.stream_priority > 2)
         return fail(CC_ERR_INVALID, "stream_priority=%d must be 0, 1 or 2", c.stream_priority);
     if (c.comm_sms < 0) return fail(CC_ERR_INVALID, "comm_sms=%d must be >= 0", c.comm_sms);
+    if (c.budget_buckets < 0)
+        return fail(CC_ERR_INVALID, "budget_buckets=%d must be >= 0", c.budget_buckets);
     if (c.num_buckets < 1 || !c.bucket_begin || !c.bucket_end || !c.bucket_ready_layer)
         return fail(CC_ERR_INVALID, "need at least one bucket");
     for (int b = 0; b < c.num_buckets; ++b) {

@@ -364,6 +364,11 @@ typedef struct cc_overlap_cfg {
     int comm_sms;                  /* > 0: overlapped arm on a spatial partition (green
                                       contexts): buckets on comm_sms SMs (rounded up to the
                                       driver's granularity), GEMMs on the rest; 0: none */
+    int budget_buckets;            /* > 0: in the overlapped arm only the first
+                                      budget_buckets buckets take the max_ctas budget (the
+                                      SMs the GEMMs leave free); the later ones wait for
+                                      the whole backward and run on the whole GPU.
+                                      0: every bucket takes max_ctas */
 } cc_overlap_cfg;
 
 typedef struct cc_overlap_result {

@@ -575,9 +575,10 @@ def test_fp32_slabs_aligned_to_16_but_not_32_bytes(use_acc):
 # per arm
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("max_ctas,prio,comm_sms", [(0, 0, 0), (0, 2, 0), (24, 1, 0),
-                                                   (0, 2, 48)])
-def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sms):
+@pytest.mark.parametrize("max_ctas,prio,comm_sms,budget", [(0, 0, 0, 0), (0, 2, 0, 0),
+                                                          (24, 1, 0, 0), (0, 2, 48, 0),
+                                                          (8, 2, 0, 3)])
+def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sms, budget):
     """With warmup 0 and one iteration the four arms step the slabs three
     times (buckets alone, overlapped, sequential; the backward-only arm does
     not step): the result must be three oracle steps, bit for bit."""
@@ -600,7 +601,8 @@ def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sm
                               ready_layers=ready, num_layers=4, gemms_per_layer=2,
                               gemm_m=M, gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B,
                               gemm_c=C, warmup=0, iters=1, max_ctas=max_ctas,
-                              stream_priority=prio, comm_sms=comm_sms, **hp)
+                              stream_priority=prio, comm_sms=comm_sms,
+                              budget_buckets=budget, **hp)
     assert r["num_buckets"] == len(buckets) and r["t_bwd_ms"] > 0
     if comm_sms:   # a spatial partition: green contexts on disjoint SM sets
         assert r["comm_sms"] >= comm_sms and r["compute_sms"] > 0
