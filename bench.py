@@ -109,6 +109,16 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_peak():
+    """Dense bf16 TFLOP/s of a cuBLAS GEMM timed alone (burst), if measured."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for path in KERNEL_SOURCES:
@@ -672,8 +682,11 @@ def run_tp(args, dev, R=8, m=8192, n=3072, k=12288, chunk_list=(1, 2, 4, 8, 16))
                      "allreduce_hidden_pct": round(100 * hidden, 1),
                      "speedup_vs_sequential": round(t["t_sequential_ms"] / t["t_overlap_ms"], 3)})
     ar = rows[0]["t_allreduce_ms"]
+    tflops = 2 * m * n * k / (rows[0]["t_gemm_ms"] * 1e-3) / 1e12
+    bf16_peak = measured_bf16_peak()
     return {"shape": {"R": R, "m": m, "n": n, "k": k},
-            "gemm_tflops": round(2 * m * n * k / (rows[0]["t_gemm_ms"] * 1e-3) / 1e12, 1),
+            "gemm_tflops": round(tflops, 1),
+            "gemm_frac_of_measured_bf16": round(tflops / bf16_peak, 3) if bf16_peak else None,
             "allreduce_bytes": 6 * R * m * n,
             "allreduce_hbm_gbs": round(6 * R * m * n / (ar * 1e-3) / 1e9, 1),
             "chunks": rows}
@@ -909,6 +922,9 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0):
         r["mode"] = "rank share (1/R of each bucket)" if rank_share else "all R replicas"
         r["exposed_pct_of_bwd"] = round(100 * r["exposed_ms"] / r["t_bwd_ms"], 1)
         r["bwd_tflops"] = round(24 * 3 * 2 * M * N * K / (r["t_bwd_ms"] * 1e-3) / 1e12, 1)
+        bf16_peak = measured_bf16_peak()
+        r["bwd_frac_of_measured_bf16"] = (round(r["bwd_tflops"] / bf16_peak, 3)
+                                          if bf16_peak else None)
         out.append(r)
     return out[0] if len(out) == 1 else out
 
