@@ -365,7 +365,11 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
-    gbuild.build()
+    # one process per node compiles (if the library is stale); the others
+    # wait, so that no two ranks write the same objects
+    if local == 0:
+        gbuild.build()
+    barrier(world)
     capi.lib()
 
     if args.small:
