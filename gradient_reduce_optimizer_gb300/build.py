@@ -94,7 +94,7 @@ def build(force: bool = False, verbose: bool = False,
         rpath = ":".join(cuda_lib_dirs())
         tmp = library + ".tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
-               "-lcublas", f"-Xlinker=-rpath={rpath}"]
+               "-lcublas", "-lcublasLt", f"-Xlinker=-rpath={rpath}"]
         cmd += [f"-L{d}" for d in cuda_lib_dirs()]
         subprocess.run(cmd, check=True)
         os.replace(tmp, library)

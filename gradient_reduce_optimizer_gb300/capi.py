@@ -56,6 +56,7 @@ class cc_overlap_cfg(ctypes.Structure):
         ("gemm_a", _vp), ("gemm_b", _vp), ("gemm_c", _vp),
         ("warmup", _i), ("iters", _i), ("max_ctas", _i),
         ("stream_priority", _i), ("comm_sms", _i), ("budget_buckets", _i),
+        ("gemm_algo", _i),
     ]
 
 
@@ -64,6 +65,7 @@ class cc_overlap_result(ctypes.Structure):
         ("t_bwd_ms", _f), ("t_comm_ms", _f), ("t_step_overlap_ms", _f),
         ("t_step_seq_ms", _f), ("exposed_ms", _f), ("exposed_bound_ms", _f),
         ("num_buckets", _i), ("comm_sms", _i), ("compute_sms", _i),
+        ("gemm_algos", _i),
     ]
 
 
@@ -291,7 +293,8 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
                      gemm_m: int, gemm_n: int, gemm_k: int, gemm_a, gemm_b,
                      gemm_c, warmup: int = 3, iters: int = 20,
                      max_ctas: int = 0, stream_priority: int = 0, comm_sms: int = 0,
-                     budget_buckets: int = 0, acc=None) -> Dict[str, float]:
+                     budget_buckets: int = 0, gemm_algo: int = 0,
+                     acc=None) -> Dict[str, float]:
     B = len(buckets)
     keep = dict(
         g=_addr_array(grads), o=_addr_array(params_out),
@@ -313,7 +316,7 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
         gemm_k=gemm_k, gemm_a=_addr(gemm_a), gemm_b=_addr(gemm_b),
         gemm_c=_addr(gemm_c), warmup=warmup, iters=iters, max_ctas=max_ctas,
         stream_priority=stream_priority, comm_sms=comm_sms,
-        budget_buckets=budget_buckets)
+        budget_buckets=budget_buckets, gemm_algo=gemm_algo)
     res = cc_overlap_result()
     _check(lib().cc_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
            "cc_overlap_bench")

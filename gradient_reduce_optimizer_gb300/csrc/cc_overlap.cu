@@ -20,6 +20,7 @@
 // keep the whole GPU, so exposed time is still measured against the
 // unpartitioned backward.
 
+#include <cublasLt.h>
 #include <cublas_v2.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -77,6 +78,12 @@ struct Resources {
     cudaEvent_t start = nullptr, stop = nullptr, side_done = nullptr;
     std::vector<cudaEvent_t> layer;
     cublasHandle_t blas = nullptr;
+    // gemm_algo > 0: the GEMMs through cuBLASLt with that heuristic candidate
+    cublasLtHandle_t lt = nullptr;
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t lay_b = nullptr, lay_a = nullptr, lay_c = nullptr;
+    cublasLtMatmulAlgo_t algo{};
+    int algos = 0;
     // the spatial partition of the overlapped arm (comm_sms > 0)
     CUgreenCtx green_comp = nullptr, green_side = nullptr;
     CUstream gcomp = nullptr, gside = nullptr;
@@ -89,6 +96,11 @@ struct Resources {
         if (gcomp) cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(gcomp));
         if (gside) cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(gside));
         if (blas) cublasDestroy(blas);
+        if (lay_a) cublasLtMatrixLayoutDestroy(lay_a);
+        if (lay_b) cublasLtMatrixLayoutDestroy(lay_b);
+        if (lay_c) cublasLtMatrixLayoutDestroy(lay_c);
+        if (op) cublasLtMatmulDescDestroy(op);
+        if (lt) cublasLtDestroy(lt);
         if (gcomp) g.stream_destroy(gcomp);
         if (gside) g.stream_destroy(gside);
         if (green_comp) g.destroy(green_comp);
@@ -141,6 +153,44 @@ int make_partition(int want, int prio_comp, int prio_side, Resources &res) {
     return CC_OK;
 }
 
+// The proxy GEMM through cuBLASLt, column-major C^T[N,M] = B^T[N,K] A^T[K,M]
+// (the same product as the cublasGemmEx call), with heuristic candidate
+// gemm_algo (1-based) among those that need no workspace.  Candidates differ
+// in tile shape and pipeline depth, and so in the registers and shared
+// memory their CTAs hold -- what decides whether a reduction block can run
+// on the same SM.
+int pick_lt_algo(const cc_overlap_cfg &c, Resources &res) {
+    const uint64_t M = c.gemm_m, N = c.gemm_n, K = c.gemm_k;
+    if (cublasLtCreate(&res.lt) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulDescCreate(&res.op, CUBLAS_COMPUTE_32F, CUDA_R_32F) !=
+            CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&res.lay_b, CUDA_R_16BF, N, K, N) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&res.lay_a, CUDA_R_16BF, K, M, K) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&res.lay_c, CUDA_R_16BF, N, M, N) != CUBLAS_STATUS_SUCCESS)
+        return fail(CC_ERR_CUDA, "cuBLASLt descriptor setup failed");
+    cublasLtMatmulPreference_t pref = nullptr;
+    if (cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS)
+        return fail(CC_ERR_CUDA, "cuBLASLt preference create failed");
+    const size_t no_workspace = 0;
+    cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES,
+                                         &no_workspace, sizeof no_workspace);
+    constexpr int kMaxAlgos = 32;
+    cublasLtMatmulHeuristicResult_t cand[kMaxAlgos];
+    int found = 0;
+    const cublasStatus_t hs = cublasLtMatmulAlgoGetHeuristic(
+        res.lt, res.op, res.lay_b, res.lay_a, res.lay_c, res.lay_c, pref, kMaxAlgos, cand,
+        &found);
+    cublasLtMatmulPreferenceDestroy(pref);
+    if (hs != CUBLAS_STATUS_SUCCESS)
+        return fail(CC_ERR_CUDA, "cuBLASLt heuristic failed (status %d)", static_cast<int>(hs));
+    res.algos = found;
+    if (c.gemm_algo > found)
+        return fail(CC_ERR_INVALID, "gemm_algo=%d but cuBLASLt offers %d candidates",
+                    c.gemm_algo, found);
+    res.algo = cand[c.gemm_algo - 1].algo;
+    return CC_OK;
+}
+
 struct Bench {
     const cc_overlap_cfg &cfg;
     const Slabs &slabs;
@@ -151,6 +201,16 @@ struct Bench {
     // C^T = B^T A^T for column-major cuBLAS.
     cublasStatus_t gemms() {
         const float alpha = 1.0f, beta = 0.0f;
+        if (cfg.gemm_algo > 0) {
+            for (int g = 0; g < cfg.gemms_per_layer; ++g) {
+                const cublasStatus_t st = cublasLtMatmul(
+                    res.lt, res.op, &alpha, cfg.gemm_b, res.lay_b, cfg.gemm_a, res.lay_a,
+                    &beta, cfg.gemm_c, res.lay_c, cfg.gemm_c, res.lay_c, &res.algo, nullptr,
+                    0, comp);
+                if (st != CUBLAS_STATUS_SUCCESS) return st;
+            }
+            return CUBLAS_STATUS_SUCCESS;
+        }
         for (int g = 0; g < cfg.gemms_per_layer; ++g) {
             const cublasStatus_t st = cublasGemmEx(
                 res.blas, CUBLAS_OP_N, CUBLAS_OP_N, cfg.gemm_n, cfg.gemm_m, cfg.gemm_k,
@@ -276,6 +336,7 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     if (c.stream_priority < 0 || c.stream_priority > 2)
         return fail(CC_ERR_INVALID, "stream_priority=%d must be 0, 1 or 2", c.stream_priority);
     if (c.comm_sms < 0) return fail(CC_ERR_INVALID, "comm_sms=%d must be >= 0", c.comm_sms);
+    if (c.gemm_algo < 0) return fail(CC_ERR_INVALID, "gemm_algo=%d must be >= 0", c.gemm_algo);
     if (c.budget_buckets < 0)
         return fail(CC_ERR_INVALID, "budget_buckets=%d must be >= 0", c.budget_buckets);
     if (c.num_buckets < 1 || !c.bucket_begin || !c.bucket_end || !c.bucket_ready_layer)
@@ -330,6 +391,7 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
             return fail_cuda(e, "layer event create");
     if (cublasCreate(&res.blas) != CUBLAS_STATUS_SUCCESS)
         return fail(CC_ERR_CUDA, "cublasCreate failed");
+    if (c.gemm_algo > 0 && (st = pick_lt_algo(c, res)) != CC_OK) return st;
     if (c.comm_sms > 0 &&
         (st = make_partition(c.comm_sms, c.stream_priority == 2 ? hi : lo,
                              c.stream_priority == 1 ? hi : lo, res)) != CC_OK)
@@ -341,6 +403,7 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     if ((st = bench.median(1, &r.t_comm_ms)) != CC_OK) return st;
     if ((st = bench.median(2, &r.t_step_overlap_ms)) != CC_OK) return st;
     if ((st = bench.median(3, &r.t_step_seq_ms)) != CC_OK) return st;
+    r.gemm_algos = res.algos;
     r.exposed_ms = r.t_step_overlap_ms - r.t_bwd_ms;
     r.exposed_bound_ms = std::max(0.0f, r.t_comm_ms - r.t_bwd_ms);
     r.num_buckets = c.num_buckets;

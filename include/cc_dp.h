@@ -369,6 +369,9 @@ typedef struct cc_overlap_cfg {
                                       SMs the GEMMs leave free); the later ones wait for
                                       the whole backward and run on the whole GPU.
                                       0: every bucket takes max_ctas */
+    int gemm_algo;                 /* 0: the proxy GEMMs through cublasGemmEx (cuBLAS's
+                                      choice); k > 0: through cuBLASLt with the k-th
+                                      candidate of its heuristic (no workspace) */
 } cc_overlap_cfg;
 
 typedef struct cc_overlap_result {
@@ -376,6 +379,7 @@ typedef struct cc_overlap_result {
     float exposed_ms, exposed_bound_ms;
     int num_buckets;
     int comm_sms, compute_sms;     /* the partition's SM counts (0 without one) */
+    int gemm_algos;                /* cuBLASLt candidates offered (0 with gemm_algo 0) */
 } cc_overlap_result;
 
 CC_API int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out);
