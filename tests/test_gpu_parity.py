@@ -575,10 +575,14 @@ def test_fp32_slabs_aligned_to_16_but_not_32_bytes(use_acc):
 # per arm
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("max_ctas,prio,comm_sms,budget", [(0, 0, 0, 0), (0, 2, 0, 0),
-                                                          (24, 1, 0, 0), (0, 2, 48, 0),
-                                                          (8, 2, 0, 3)])
-def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sms, budget):
+@pytest.mark.parametrize("max_ctas,prio,comm_sms,budget,algo", [(0, 0, 0, 0, 0),
+                                                               (0, 2, 0, 0, 0),
+                                                               (24, 1, 0, 0, 0),
+                                                               (0, 2, 48, 0, 0),
+                                                               (8, 2, 0, 3, 0),
+                                                               (0, 2, 0, 0, 1)])
+def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sms, budget,
+                                                         algo):
     """With warmup 0 and one iteration the four arms step the slabs three
     times (buckets alone, overlapped, sequential; the backward-only arm does
     not step): the result must be three oracle steps, bit for bit."""
@@ -602,8 +606,9 @@ def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sm
                               gemm_m=M, gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B,
                               gemm_c=C, warmup=0, iters=1, max_ctas=max_ctas,
                               stream_priority=prio, comm_sms=comm_sms,
-                              budget_buckets=budget, **hp)
+                              budget_buckets=budget, gemm_algo=algo, **hp)
     assert r["num_buckets"] == len(buckets) and r["t_bwd_ms"] > 0
+    assert (r["gemm_algos"] >= 1) == (algo > 0)
     if comm_sms:   # a spatial partition: green contexts on disjoint SM sets
         assert r["comm_sms"] >= comm_sms and r["compute_sms"] > 0
     torch.cuda.synchronize()
@@ -625,6 +630,10 @@ def test_overlap_bench_rejects_bad_schedules():
         with pytest.raises(capi.CCError) as ei:
             capi.cc_overlap_bench(buckets=buckets, ready_layers=ready, **base)
         assert ei.value.status == status
+    for kw in (dict(gemm_algo=-1), dict(gemm_algo=10_000), dict(budget_buckets=-1)):
+        with pytest.raises(capi.CCError) as ei:
+            capi.cc_overlap_bench(buckets=[(0, 4096)], ready_layers=[0], **kw, **base)
+        assert ei.value.status == capi.CC_ERR_INVALID
 
 
 # ---------------------------------------------------------------------------
