@@ -368,6 +368,26 @@ def test_full_size_gpt2_slice_r4():
     check_sampled(s, hp_of(w), idx, w.bucket_bytes)
 
 
+def test_max_replicas_past_2_31_elements():
+    """R = 16, the largest replica count, over 2^31 + 29 elements (about 163 GB
+    of slabs): 64-bit element indexing with the most replica pointers, a
+    ragged tail, 100 MiB buckets; sampled elements against the oracle."""
+    R, n = 16, (1 << 31) + 29
+    if torch.cuda.get_device_properties(0).total_memory < 200 * (1 << 30):
+        pytest.skip("needs about 180 GB of device memory")
+    torch.cuda.empty_cache()
+    s = new_slabs(*random_inputs(R, n, seed=91, step=3))
+    bb = 100 << 20
+    cuts = uniform_cuts(n, bb)[::5] + [1 << 31, (1 << 31) + 8, (1 << 31) + 24]
+    idx = sample_indices(n, cuts, 1 << 19, seed=3)
+    past = torch.arange(1 << 31, n, device=DEV)          # every element past 2^31
+    idx = torch.unique(torch.cat([idx, past]))
+    assert int((idx >= (1 << 31)).sum()) == n - (1 << 31)
+    check_sampled(s, dict(HP10, step=3), idx, bb)
+    del s
+    torch.cuda.empty_cache()
+
+
 def test_full_size_bert_large_accumulation_k4():
     """k=4 on the 336M set at R=8: three local micro-steps, then the reducing
     step, sampled against the oracle run through the same micro-steps."""
