@@ -920,7 +920,8 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0):
             gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
             warmup=args.warmup, iters=args.overlap_iters,
             max_ctas=args.overlap_ctas, stream_priority=args.stream_priority,
-            comm_sms=comm_sms, gemm_algo=args.overlap_gemm_algo, **step_args(wk, w.step))
+            comm_sms=comm_sms, gemm_algo=args.overlap_gemm_algo,
+            budget_buckets=args.overlap_budget_buckets, **step_args(wk, w.step))
         r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
         r["bucket_mib"] = mib
         r["mode"] = "rank share (1/R of each bucket)" if rank_share else "all R replicas"
@@ -1016,6 +1017,9 @@ def parse_args(argv=None):
     p.add_argument("--no-overlap", action="store_true")
     p.add_argument("--overlap-iters", type=int, default=20)
     p.add_argument("--overlap-ctas", type=int, default=0)
+    p.add_argument("--overlap-budget-buckets", type=int, default=0,
+                   help="overlap: only the first this-many buckets take --overlap-ctas; "
+                        "the rest wait for the backward and take the whole GPU")
     p.add_argument("--overlap-gemm-algo", type=int, default=0,
                    help="overlap: 0 = the proxy GEMMs through cublasGemmEx; k > 0 = "
                         "through cuBLASLt with its k-th heuristic candidate")
