@@ -389,8 +389,17 @@ def run_ours(args):
         acc = [g.float() * 3.0 for g in wk["grads"]]
         torch.cuda.synchronize()
 
+    ws = None
+    if args.small and args.unfused:
+        ws = torch.empty(n_slab, dtype=torch.float32, device=dev)
+
     def one_step(step):
-        if args.small and args.micro:
+        if ws is not None:
+            # profile case: the unfused schedule (reduce, AdamW, R-1 copies)
+            capi.cc_unfused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"], wk["outs"],
+                                    ws, ws.numel() * 4, n_slab, R, bb, stream=stream,
+                                    **step_args(wk, step))
+        elif args.small and args.micro:
             # profile case: one local micro-step (acc = g, or acc += g)
             capi.cc_accumulate_local(wk["grads"], acc, n_slab, R, args.micro == "first",
                                      stream=stream)
@@ -430,7 +439,8 @@ def run_ours(args):
     ms_local = ev0.elapsed_time(ev1) / args.steps
     ms, value = aggregate(ms_local, float(n_params), world, device=dev)
 
-    bytes_per_param = (4 * R + 24 if acc is None else
+    bytes_per_param = (6 * R + 30 if ws is not None else
+                       4 * R + 24 if acc is None else
                        (6 * R if args.micro == "first" else 10 * R) if args.micro else
                        8 * R + 24)
     launches = launches_per_step(n_slab, bb)
@@ -438,13 +448,15 @@ def run_ours(args):
     launch_ms = ms_local / launches           # launches run back to back
     achieved = bytes_per_param * per_launch_elems / (launch_ms * 1e-3) / 1e9
     peak, peak_src = measured_hbm_peak()
-    tpp = profiled_traffic_per_param(R) if args.engine_ctas == 0 and acc is None else None
+    tpp = (profiled_traffic_per_param(R)
+           if args.engine_ctas == 0 and acc is None and ws is None else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": (round(tpp * per_launch_elems) if tpp else None),
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": round(bytes_per_param * per_launch_elems),
-                "kernel": (f"accumulate_kernel<R={R}, first={args.micro == 'first'}>"
+                "kernel": ("reduce_kernel + adamw_kernel + copies" if ws is not None else
+                           f"accumulate_kernel<R={R}, first={args.micro == 'first'}>"
                            if args.micro else
                            f"fused_step_kernel<R={R}, accumulators>" if acc is not None else
                            f"fused_step_bulk_kernel<R={R}> on {args.engine_ctas} SMs"
@@ -467,14 +479,15 @@ def run_ours(args):
             "l2": "inputs 14.8 GB per GPU, larger than the 129 MB L2: no flush",
         } if not args.small else {
             "workload": (f"profile case: flat slab of {n_slab} elements, R={R}, one bucket"
-                         + (f", {args.micro} local micro-step" if args.micro else
+                         + (", unfused schedule" if ws is not None else
+                            f", {args.micro} local micro-step" if args.micro else
                             ", reducing step with fp32 accumulators" if acc is not None else "")),
             "R": R, "n_slab": n_slab, "bucket_bytes": 0},
         "hbm_gbs": round(bytes_per_param * n_slab / (ms * 1e-3) / 1e9, 1),
         "hbm_pct_of_8tbs": round(100 * bytes_per_param * n_slab / (ms * 1e-3) / 8e12, 2),
         "roofline": roofline,
         "clocks": clk,
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": launches * args.steps * (2 if ws is not None else 1),
     }
 
     if not args.no_unfused and not args.small:
@@ -998,6 +1011,8 @@ def parse_args(argv=None):
                         "one bucket, device timing only")
     p.add_argument("--reducing", action="store_true",
                    help="with --small: time the reducing step with fp32 accumulators")
+    p.add_argument("--unfused", action="store_true",
+                   help="with --small: time the unfused schedule (reduce, AdamW, copies)")
     p.add_argument("--micro", choices=("first", "later"), default=None,
                    help="with --small: time one local micro-step (acc = g, or acc += g)")
     p.add_argument("--no-e2e", action="store_true")
