@@ -40,6 +40,38 @@ def test_exports_every_declared_symbol():
         assert callable(getattr(capi, name)), name
 
 
+def test_header_is_plain_c_and_links(tmp_path):
+    """include/cc_dp.h compiles as C99 with warnings as errors, and a C
+    program that calls the ABI links against the library and runs without
+    a GPU (the planner is host-only)."""
+    src = tmp_path / "use_abi.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "cc_dp.h"
+int main(void) {
+    size_t numel[3] = {100, 7, 300};
+    size_t offsets[3], begin[4], end[4], n_padded = 0;
+    int count = 0;
+    int st = cc_plan_buckets(numel, 3, 512, offsets, begin, end, 4, &count, &n_padded);
+    cc_overlap_cfg cfg = {0};
+    (void)cfg;
+    printf("%s %d %zu %zu\n", cc_status_string(st), count, n_padded, offsets[2]);
+    return st == CC_OK ? 0 : 1;
+}
+""")
+    exe = tmp_path / "use_abi"
+    lib_dir = os.path.dirname(capi.LIBRARY)
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER),
+           str(src), "-o", str(exe), f"-L{lib_dir}", "-lcc_dp", f"-Wl,-rpath,{lib_dir}"]
+    import subprocess
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    # 300 -> [0, 304), 7 -> [304, 312), 100 -> [312, 416): buckets close at >= 512 B
+    assert r.stdout.split() == ["CC_OK", "2", "416", "0"]
+
+
 def test_status_strings():
     assert capi.cc_status_string(0) == "CC_OK"
     for code, name in [(-1, "CC_ERR_INVALID"), (-2, "CC_ERR_ALIAS"),
