@@ -74,6 +74,27 @@ MUTATIONS = {
     "all-reduce truncates to bf16":
         ("        const uint16_t b = oracle_bf16_round(s);\n        for (int r = 0; r < R; ++r) out[r][i] = b;",
          "        uint32_t u_; memcpy(&u_, &s, 4);\n        const uint16_t b = (uint16_t)(u_ >> 16);\n        for (int r = 0; r < R; ++r) out[r][i] = b;"),
+    "accumulator ignored for replica 0":
+        ("s = acc[0][i] + oracle_bf16_widen(grads[0][i]);",
+         "s = oracle_bf16_widen(grads[0][i]);"),
+    "beta1 decays the second moment":
+        ("const float v_decayed = beta2 * v[i];",
+         "const float v_decayed = beta1 * v[i];"),
+    "square root dropped":
+        ("const float denom = sqrtf(v_hat) + eps;",
+         "const float denom = v_hat + eps;"),
+    "eps dropped":
+        ("const float denom = sqrtf(v_hat) + eps;",
+         "const float denom = sqrtf(v_hat);"),
+    "NaN not kept a NaN by the cast":
+        ("        return (uint16_t)((u >> 16) | 0x0040u);",
+         "        return (uint16_t)(u >> 16);"),
+    "widening shifts by 15":
+        ("float oracle_bf16_widen(uint16_t h) { return bits_to_f32((uint32_t)h << 16); }",
+         "float oracle_bf16_widen(uint16_t h) { return bits_to_f32((uint32_t)h << 15); }"),
+    "micro-step adds the gradient twice":
+        ("                acc[r][i] = acc[r][i] + g;",
+         "                acc[r][i] = acc[r][i] + g + g;"),
     "only replica 0 receives parameters":
         ("for (int r = 0; r < R; ++r) params_out[r][i] = b;",
          "params_out[0][i] = b; for (int r = 1; r < R; ++r) params_out[r][i] = 0;"),
