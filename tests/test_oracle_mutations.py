@@ -113,7 +113,7 @@ def _run_pins_on(mutated_source: str) -> subprocess.CompletedProcess:
                         ignore=ign)
         pkg = "gradient_reduce_optimizer_gb300"
         os.makedirs(os.path.join(work, pkg))
-        for name in ("__init__.py", "workloads.py"):
+        for name in ("__init__.py", "capi.py", "workloads.py"):
             shutil.copy(os.path.join(ROOT, pkg, name), os.path.join(work, pkg))
         shutil.copy(os.path.join(ROOT, "pytest.ini"), work)
         return subprocess.run(
