@@ -352,9 +352,162 @@ def time_oracle(R, sample, min_seconds, max_seconds, threads=1):
     return sample * passes / el, sample, passes, el
 
 
+def host_bytes_available() -> int:
+    try:
+        return os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        return 0
+
+
+def to_host_inputs(grads, state):
+    """Host copies (bf16 bits as uint16, fp32) of device inputs drawn by the
+    workload generators."""
+    import numpy as np
+    import torch
+    g16 = [g.view(torch.int16).cpu().numpy().view(np.uint16) for g in grads]
+    st = [x.cpu().numpy() for x in state]
+    return g16, st
+
+
+def time_full_steps(g16, st, hp, threads, min_passes=1, min_seconds=0.0):
+    """The oracle's step over whole slabs: one untimed pass when more than
+    one thread runs (to start the pool), then timed passes until both
+    min_passes and min_seconds are met.  Returns (seconds per step, passes,
+    threads used)."""
+    runner = OracleRunner(g16, st, hp, threads)
+    if len(runner.chunks) > 1:
+        runner.step()
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        runner.step()
+        passes += 1
+        el = time.perf_counter() - t0
+        if passes >= min_passes and el >= min_seconds:
+            break
+    runner.close()
+    return el / passes, passes, len(runner.chunks)
+
+
+def run_cpu_baseline(args, wk, dev):
+    """The oracle (single-threaded C, as it stands) timed on the host's cores
+    on whole steps: the headline workload's full step (336,226,120 slab
+    elements, R = 8) on one core and on every core, the small flat case
+    (1,048,576 elements, R = 2) in full, and the 2.7B GPT-2 slice (R = 4) on
+    one eighth of its slab, extrapolated.  Inputs are drawn by the same
+    seeded generators on the device and copied to the host; the gradient
+    slabs are the headline step's own (kernels only read them), master/m/v
+    are drawn afresh.  Also the bounded 4M-element sample of earlier runs."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+
+    w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
+    cores = host_cores()
+    hp = step_args(wk, w.step)
+    out = {"unit": UNIT, "kind": "oracle", "host_cores": cores}
+
+    # C2, the headline step, whole
+    need = n_slab * (2 * R + 12 + 2 * R) * 2          # inputs, outputs, slack
+    avail = host_bytes_available()
+    if avail and avail < need:
+        out["headline_full_step"] = {"skipped": f"host memory: {avail} B free, {need} B needed"}
+    else:
+        state = wl.make_state(n_slab, w.step, w.grad_sigma, master_sigma=w.master_sigma,
+                              device=dev)
+        g16, st = to_host_inputs(wk["grads"], state)
+        del state
+        torch.cuda.empty_cache()
+        t1, p1, _ = time_full_steps(g16, st, hp, 1)
+        tn, pn, used = time_full_steps(g16, st, hp, cores, min_passes=3)
+        out["headline_full_step"] = {
+            "workload": f"BERT-large list, R={R}, {n_slab:,} slab elements (one whole step)",
+            "one_core": {"s_per_step": round(t1, 3), "params_per_s": round(w.n / t1),
+                         "passes": p1},
+            "all_cores": {"s_per_step": round(tn, 4), "params_per_s": round(w.n / tn),
+                          "passes": pn, "cores": used}}
+        del g16, st
+
+    # C1, the small flat case, whole
+    c1 = wl.flat_1m_r2()
+    grads = wl.make_grads(c1.R, c1.n, c1.grad_sigma, device=dev)
+    state = wl.make_state(c1.n, c1.step, c1.grad_sigma, device=dev)
+    g16, st = to_host_inputs(grads, state)
+    hp1 = dict(lr=c1.lr, beta1=c1.beta1, beta2=c1.beta2, eps=c1.eps,
+               weight_decay=c1.weight_decay, step=c1.step, grad_scale=c1.grad_scale)
+    t1, p1, _ = time_full_steps(g16, st, hp1, 1, min_seconds=1.0)
+    tn, pn, used = time_full_steps(g16, st, hp1, cores, min_seconds=1.0)
+    out["flat_1m_r2_full_step"] = {
+        "one_core": {"ms_per_step": round(1e3 * t1, 3), "params_per_s": round(c1.n / t1),
+                     "passes": p1},
+        "all_cores": {"ms_per_step": round(1e3 * tn, 3), "params_per_s": round(c1.n / tn),
+                      "passes": pn, "cores": used}}
+    del grads, state, g16, st
+
+    # C3, one eighth of the GPT-2 slice (every tensor is a multiple of 8
+    # elements, so the slab has no padding), extrapolated to the whole
+    c3 = wl.gpt2_slice_r4()
+    part = c3.n // 8 // 8 * 8
+    need3 = part * (2 * c3.R + 12 + 2 * c3.R) * 2
+    if avail and avail < need3:
+        out["gpt2_slice_eighth"] = {"skipped": f"host memory: {avail} B free, {need3} B needed"}
+    else:
+        grads = wl.make_grads(c3.R, part, c3.grad_sigma, device=dev, premultiply=c3.grad_scale)
+        state = wl.make_state(part, c3.step, c3.grad_sigma, device=dev)
+        g16, st = to_host_inputs(grads, state)
+        del grads, state
+        torch.cuda.empty_cache()
+        hp3 = dict(lr=c3.lr, beta1=c3.beta1, beta2=c3.beta2, eps=c3.eps,
+                   weight_decay=c3.weight_decay, step=c3.step, grad_scale=c3.grad_scale)
+        t1, p1, _ = time_full_steps(g16, st, hp3, 1)
+        tn, pn, used = time_full_steps(g16, st, hp3, cores, min_passes=3)
+        scale = c3.n / part
+        out["gpt2_slice_eighth"] = {
+            "workload": (f"GPT-2 slice recipe, R={c3.R}, first {part:,} of {c3.n:,} "
+                         "elements; whole-step seconds extrapolated x8 (elementwise step)"),
+            "one_core": {"s_per_eighth": round(t1, 3),
+                         "s_per_step_extrapolated": round(t1 * scale, 2),
+                         "params_per_s": round(part / t1), "passes": p1},
+            "all_cores": {"s_per_eighth": round(tn, 4),
+                          "s_per_step_extrapolated": round(tn * scale, 3),
+                          "params_per_s": round(part / tn), "passes": pn, "cores": used}}
+        del g16, st
+
+    # the bounded sample of earlier runs, kept beside the whole steps
+    v, sample, passes, el = time_oracle(R, args.cpu_sample, 3.0, 10.0)
+    out["sample_4m"] = {"params_per_s": round(v), "cores": 1,
+                        "sample": f"first {sample:,} slab elements, {passes} passes in {el:.1f} s"}
+
+    full = out.get("headline_full_step", {})
+    if "one_core" in full:
+        out["value"] = full["one_core"]["params_per_s"]
+        out["cores"] = 1
+        out["sample"] = (f"one whole step of the same workload ({n_slab:,} slab elements, "
+                         f"R={R}), single-threaded C oracle, {full['one_core']['passes']} "
+                         f"pass(es) of {full['one_core']['s_per_step']} s")
+    else:
+        out["value"], out["cores"] = round(v), 1
+        out["sample"] = (f"first {sample:,} slab elements of the same workload (R={R}), "
+                         f"{passes} passes in {el:.1f} s, single-threaded C oracle")
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+
+def headline_config(args, R, world, n_params, n_slab, bucket_bytes):
+    """The `config` of the headline line, shared by both arms."""
+    return {
+        "workload": (f"BERT-large parameter list (336,226,108 params, 398 tensors), "
+                     f"R={R} emulated replicas, {args.bucket_mib} MiB buckets in "
+                     "reverse layer order, AdamW wd=0.01 step>=10, bf16 grads "
+                     "N(0,1e-3) x U(0.5,2) per layer"),
+        "R": R, "n_params": n_params, "n_slab": n_slab,
+        "bucket_bytes": bucket_bytes,
+        "launches_per_step": launches_per_step(n_slab, bucket_bytes),
+        "parallelism": f"replicas x{world} (R={R} emulated per GPU)",
+        "l2": "inputs 14.8 GB per GPU, larger than the 129 MB L2: no flush",
+    }
+
 
 def run_ours(args):
     import torch
@@ -375,6 +528,8 @@ def run_ours(args):
     if args.small:
         wk = build_small_workload(dev, args.small)
         args.no_e2e = args.no_overlap = args.no_cpu_baseline = True
+        args.no_unfused = args.no_tp = args.no_launch_floor = True
+        args.no_gpt2_slice = args.no_accum = True
     else:
         wk = build_workload(dev, bucket_mib=args.bucket_mib)
     w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
@@ -468,16 +623,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {
-            "workload": (f"BERT-large parameter list (336,226,108 params, 398 tensors), "
-                         f"R={R} emulated replicas, {args.bucket_mib} MiB buckets in "
-                         "reverse layer order, AdamW wd=0.01 step>=10, bf16 grads "
-                         "N(0,1e-3) x U(0.5,2) per layer"),
-            "R": R, "n_params": n_params, "n_slab": n_slab,
-            "bucket_bytes": bb, "launches_per_step": launches,
-            "parallelism": f"replicas x{world} (R={R} emulated per GPU)",
-            "l2": "inputs 14.8 GB per GPU, larger than the 129 MB L2: no flush",
-        } if not args.small else {
+        "config": headline_config(args, R, world, n_params, n_slab, bb)
+        if not args.small else {
             "workload": (f"profile case: flat slab of {n_slab} elements, R={R}, one bucket"
                          + (", unfused schedule" if ws is not None else
                             f", {args.micro} local micro-step" if args.micro else
@@ -502,6 +649,11 @@ def run_ours(args):
         result["accumulation"] = run_accumulation(args, wk, stream)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wk, stream, world, dev)
+    if args.small and args.overlap_small:
+        # profile case: the overlap bench on the flat slab cut into 4 layers
+        # (the proxy GEMM is the full-size one; a few GB resident)
+        swk = small_overlap_workload(wk, 4)
+        result["overlap_small"] = run_overlap(args, swk, dev, [1], num_layers=4)
     if not args.no_overlap:
         result["overlap"] = run_overlap(args, wk, dev, [args.bucket_mib])
         result["overlap_rank_share"] = run_overlap(args, wk, dev, [args.bucket_mib],
@@ -513,29 +665,30 @@ def run_ours(args):
             "rank_share_48_sms": run_overlap(args, wk, dev, [args.bucket_mib],
                                              rank_share=True, comm_sms=48)}
         if not args.no_sweep:
-            keep = ("bucket_mib", "num_buckets", "t_bwd_ms", "t_comm_ms",
-                    "t_step_overlap_ms", "t_step_seq_ms", "exposed_ms",
-                    "exposed_bound_ms")
             sweep = {}
             for share in (False, True):
                 rows = run_overlap(args, wk, dev, [1, 4, 25, 100, 500], rank_share=share)
                 sweep["rank_share" if share else "all_replicas"] = [
-                    {k: r[k] for k in keep} for r in rows]
+                    {k: r[k] for k in OVERLAP_KEEP} for r in rows]
             result["overlap_sweep"] = sweep
+        if not args.no_accum:
+            # the reducing k-th step of accumulation (k = 4) behind the same
+            # backward: accumulators that stand for three earlier micro-steps
+            acc = [torch.empty(n_slab, dtype=torch.float32, device=dev) for _ in range(R)]
+            for j in range(3):
+                capi.cc_accumulate_local(wk["grads"], acc, n_slab, R, j == 0, stream=stream)
+            torch.cuda.synchronize()
+            red = {}
+            for share in (False, True):
+                rows = run_overlap(args, wk, dev, [1, 4, 25, 100, 500], rank_share=share,
+                                   acc=acc)
+                red["rank_share" if share else "all_replicas"] = [
+                    {k: r[k] for k in OVERLAP_KEEP} for r in rows]
+            result["overlap_reducing_step"] = red
+            del acc
+            torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, passes, el = time_oracle(R, args.cpu_sample, 10.0, 30.0)
-        result["cpu_baseline"] = {
-            "value": round(v), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"first {sample:,} slab elements of the same workload (R={R}), "
-                       f"{passes} passes in {el:.1f} s, single-threaded C oracle")}
-        cores = host_cores()
-        if cores > 1:
-            va, sa, pa, ela = time_oracle(R, args.cpu_sample * 4, 5.0, 15.0, threads=cores)
-            result["cpu_baseline"]["all_cores"] = {
-                "value": round(va), "unit": UNIT, "cores": cores,
-                "sample": (f"first {sa:,} slab elements, {pa} passes in {ela:.1f} s, "
-                           f"split into {cores} contiguous chunks, one oracle call "
-                           "per chunk on its own thread")}
+        result["cpu_baseline"] = run_cpu_baseline(args, wk, dev)
     if rank == 0:
         print(json.dumps(result), flush=True)
     return result
@@ -898,15 +1051,22 @@ def shard_range(begin, end, count, index):
     return lo, hi
 
 
-def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0):
-    """Exposed time of the bucketed step behind a proxy backward of 24 layers
-    x 3 bf16 GEMMs (M=8192, N=K=1024); buckets planned at each size.
+def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0, acc=None,
+                num_layers=24):
+    """Exposed time of the bucketed step behind a proxy backward of
+    num_layers x 3 bf16 GEMMs (M=8192, N=K=1024); buckets planned at each
+    size.
 
     rank_share=False: one GPU carries all R replicas' traffic (the emulated
     step).  rank_share=True: one rank's share of the sharded step -- each
     bucket shrinks to rank 0's 1/R shard: it reads the R replicas' gradients
     of the shard, updates the shard's master/m/v and writes the shard's
-    parameters to all R replica slabs, (4 + 24/R) bytes per parameter."""
+    parameters to all R replica slabs, (4 + 24/R) bytes per parameter.
+    acc: the R fp32 accumulators of gradient accumulation, which makes every
+    bucket the reducing k-th step ((8R + 24) bytes per parameter; a rank's
+    share (8 + 24/R)): "That reducing step has only its own backward compute
+    to hide a full model's worth of gradient traffic" (Overlapping
+    Communication and Computation)."""
     import torch
     from gradient_reduce_optimizer_gb300 import capi
 
@@ -929,22 +1089,46 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0):
         r = capi.cc_overlap_bench(
             grads=wk["grads"], master=wk["master"], m=wk["m"], v=wk["v"],
             params_out=wk["outs"], n=n_slab, R=w.R, buckets=buckets,
-            ready_layers=ready, num_layers=24, gemms_per_layer=3, gemm_m=M,
+            ready_layers=ready, num_layers=num_layers, gemms_per_layer=3, gemm_m=M,
             gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
             warmup=args.warmup, iters=args.overlap_iters,
             max_ctas=args.overlap_ctas, stream_priority=args.stream_priority,
             comm_sms=comm_sms, gemm_algo=args.overlap_gemm_algo,
-            budget_buckets=args.overlap_budget_buckets, **step_args(wk, w.step))
+            budget_buckets=args.overlap_budget_buckets, acc=acc,
+            **step_args(wk, w.step))
         r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
         r["bucket_mib"] = mib
-        r["mode"] = "rank share (1/R of each bucket)" if rank_share else "all R replicas"
+        r["mode"] = (("rank share (1/R of each bucket)" if rank_share else "all R replicas")
+                     + (", reducing step with fp32 accumulators" if acc is not None else ""))
         r["exposed_pct_of_bwd"] = round(100 * r["exposed_ms"] / r["t_bwd_ms"], 1)
-        r["bwd_tflops"] = round(24 * 3 * 2 * M * N * K / (r["t_bwd_ms"] * 1e-3) / 1e12, 1)
+        r["bwd_tflops"] = round(num_layers * 3 * 2 * M * N * K / (r["t_bwd_ms"] * 1e-3) / 1e12,
+                                1)
         bf16_peak = measured_bf16_peak()
         r["bwd_frac_of_measured_bf16"] = (round(r["bwd_tflops"] / bf16_peak, 3)
                                           if bf16_peak else None)
         out.append(r)
     return out[0] if len(out) == 1 else out
+
+
+OVERLAP_KEEP = ("bucket_mib", "num_buckets", "t_bwd_ms", "t_comm_ms", "t_step_overlap_ms",
+                "t_step_seq_ms", "exposed_ms", "exposed_bound_ms", "t_overlap_ms",
+                "overlap_eff")
+
+
+def small_overlap_workload(wk, num_layers):
+    """The profile case's flat slab seen as num_layers equal tensors (one
+    per layer), so that the overlap bench has buckets that become ready
+    layer by layer, with few GB resident."""
+    n = wk["n_slab"]
+    per = n // num_layers // 8 * 8
+    numel = [per] * (num_layers - 1) + [n - per * (num_layers - 1)]
+    wk = dict(wk)
+    wk["numel"], wk["layer_of"] = numel, list(range(num_layers))
+    from gradient_reduce_optimizer_gb300 import capi
+    offsets, _, n_slab = capi.cc_plan_buckets(numel, 0)
+    assert n_slab == n
+    wk["offsets"] = offsets
+    return wk
 
 
 # ---------------------------------------------------------------------------
@@ -961,7 +1145,10 @@ def run_reference(args):
     from oracle import build as obuild
     obuild.build()
     import oracle
-    R = 8
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+    w = wl.bert_large_r8(bucket_bytes=args.bucket_mib * wl.MiB)
+    R = w.R
+    _, _, n_slab = oracle.plan_buckets(w.numel(), w.bucket_bytes)
     threads = args.ref_threads or host_cores()
     g16, st, hp, sample = oracle_sample_inputs(R, args.ref_sample)
     runner = OracleRunner(g16, st, hp, threads)
@@ -984,8 +1171,7 @@ def run_reference(args):
         "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": "BERT-large parameter list, R=8, 25 MiB buckets "
-                   "(bounded sample per step)", "R": R, "sample_elements": sample},
+        "config": headline_config(args, R, world, w.n, n_slab, w.bucket_bytes),
         "cpu_baseline": {"value": round(value), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -1030,6 +1216,9 @@ def parse_args(argv=None):
                    help="skip timing the unfused (reduce, AdamW, copies) schedule")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-overlap", action="store_true")
+    p.add_argument("--overlap-small", action="store_true",
+                   help="with --small: the overlap bench on the flat slab cut into 4 "
+                        "layers (profile case for the proxy GEMM)")
     p.add_argument("--overlap-iters", type=int, default=20)
     p.add_argument("--overlap-ctas", type=int, default=0)
     p.add_argument("--overlap-budget-buckets", type=int, default=0,

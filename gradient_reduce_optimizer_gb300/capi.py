@@ -21,6 +21,7 @@ LIBRARY = os.path.join(PKG, "libcc_dp.so")
 
 CC_MAX_R = 16
 CC_PAD_ELEMS = 8
+CC_NOALLOC_SCRATCH_ELEMS = 16 * 1024 * 1024   # fixed scratch of the allocation-free entry point
 CC_OK = 0
 CC_ERR_INVALID = -1
 CC_ERR_ALIAS = -2
@@ -65,7 +66,7 @@ class cc_overlap_result(ctypes.Structure):
         ("t_bwd_ms", _f), ("t_comm_ms", _f), ("t_step_overlap_ms", _f),
         ("t_step_seq_ms", _f), ("exposed_ms", _f), ("exposed_bound_ms", _f),
         ("num_buckets", _i), ("comm_sms", _i), ("compute_sms", _i),
-        ("gemm_algos", _i),
+        ("gemm_algos", _i), ("t_overlap_ms", _f), ("overlap_eff", _f),
     ]
 
 

@@ -102,6 +102,10 @@ int check_device_range(const void *ptr, size_t bytes, const char *name);
 // host allocation mapped at the same device address is accepted too.
 int check_slab_range(const void *ptr, size_t bytes, const char *name, bool allow_host);
 
+// The one-shot launch failure armed by cc_inject_launch_failure: true (and
+// disarmed) when the bucket launch about to be made must fail instead.
+bool injected_failure();
+
 // Validate and round the AdamW hyper-parameters to the kernel's scalars.
 int make_scalars(float lr, float beta1, float beta2, float eps,
                  float weight_decay, int step, float grad_scale,

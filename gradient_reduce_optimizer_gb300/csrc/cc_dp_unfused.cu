@@ -19,12 +19,14 @@
 // differs.  It moves (2R + 4) + (4 + 24 + 2) + 4(R - 1) = 6R + 30 bytes per
 // parameter against the fused 4R + 24 (78 against 56 at R = 8).
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "cc_dp_device.cuh"
 #include "cc_dp_internal.h"
+#include "cc_trace.h"
 
 namespace ccdp {
 namespace {
@@ -213,11 +215,34 @@ static __device__ __align__(256) float g_noalloc_scratch[CC_NOALLOC_SCRATCH_ELEM
 
 constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mutex;
-float *g_scratch_addr[kMaxScratchDevices] = {};
+struct ScratchAddress {
+    CUcontext ctx;   // the context the address was looked up in
+    float *ptr;
+};
+ScratchAddress g_scratch_addr[kMaxScratchDevices] = {};
 
-// The device address of g_noalloc_scratch on the current device, looked up
-// once per device.  In host code the array's name is only a host-side
-// stand-in, so the address must come from cudaGetSymbolAddress.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+// cuCtxGetCurrent through the runtime's driver entry points (no link-time
+// libcuda), looked up once.
+CtxGetCurrentFn ctx_get_current_fn() {
+    static const CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
+
+// The device address of g_noalloc_scratch on the current device.  In host
+// code the array's name is only a host-side stand-in, so the address comes
+// from cudaGetSymbolAddress, looked up once per device and context: a
+// device reset destroys the primary context and the module with it, so a
+// context other than the one of the last lookup means a new lookup.
 int scratch_address(float **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -225,14 +250,23 @@ int scratch_address(float **out) {
     if (dev < 0 || dev >= kMaxScratchDevices)
         return fail(CC_ERR_UNSUPPORTED, "device %d beyond the %d supported", dev,
                     kMaxScratchDevices);
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    if (!get_ctx) return fail(CC_ERR_UNSUPPORTED, "cuCtxGetCurrent unavailable");
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddress &a = g_scratch_addr[dev];
+    if (!ctx || !a.ptr || a.ctx != ctx) {
+        // The lookup makes the device's primary context current if no
+        // context was; the context is then read again for the cache key.
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(scratch)");
-        g_scratch_addr[dev] = static_cast<float *>(p);
+        if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+        a.ptr = static_cast<float *>(p);
+        a.ctx = ctx;
     }
-    *out = g_scratch_addr[dev];
+    *out = a.ptr;
     return CC_OK;
 }
 
@@ -245,6 +279,7 @@ extern "C" int cc_unfused_dp_step_noalloc(const void *const *grads, float *maste
                                           float beta2, float eps, float weight_decay,
                                           int step, float grad_scale, void *stream) {
     using namespace ccdp;
+    TraceRange call("cc_unfused_dp_step_noalloc", n);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     AdamScalars c;
     int st = make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
@@ -252,12 +287,22 @@ extern "C" int cc_unfused_dp_step_noalloc(const void *const *grads, float *maste
     if (n == 0) return CC_OK;
     const size_t per = bucket_elems(bucket_bytes, n);
     const size_t largest = per < n ? per : n;
-    if (largest > CC_NOALLOC_SCRATCH_ELEMS)
+    if (largest > CC_NOALLOC_SCRATCH_ELEMS) {
+        if (bucket_bytes == 0 || per >= n)
+            return fail(CC_ERR_INVALID,
+                        "n=%zu elements in one bucket exceed the fixed scratch of %u "
+                        "elements; cut the step into buckets of at most %u elements "
+                        "(bucket_bytes < %u) or use cc_unfused_dp_step with a workspace",
+                        n, static_cast<unsigned>(CC_NOALLOC_SCRATCH_ELEMS),
+                        static_cast<unsigned>(CC_NOALLOC_SCRATCH_ELEMS),
+                        static_cast<unsigned>(2u * CC_NOALLOC_SCRATCH_ELEMS + 16u));
         return fail(CC_ERR_INVALID,
-                    "a bucket of %zu elements exceeds the fixed scratch of %u elements; "
-                    "use bucket_bytes <= %u (or cc_unfused_dp_step with a workspace)",
-                    largest, static_cast<unsigned>(CC_NOALLOC_SCRATCH_ELEMS),
-                    static_cast<unsigned>(2u * CC_NOALLOC_SCRATCH_ELEMS));
+                    "bucket_bytes=%zu gives buckets of %zu elements (floor(bucket_bytes/16)*8), "
+                    "more than the fixed scratch of %u elements; use bucket_bytes < %u "
+                    "or cc_unfused_dp_step with a workspace",
+                    bucket_bytes, per, static_cast<unsigned>(CC_NOALLOC_SCRATCH_ELEMS),
+                    static_cast<unsigned>(2u * CC_NOALLOC_SCRATCH_ELEMS + 16u));
+    }
     Slabs s;
     st = validate_slabs(grads, nullptr, master, m, v, params_out, n, R, false, &s);
     if (st != CC_OK) return st;
@@ -267,6 +312,9 @@ extern "C" int cc_unfused_dp_step_noalloc(const void *const *grads, float *maste
     // the AdamW kernel reads it, so nothing needs clearing between calls.
     for (size_t b = 0; b < n; b += per) {
         const size_t e = b + per < n ? b + per : n;
+        if (injected_failure())
+            return fail(CC_ERR_CUDA, "injected launch failure before the bucket at element %zu", b);
+        TraceRange bucket("bucket", b);
         const cudaError_t err = launch_unfused_bucket(s, c, scratch, b, e,
                                                       static_cast<cudaStream_t>(stream));
         if (err != cudaSuccess) return fail_cuda(err, "allocation-free step launch");

@@ -406,6 +406,11 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     r.gemm_algos = res.algos;
     r.exposed_ms = r.t_step_overlap_ms - r.t_bwd_ms;
     r.exposed_bound_ms = std::max(0.0f, r.t_comm_ms - r.t_bwd_ms);
+    // The step-time equation solved for the hidden part: T_overlap =
+    // T_bwd + T_comm - T_step, as a fraction of the most that could hide.
+    r.t_overlap_ms = r.t_bwd_ms + r.t_comm_ms - r.t_step_overlap_ms;
+    const float hideable = std::min(r.t_comm_ms, r.t_bwd_ms);
+    r.overlap_eff = hideable > 0.0f ? r.t_overlap_ms / hideable : 0.0f;
     r.num_buckets = c.num_buckets;
     r.comm_sms = res.comm_sms;
     r.compute_sms = res.compute_sms;

@@ -253,13 +253,16 @@ CC_API int cc_unfused_dp_step(const void *const *grads, float *master, float *m,
  * inside the library's own device memory, which every GPU that loads the
  * library holds until the process exits.  It allocates nothing.
  *
- *  - A bucket (min(n, floor(bucket_bytes/16)*8 elements)) larger than the
- *    array is rejected with CC_ERR_INVALID: keep bucket_bytes <=
- *    2 * CC_NOALLOC_SCRATCH_ELEMS (32 MiB), or n within the array when
- *    bucket_bytes is 0.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) for that device; make that first call before
- *    any stream capture begins.
+ *  - The largest bucket, min(n, floor(bucket_bytes/16)*8) elements (n when
+ *    bucket_bytes is 0), must fit the array: floor(bucket_bytes/16)*8 <=
+ *    CC_NOALLOC_SCRATCH_ELEMS, i.e. bucket_bytes < 2*CC_NOALLOC_SCRATCH_ELEMS
+ *    + 16 (32 MiB + 16 bytes), or n <= CC_NOALLOC_SCRATCH_ELEMS.  A larger
+ *    bucket is rejected with CC_ERR_INVALID before any launch, and the
+ *    reason names whichever of n and bucket_bytes set its size.
+ *  - The first call on a device (and the first after a device reset, which
+ *    makes a new context) looks up the array's device address
+ *    (cudaGetSymbolAddress) for that device with it current; make that
+ *    first call before any stream capture begins.
  *  - Every call shares the one array, and each bucket overwrites the part
  *    it uses before reading it, so no state carries over between calls.
  *    Calls that overlap on the GPU (on different streams, or from different
@@ -334,6 +337,10 @@ CC_API int cc_bucket_ready_layers(const size_t *numel, const int *layer_of,
  *   t_step_seq_ms     GEMMs, then all buckets, on one stream.
  * exposed_ms = t_step_overlap_ms - t_bwd_ms; exposed_bound_ms =
  * max(0, t_comm_ms - t_bwd_ms), the least any schedule can expose.
+ * t_overlap_ms = t_bwd_ms + t_comm_ms - t_step_overlap_ms is the time the
+ * step-time equation says was hidden (negative when the overlapped arm is
+ * slower than the two parts back to back), and overlap_eff = t_overlap_ms /
+ * min(t_comm_ms, t_bwd_ms) the fraction of what could hide that did.
  *
  * The slabs are stepped for real (master/m/v change on every run).  The GEMM
  * operands are caller-owned bf16 device buffers: A holds M*K, B K*N and C
@@ -380,6 +387,7 @@ typedef struct cc_overlap_result {
     int num_buckets;
     int comm_sms, compute_sms;     /* the partition's SM counts (0 without one) */
     int gemm_algos;                /* cuBLASLt candidates offered (0 with gemm_algo 0) */
+    float t_overlap_ms, overlap_eff;
 } cc_overlap_result;
 
 CC_API int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out);
@@ -445,7 +453,8 @@ CC_API int cc_device_status(unsigned *status, int clear);
  * cc_inject_launch_failure -- failure injection on the host, for testing how
  * errors propagate (no GPU fault is involved).  Arms a one-shot failure for
  * the calling thread: after `after_launches` more bucket launches by
- * cc_fused_dp_step, cc_fused_dp_step_accum or cc_unfused_dp_step, the next
+ * cc_fused_dp_step, cc_fused_dp_step_accum, cc_unfused_dp_step or
+ * cc_unfused_dp_step_noalloc, the next
  * bucket is not launched and the call returns CC_ERR_CUDA ("injected launch
  * failure ...") -- the documented partial-launch case: earlier buckets of
  * that call were enqueued, later ones were not.  -1 disarms.

@@ -317,3 +317,36 @@ def test_inject_launch_failure_arguments():
     with pytest.raises(capi.CCError) as ei:
         capi.cc_inject_launch_failure(-2)
     assert ei.value.status == capi.CC_ERR_INVALID
+
+
+def test_binding_constants_match_the_header():
+    """Every numeric #define of include/cc_dp.h that the binding mirrors has
+    the header's value (the header is the source of truth)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    defines = {k: v for k, v in re.findall(r"#define\s+(CC_\w+)\s+(\([^\n]*\)|\d+)", text)}
+    assert set(defines) >= {"CC_MAX_R", "CC_PAD_ELEMS", "CC_NOALLOC_SCRATCH_ELEMS"}
+    for name, expr in defines.items():
+        value = eval(expr.replace("u", ""))          # plain integer arithmetic
+        assert getattr(capi, name) == value, name
+
+
+def test_noalloc_size_refusals_name_their_cause():
+    """The allocation-free entry point refuses, before looking at any pointer,
+    a bucket larger than its fixed scratch, and says whether n or
+    bucket_bytes set the bucket's size; 15 bytes past 32 MiB still floor to
+    an accepted bucket."""
+    cap = capi.CC_NOALLOC_SCRATCH_ELEMS
+    g, acc, p, m, v, o = fake_slabs(2, cap + 1000)
+    def reason(n, bucket_bytes):
+        try:
+            capi.cc_unfused_dp_step_noalloc(g, p, m, v, o, n, 2, bucket_bytes,
+                                            stream=0, **ADAM)
+            return "ok"
+        except capi.CCError as err:
+            return err.reason if err.status == capi.CC_ERR_INVALID else "other"
+    assert "n=" in reason(cap + 8, 0) and "scratch" in reason(cap + 8, 0)
+    assert "bucket_bytes=" in reason(cap + 1000, 2 * cap + 16)
+    # accepted sizes go on to pointer validation (fake pointers: refused there)
+    for bb in (2 * cap, 2 * cap + 15):
+        r = reason(cap + 1000, bb)
+        assert "scratch" not in r, r

@@ -83,6 +83,7 @@ def test_guard_bands_around_every_slab_stay_intact(R, n):
     capi.cc_accumulate_local(grads, acc, n, R, True)
     capi.cc_accumulate_local(grads, acc, n, R, False)
     capi.cc_unfused_dp_step(grads, master, m, v, outs, work, 4 * n, n, R, 2048, **HP)
+    capi.cc_unfused_dp_step_noalloc(grads, master, m, v, outs, n, R, 2048, **HP)
     capi.cc_tp_allreduce(partials, outs, n, R)
     torch.cuda.synchronize()
     for s in slabs:

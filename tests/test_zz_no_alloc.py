@@ -48,6 +48,32 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
             assert torch.equal(bits(x), bits(y)), f"call {call}"
 
 
+def test_noalloc_fills_its_whole_scratch():
+    """A bucket of exactly CC_NOALLOC_SCRATCH_ELEMS elements (bucket_bytes of
+    32 MiB, and also 15 bytes past it, which floor to the same bucket) uses
+    the last element of the fixed array; a ragged second bucket follows.
+    Two calls in a row, bit for bit against the workspace entry point."""
+    gbuild.build()
+    R = 2
+    cap = capi.CC_NOALLOC_SCRATCH_ELEMS
+    n = cap + 4096 + 5
+    _, master, m, v = random_inputs(R, n, seed=41, step=2)
+    a = new_slabs([None] * R, master.clone(), m.clone(), v.clone())
+    b = new_slabs([None] * R, master.clone(), m.clone(), v.clone())
+    workspace = torch.empty(cap, dtype=torch.float32, device=DEV)
+    for call, bucket_bytes in enumerate((2 * cap, 2 * cap + 15)):
+        grads = random_inputs(R, n, seed=200 + call, step=1)[0]
+        a.grads = b.grads = grads
+        hp = dict(HP, step=2 + call)
+        capi.cc_unfused_dp_step(a.grads, a.master, a.m, a.v, a.outs, workspace,
+                                workspace.numel() * 4, n, R, bucket_bytes, **hp)
+        capi.cc_unfused_dp_step_noalloc(b.grads, b.master, b.m, b.v, b.outs, n, R,
+                                        bucket_bytes, **hp)
+        torch.cuda.synchronize()
+        for x, y in zip([a.master, a.m, a.v] + a.outs, [b.master, b.m, b.v] + b.outs):
+            assert torch.equal(bits(x), bits(y)), f"call {call}"
+
+
 def test_noalloc_refuses_buckets_beyond_its_scratch():
     gbuild.build()
     R, n = 2, 4096
@@ -57,4 +83,12 @@ def test_noalloc_refuses_buckets_beyond_its_scratch():
         capi.cc_unfused_dp_step_noalloc(s.grads, s.master, s.m, s.v, s.outs, too_many,
                                         R, 0, step=1, **HP)
     assert ei.value.status == capi.CC_ERR_INVALID
-    assert "scratch" in ei.value.reason
+    assert "scratch" in ei.value.reason and "n=" in ei.value.reason
+    # the same refusal when bucket_bytes sets the size: 16 bytes past the edge
+    big = torch.empty(too_many, dtype=torch.float32, device=DEV)
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_unfused_dp_step_noalloc([big] * R, big, big, big, [big] * R, too_many, R,
+                                        2 * capi.CC_NOALLOC_SCRATCH_ELEMS + 16,
+                                        step=1, **HP)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    assert "bucket_bytes=" in ei.value.reason
