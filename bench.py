@@ -854,12 +854,55 @@ def run_tp(args, dev, R=8, m=8192, n=3072, k=12288, chunk_list=(1, 2, 4, 8, 16))
     ar = rows[0]["t_allreduce_ms"]
     tflops = 2 * m * n * k / (rows[0]["t_gemm_ms"] * 1e-3) / 1e12
     bf16_peak = measured_bf16_peak()
+    del partials
+    fused = run_tp_fused(args, dev, x, w, outs, R, m, n, k,
+                         sequential_ms=rows[0]["t_sequential_ms"])
     return {"shape": {"R": R, "m": m, "n": n, "k": k},
             "gemm_tflops": round(tflops, 1),
             "gemm_frac_of_measured_bf16": round(tflops / bf16_peak, 3) if bf16_peak else None,
             "allreduce_bytes": 6 * R * m * n,
             "allreduce_hbm_gbs": round(6 * R * m * n / (ar * 1e-3) / 1e9, 1),
-            "chunks": rows}
+            "chunks": rows, "fused_tcgen05": fused}
+
+
+def run_tp_fused(args, dev, x, w, outs, R, m, n, k, sequential_ms=None, reps=20):
+    """The same layer through cc_tp_matmul_allreduce: one tcgen05 kernel that
+    keeps the R partial products in TMEM and writes only the R bf16 outputs.
+    The weight shards are given K-contiguous (n x k/R, a linear layer's
+    layout): the transposes of the shards the cuBLAS arm reads."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    kr = k // R
+    wt = [wr.view(kr, n).t().contiguous() for wr in w]
+    stream = torch.cuda.current_stream()
+
+    def call():
+        capi.cc_tp_matmul_allreduce(x, wt, outs, None, m, n, k, R, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    status = capi.cc_device_status(clear=True)
+    tflops = 2 * m * n * k / (ms * 1e-3) / 1e12
+    bf16_peak = measured_bf16_peak()
+    out = {"kernel": "tp_fused_kernel (tcgen05, TMA, TMEM accumulators)",
+           "ms": round(ms, 4), "tflops": round(tflops, 1),
+           "frac_of_measured_bf16": round(tflops / bf16_peak, 3) if bf16_peak else None,
+           "hbm_bytes_algorithmic": 2 * (m * k + n * k) + 2 * R * m * n,
+           "status_word": status, "launches": reps}
+    if sequential_ms:
+        out["speedup_vs_cublas_then_allreduce"] = round(sequential_ms / ms, 3)
+    del wt
+    return out
 
 
 def run_accumulation(args, wk, stream, k=4):

@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libcc_dp.so")
 
 SOURCES = ["cc_dp_kernels.cu", "cc_dp_bulk.cu", "cc_dp_unfused.cu", "cc_dp_api.cu",
-           "cc_overlap.cu", "cc_tp.cu"]
+           "cc_overlap.cu", "cc_tp.cu", "cc_tp_fused.cu"]
 HEADERS = [os.path.join(CSRC, "cc_dp_internal.h"), os.path.join(CSRC, "cc_dp_device.cuh"),
            os.path.join(CSRC, "cc_trace.h"), os.path.join(INCLUDE, "cc_dp.h")]
 

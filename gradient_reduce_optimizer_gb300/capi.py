@@ -106,6 +106,8 @@ _SIGNATURES = {
     "cc_unfused_dp_step_noalloc": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _f, _f,
                                     _f, _f, _f, _i, _f, _vp], _i),
     "cc_tp_allreduce": ([_vp, _vp, _sz, _i, _vp], _i),
+    "cc_tp_matmul_allreduce": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "cc_inject_bulk_stall": ([ctypes.c_longlong, ctypes.c_uint], _i),
     "cc_inject_launch_failure": ([_i], _i),
     "cc_tp_overlap_bench": ([ctypes.POINTER(cc_tp_cfg), ctypes.POINTER(cc_tp_result)], _i),
 }
@@ -351,10 +353,27 @@ def cc_tp_overlap_bench(*, R: int, m: int, n: int, k: int, chunks: int, x, w,
     return {name: getattr(res, name) for name, _ in res._fields_}
 
 
+def cc_tp_matmul_allreduce(x, w, out, partials, m: int, n: int, k: int, R: int,
+                           stream=None) -> None:
+    """The fused tensor-parallel MatMul + AllReduce: x[r] bf16 m x k/R,
+    w[r] bf16 n x k/R (K contiguous), out[r] bf16 m x n; partials None or
+    [R] fp32 m x n (each rank's partial product, for checking)."""
+    _check(lib().cc_tp_matmul_allreduce(
+        _addr_array(x), _addr_array(w), _addr_array(out),
+        _addr_array(partials) if partials is not None else None, m, n, k, R,
+        _stream(stream)), "cc_tp_matmul_allreduce")
+
+
 def cc_inject_launch_failure(after_launches: int) -> None:
     """Arm (or with -1 disarm) a one-shot injected launch failure on this
     thread, for testing error propagation."""
     _check(lib().cc_inject_launch_failure(after_launches), "cc_inject_launch_failure")
+
+
+def cc_inject_bulk_stall(tile: int, timeout_us: int = 20000) -> None:
+    """Arm (or with -1 disarm) a one-shot skipped tile in the next bulk-engine
+    launch on this thread, with its pipeline waits bounded by timeout_us."""
+    _check(lib().cc_inject_bulk_stall(tile, timeout_us), "cc_inject_bulk_stall")
 
 
 def cc_l2_flush(buf, nbytes: int, stream=None) -> None:

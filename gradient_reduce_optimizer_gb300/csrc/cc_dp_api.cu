@@ -563,12 +563,24 @@ int cc_inject_launch_failure(int after_launches) {
     return CC_OK;
 }
 
+int cc_inject_bulk_stall(long long tile, unsigned timeout_us) {
+    if (tile < -1) return fail(CC_ERR_INVALID, "tile=%lld must be >= -1", tile);
+    if (tile >= 0 && (timeout_us < 1 || timeout_us > 1000000))
+        return fail(CC_ERR_INVALID, "timeout_us=%u must be in 1..1000000", timeout_us);
+    arm_bulk_stall(tile, 1000ull * timeout_us);
+    return CC_OK;
+}
+
 int cc_device_status(unsigned *status, int clear) {
     if (!status) return fail(CC_ERR_INVALID, "status is NULL");
     int st = ensure_device();
     if (st != CC_OK) return st;
-    const cudaError_t e = read_bulk_status(status, clear != 0);
-    return e == cudaSuccess ? CC_OK : fail_cuda(e, "status read");
+    unsigned bulk = 0, tp = 0;
+    cudaError_t e = read_bulk_status(&bulk, clear != 0);
+    if (e == cudaSuccess) e = read_tp_status(&tp, clear != 0);
+    if (e != cudaSuccess) return fail_cuda(e, "status read");
+    *status = bulk | tp;
+    return CC_OK;
 }
 
 int cc_l2_flush(void *buf, size_t bytes, void *stream) {

@@ -75,7 +75,10 @@ struct BulkParams {
     int tail_len;
     int tile;            // T, elements per tile (multiple of 8)
     int stages;          // S
-    unsigned long long timeout_ns;  // bound on any single wait
+    unsigned long long timeout_ns;        // bound on a pipeline wait
+    unsigned long long drain_timeout_ns;  // bound on the final wait for copies issued
+    size_t skip_tile;    // failure injection: a tile the producer never issues
+                         // (SIZE_MAX: none)
 };
 
 // Byte offsets of one stage's slices (all multiples of 16).
@@ -249,16 +252,17 @@ fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
             int issued_use[kMaxStages];
             for (int s = 0; s < kMaxStages; ++s) issued_use[s] = -1;
             size_t i = 0;
-            bool ok = true;
             for (size_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
                 const int s = static_cast<int>(i % S);
                 const int k = static_cast<int>(i / S);
                 if (k > 0 &&
                     !mbar_wait(smem_addr(&empty_bar[s]), (k - 1) & 1, p.timeout_ns)) {
                     atomicOr(&g_bulk_status, kStatusProducerTimeout);
-                    ok = false;
                     break;
                 }
+                // Failure injection: this tile is never issued, so its stage
+                // never fills and the consumers' waits for it run out.
+                if (t == p.skip_tile) continue;
                 const size_t e0 = p.begin + t * static_cast<size_t>(T);
                 const size_t left = p.tiled - t * static_cast<size_t>(T);
                 const uint32_t len = static_cast<uint32_t>(left < static_cast<size_t>(T) ? left : T);
@@ -280,15 +284,16 @@ fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
                 bulk_load(smem_addr(st + L.v), p.v + e0, 4u * len, bar, pol);
                 issued_use[s] = k;
             }
-            if (!ok) {
-                // Let the copies already issued land before the CTA can exit.
-                // The consumers learn of the abort through their own bounded
-                // waits on tiles that are never issued.
-                for (int s = 0; s < S; ++s)
-                    if (issued_use[s] >= 0 &&
-                        !mbar_wait(smem_addr(&full_bar[s]), issued_use[s] & 1, p.timeout_ns))
-                        atomicOr(&g_bulk_status, kStatusDrainTimeout);
-            }
+            // Whether the loop ended normally or gave up, every copy issued
+            // lands before this thread -- and so the CTA, whose shared memory
+            // the copies write -- may exit: consumers that abandoned the
+            // pipeline no longer wait for them.  A stage's last issued use
+            // completes its full barrier's phase once its bytes have landed;
+            // issued copies always land, so this wait keeps the long bound.
+            for (int s = 0; s < S; ++s)
+                if (issued_use[s] >= 0 &&
+                    !mbar_wait(smem_addr(&full_bar[s]), issued_use[s] & 1, p.drain_timeout_ns))
+                    atomicOr(&g_bulk_status, kStatusDrainTimeout);
         }
         return;
     }
@@ -368,7 +373,19 @@ constexpr int kMaxDevices = 64;
 bool g_smem_attr_set[kMaxDevices][CC_MAX_R + 1][2];
 std::mutex g_smem_attr_mutex;
 
+// One-shot failure injection of the next bulk-engine launch on this thread
+// (cc_inject_bulk_stall): the tile to skip, or -1, and the wait bound.
+thread_local long long g_stall_tile = -1;
+thread_local unsigned long long g_stall_timeout_ns = 0;
+
+constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;   // one second
+
 }  // namespace
+
+void arm_bulk_stall(long long tile, unsigned long long timeout_ns) {
+    g_stall_tile = tile;
+    g_stall_timeout_ns = timeout_ns;
+}
 
 cudaError_t launch_fused_bulk(const Slabs &s, const AdamScalars &c, size_t begin,
                               size_t end, int num_ctas, cudaStream_t stream) {
@@ -409,7 +426,14 @@ cudaError_t launch_fused_bulk(const Slabs &s, const AdamScalars &c, size_t begin
     p.num_tiles = (p.tiled + T - 1) / T;
     p.tail_begin = begin + p.tiled;
     p.tail_len = static_cast<int>(end - p.tail_begin);
-    p.timeout_ns = 1000000000ull;  // one second per wait
+    p.timeout_ns = kWaitTimeoutNs;
+    p.drain_timeout_ns = kWaitTimeoutNs;
+    p.skip_tile = SIZE_MAX;
+    if (g_stall_tile >= 0) {
+        p.skip_tile = static_cast<size_t>(g_stall_tile);
+        p.timeout_ns = g_stall_timeout_ns;
+        g_stall_tile = -1;
+    }
     size_t grid = num_ctas > 0 ? static_cast<size_t>(num_ctas) : static_cast<size_t>(sms);
     if (grid > static_cast<size_t>(sms)) grid = sms;
     if (p.num_tiles > 0 && grid > p.num_tiles) grid = p.num_tiles;

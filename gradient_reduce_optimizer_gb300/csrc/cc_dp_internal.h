@@ -67,9 +67,29 @@ cudaError_t launch_unfused_bucket(const Slabs &s, const AdamScalars &c, float *w
 // Elements per bucket for a bf16 byte size (0 = the whole slab).
 size_t bucket_elems(size_t bucket_bytes, size_t n);
 
+// Arm a one-shot failure of the next bulk-engine launch on this thread: its
+// producer never issues tile `tile` (counted from the launch's first tile),
+// and its pipeline waits give up after timeout_ns.  tile < 0 disarms.
+void arm_bulk_stall(long long tile, unsigned long long timeout_ns);
+
 // Read (and optionally clear) the bulk engine's status word: 0, or codes of
 // waits that ran out (1 consumer, 2 producer, 4 drain).  Synchronous.
 cudaError_t read_bulk_status(unsigned *status, bool clear);
+
+// The fused tensor-parallel MatMul + AllReduce (cc_tp_fused.cu) on shapes
+// already validated; max_ctas > 0 caps the persistent grid.  Returns a
+// cc_status (the reason recorded with fail()).
+int launch_tp_fused(const void *const *x, const void *const *w, void *const *out,
+                    float *const *partials, int m, int n, int k, int R, int max_ctas,
+                    cudaStream_t stream);
+int tp_fused_tile_m();
+int tp_fused_tile_n();
+int tp_fused_tile_k();
+
+// Read (and optionally clear) the fused tensor-parallel kernel's status word:
+// 0, or codes of waits that ran out (8 producer, 16 MMA, 32 epilogue, 64
+// drain).  Synchronous.
+cudaError_t read_tp_status(unsigned *status, bool clear);
 
 // Multiprocessor count of the current device (queried once per device).
 cudaError_t device_sm_count(int *count);

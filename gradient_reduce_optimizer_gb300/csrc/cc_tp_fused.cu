@@ -1,0 +1,587 @@
+// The tensor-parallel MatMul and the AllReduce that follows it, fused into
+// one tcgen05 kernel for sm_103a ("LIT-735: Breaking the Computation and
+// Communication Abstraction Barrier in Distributed Machine Learning
+// Workloads", Key takeaways: the model-parallel MatMul followed by an
+// AllReduce, whose overlap CoCoNet exploits).
+//
+// R tensor-parallel ranks of a row-parallel linear layer are emulated in one
+// GPU.  Rank r holds X_r (m x k/R, bf16, row-major) and its weight shard W_r
+// (n x k/R, bf16, row-major: the K-contiguous layout of a linear layer's
+// weight) and computes the partial product Y_r = X_r W_r^T with fp32
+// accumulation.  The AllReduce gives every rank
+//     out[r] = bf16_rne( (..((Y_0 + Y_1) + Y_2) .. ) + Y_{R-1} )
+// summed in rank order in fp32, the same value for every r.
+//
+// Unfused, the R partial products go to HBM in fp32 and an AllReduce pass
+// reads them back (4R bytes written + 4R read + 2R written per output
+// element).  Here no partial product leaves the SM: one persistent CTA per
+// SM walks output tiles of 128 x BN, and for each tile
+//   * a producer warp streams 128 x 64 tiles of X_r and BN x 64 tiles of W_r
+//     for r = 0..R-1 with TMA (cp.async.bulk.tensor, 128-byte swizzle) into a
+//     ring of shared-memory stages;
+//   * an MMA warp issues tcgen05.mma (M = 128, N = BN, K = 16, bf16 in, fp32
+//     accumulate) from those stages into one of two TMEM accumulators: rank
+//     r of the CTA's j-th job goes to accumulator (j*R + r) % 2, so the next
+//     rank's MMAs run while the epilogue drains the previous one;
+//   * eight epilogue warps read each finished accumulator from TMEM
+//     (tcgen05.ld), add it to a running fp32 sum in registers in rank order,
+//     release the accumulator, and after the last rank round the sum to bf16
+//     once and store it to all R outputs -- the AllReduce's broadcast --
+//     while the MMA warp already works on the next tile.
+// Only the operands are read and only the R bf16 outputs are written.
+//
+// Every wait on an mbarrier is bounded by the global timer.  A wait that
+// runs out records a code in this file's status word (read through
+// cc_device_status), and its warp leaves its loop; the producer then waits,
+// bounded again, for the copies it issued, the MMA warp for the MMAs it
+// issued, and the TMEM is freed before the CTA exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "cc_dp_internal.h"
+#include "cc_trace.h"
+
+namespace ccdp {
+
+// Codes or-ed in by a wait of the fused tensor-parallel kernel that ran out.
+__device__ unsigned int g_tp_status = 0;
+
+namespace {
+
+#ifndef CC_TP_BN
+#define CC_TP_BN 128   // output columns per tile (tcgen05 N)
+#endif
+
+constexpr int kBM = 128;                 // output rows per tile (MMA M)
+constexpr int kBN = CC_TP_BN;            // output columns per tile (MMA N)
+constexpr int kBK = 64;                  // K per stage: 128 bytes of bf16
+constexpr int kUmmaK = 16;               // K of one tcgen05.mma for 16-bit inputs
+constexpr int kTileA = kBM * kBK * 2;    // 16 KiB
+constexpr int kTileB = kBN * kBK * 2;
+constexpr int kStageBytes = kTileA + kTileB;
+// As many stages as fit beside the alignment slack (at most 8).
+constexpr int kStages = (220 * 1024) / kStageBytes < 8 ? (220 * 1024) / kStageBytes : 8;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kAccCols = 256;            // TMEM columns per accumulator
+constexpr int kTmemCols = 2 * kAccCols;  // two accumulators: all 512 columns
+constexpr int kColsPerThread = kBN / 2;  // each epilogue warp covers half a row
+constexpr int kChunks = kColsPerThread / 16;
+static_assert(kBN % 32 == 0 && kColsPerThread % 16 == 0, "epilogue chunks of 16 columns");
+static_assert(kBN % 16 == 0 && kBN <= 256, "tcgen05 N for M = 128");
+static_assert(kBN <= kAccCols, "an accumulator must fit its TMEM columns");
+static_assert(kTileA % 1024 == 0 && kTileB % 1024 == 0, "128B-swizzle atoms are 1 KiB");
+
+constexpr unsigned kStatusProducer = 8u;
+constexpr unsigned kStatusMma = 16u;
+constexpr unsigned kStatusEpilogue = 32u;
+constexpr unsigned kStatusDrain = 64u;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;   // two seconds per wait
+
+struct TpFusedParams {
+    CUtensorMap tx[CC_MAX_R];     // X_r: {k/R, m}, box {64, 128}
+    CUtensorMap tw[CC_MAX_R];     // W_r: {k/R, n}, box {64, BN}
+    __nv_bfloat16 *out[CC_MAX_R]; // m x n each
+    float *partials[CC_MAX_R];    // m x n each, or all null
+    int R, m, n, kb_per_rank;     // kb_per_rank = (k/R) / 64
+    int tiles_n, num_tiles;
+};
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 st;\n\t"
+                 "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Wait for the phase of this parity to complete, at most kTimeoutNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_test(bar, parity))
+        if (global_ns() - t0 > kTimeoutNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x,
+                                            int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row atoms of 1 KiB one after the
+// other (stride-dimension offset 1024 B), start address in 16-byte units.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);       // start address
+    d |= static_cast<uint64_t>(1) << 16;                      // leading offset (unused)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;              // stride offset: 1 KiB
+    d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, both
+// K-major, fp32 accumulator, M = 128, N = kBN.
+constexpr uint32_t kInstrDesc = (1u << 4)                    // D: f32
+                              | (1u << 7)                    // A: bf16
+                              | (1u << 10)                   // B: bf16
+                              | (static_cast<uint32_t>(kBN >> 3) << 17)
+                              | (static_cast<uint32_t>(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                         uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(kInstrDesc), "r"(accumulate)
+                 : "memory");
+}
+
+// The mbarrier arrives once every tcgen05 operation this thread issued
+// before has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes: lane i of the
+// warp gets row (lane base + i), columns [col, col + 16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t mma_done;
+    __shared__ uint32_t tmem_base_slot;
+
+    // The 128-byte swizzle wants 1 KiB-aligned tiles.
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int R = p.R;
+    const int kb_per_rank = p.kb_per_rank;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&acc_full[a]), 1);
+            mbar_init(smem_u32(&acc_empty[a]), kEpiWarps);
+        }
+        mbar_init(smem_u32(&mma_done), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        for (int r = 0; r < R; ++r) {
+            prefetch_map(&p.tx[r]);
+            prefetch_map(&p.tw[r]);
+        }
+    }
+    if (warp == 1) {
+        // One warp allocates all 512 TMEM columns (one CTA per SM).
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&tmem_base_slot)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_slot;
+
+    if (warp == 0) {
+        // ---------------- producer: TMA loads of X_r and W_r tiles --------
+        if (lane == 0) {
+            int issued_use[kStages];
+            for (int s = 0; s < kStages; ++s) issued_use[s] = -1;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                const int m0 = (tile / p.tiles_n) * kBM;
+                const int n0 = (tile % p.tiles_n) * kBN;
+                for (int r = 0; ok && r < R; ++r) {
+                    for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
+                        const int s = static_cast<int>(it % kStages);
+                        const int use = static_cast<int>(it / kStages);
+                        if (use > 0 && !mbar_wait(smem_u32(&empty_bar[s]), (use - 1) & 1)) {
+                            atomicOr(&g_tp_status, kStatusProducer);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sa = base + static_cast<uint32_t>(s) * kStageBytes;
+                        const uint32_t bar = smem_u32(&full_bar[s]);
+                        mbar_arrive_expect_tx(bar, kStageBytes);
+                        tma_load_2d(sa, &p.tx[r], kb * kBK, m0, bar);
+                        tma_load_2d(sa + kTileA, &p.tw[r], kb * kBK, n0, bar);
+                        issued_use[s] = use;
+                    }
+                }
+            }
+            // Every copy issued lands before the CTA may exit (it writes this
+            // CTA's shared memory).  Issued copies always land.
+            for (int s = 0; s < kStages; ++s)
+                if (issued_use[s] >= 0 &&
+                    !mbar_wait(smem_u32(&full_bar[s]), issued_use[s] & 1))
+                    atomicOr(&g_tp_status, kStatusDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer --------------------------------------
+        if (lane == 0) {
+            uint32_t it = 0, job = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                for (int r = 0; ok && r < R; ++r, ++job) {
+                    const uint32_t acc = job & 1u;
+                    const uint32_t acc_use = job >> 1;
+                    if (acc_use > 0 && !mbar_wait(smem_u32(&acc_empty[acc]), (acc_use - 1) & 1)) {
+                        atomicOr(&g_tp_status, kStatusMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + acc * kAccCols;
+                    for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
+                        const int s = static_cast<int>(it % kStages);
+                        const int use = static_cast<int>(it / kStages);
+                        if (!mbar_wait(smem_u32(&full_bar[s]), use & 1)) {
+                            atomicOr(&g_tp_status, kStatusMma);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = base + static_cast<uint32_t>(s) * kStageBytes;
+                        const uint64_t da = smem_desc_sw128(sa);
+                        const uint64_t db = smem_desc_sw128(sa + kTileA);
+#pragma unroll
+                        for (int j = 0; j < kBK / kUmmaK; ++j) {
+                            // K step j: 16 elements = 32 bytes further along the
+                            // 128-byte swizzled rows (2 in 16-byte units).
+                            mma_bf16(d_tmem, da + 2u * j, db + 2u * j,
+                                     (kb > 0 || j > 0) ? 1u : 0u);
+                        }
+                        mma_commit(smem_u32(&empty_bar[s]));   // stage free once read
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&acc_full[acc]));      // accumulator complete
+                }
+            }
+            // Every MMA issued completes before the TMEM is freed.
+            mma_commit(smem_u32(&mma_done));
+            if (!mbar_wait(smem_u32(&mma_done), 0)) atomicOr(&g_tp_status, kStatusDrain);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: rank-order sum, bf16, R stores ---------
+        const int e = warp - 2;                   // 0..7
+        const int quarter = warp % 4;             // TMEM lanes 32*quarter.. (hardware rule)
+        const int half = e / 4;                   // column half of the tile
+        const int row_in_tile = 32 * quarter + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
+        // Rank-indexed pointers read through the parameter's own address
+        // (a __grid_constant__ parameter is never copied).
+        __nv_bfloat16 *const *outs = p.out;
+        float *const *partials = p.partials;
+        uint32_t job = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            const int m0 = (tile / p.tiles_n) * kBM;
+            const int n0 = (tile % p.tiles_n) * kBN;
+            const size_t row = static_cast<size_t>(m0 + row_in_tile);
+            const int col0 = n0 + half * kColsPerThread;
+            float sum[kColsPerThread];
+            for (int r = 0; r < R; ++r, ++job) {
+                const uint32_t acc = job & 1u;
+                const bool ready = mbar_wait(smem_u32(&acc_full[acc]), (job >> 1) & 1);
+                if (!__all_sync(0xFFFFFFFFu, ready)) {
+                    if (lane == 0) atomicOr(&g_tp_status, kStatusEpilogue);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t t0 = tmem + lane_addr + acc * kAccCols + half * kColsPerThread;
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    float v[16];
+                    tmem_ld16(t0 + 16 * c, v);
+                    if (partials[0] != nullptr) {
+                        float4 *dst = reinterpret_cast<float4 *>(
+                            partials[r] + row * p.n + col0 + 16 * c);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                                 v[4 * q + 3]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        sum[16 * c + i] = (r == 0) ? v[i] : __fadd_rn(sum[16 * c + i], v[i]);
+                }
+                // This warp is done with the accumulator: hand it back.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+            }
+            if (!ok) break;
+            // Round once to bf16 and store the same 16 bytes to every rank's
+            // output (the AllReduce's result on every rank).
+            const size_t off = row * p.n + col0;
+#pragma unroll
+            for (int q = 0; q < kColsPerThread / 8; ++q) {
+                const uint4 pk = make_uint4(pack_bf16x2(sum[8 * q], sum[8 * q + 1]),
+                                            pack_bf16x2(sum[8 * q + 2], sum[8 * q + 3]),
+                                            pack_bf16x2(sum[8 * q + 4], sum[8 * q + 5]),
+                                            pack_bf16x2(sum[8 * q + 6], sum[8 * q + 7]));
+                for (int r = 0; r < R; ++r)
+                    reinterpret_cast<uint4 *>(outs[r] + off)[q] = pk;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and the launch
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static const EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A bf16 row-major matrix of `rows` x `cols` (cols contiguous), read in
+// boxes of 64 columns x box_rows rows with the 128-byte swizzle.
+int encode_bf16_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows,
+                    const char *name, int r) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return fail(CC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr),
+                            dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (res != CUDA_SUCCESS)
+        return fail(CC_ERR_INVALID, "%s[%d]: tensor map rejected (CUresult %d)", name, r,
+                    static_cast<int>(res));
+    return CC_OK;
+}
+
+constexpr int kMaxDevices = 64;
+bool g_attr_set[kMaxDevices];
+std::mutex g_attr_mutex;
+
+}  // namespace
+
+int launch_tp_fused(const void *const *x, const void *const *w, void *const *out,
+                    float *const *partials, int m, int n, int k, int R, int max_ctas,
+                    cudaStream_t stream) {
+    TpFusedParams p{};
+    const int kr = k / R;
+    int st;
+    for (int r = 0; r < R; ++r) {
+        if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM, "x", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, kBN, "w", r)) != CC_OK) return st;
+        p.out[r] = static_cast<__nv_bfloat16 *>(out[r]);
+        p.partials[r] = partials ? partials[r] : nullptr;
+    }
+    p.R = R;
+    p.m = m;
+    p.n = n;
+    p.kb_per_rank = kr / kBK;
+    p.tiles_n = n / kBN;
+    p.num_tiles = (m / kBM) * p.tiles_n;
+
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(CC_ERR_UNSUPPORTED, "device %d beyond the %d supported", dev, kMaxDevices);
+    if ((e = device_sm_count(&sms)) != cudaSuccess) return fail_cuda(e, "SM count");
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mutex);
+        if (!g_attr_set[dev]) {
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(tp_fused_kernel),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return fail_cuda(e, "shared memory attribute");
+            g_attr_set[dev] = true;
+        }
+    }
+    int grid = sms;
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+    if (grid > p.num_tiles) grid = p.num_tiles;
+    if (grid < 1) grid = 1;
+    tp_fused_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused tensor-parallel launch");
+}
+
+int tp_fused_tile_n() { return kBN; }
+int tp_fused_tile_m() { return kBM; }
+int tp_fused_tile_k() { return kBK; }
+
+cudaError_t read_tp_status(unsigned *status, bool clear) {
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_tp_status, sizeof(unsigned));
+    if (e == cudaSuccess && clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_tp_status, &zero, sizeof(unsigned));
+    }
+    return e;
+}
+
+}  // namespace ccdp
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct Span {
+    uintptr_t lo, hi;
+    bool written;
+    const char *name;
+    int index;
+};
+
+}  // namespace
+
+extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w,
+                                      void *const *out, float *const *partials, int m, int n,
+                                      int k, int R, void *stream) {
+    using namespace ccdp;
+    TraceRange call("cc_tp_matmul_allreduce", static_cast<uint64_t>(m));
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    if (m <= 0 || n <= 0 || k <= 0) return fail(CC_ERR_INVALID, "m, n, k must be > 0");
+    if (k % R != 0) return fail(CC_ERR_INVALID, "k=%d is not a multiple of R=%d", k, R);
+    const int kr = k / R;
+    if (m % tp_fused_tile_m() != 0 || n % tp_fused_tile_n() != 0 || kr % tp_fused_tile_k() != 0)
+        return fail(CC_ERR_INVALID,
+                    "shape m=%d n=%d k/R=%d: needs m %% %d == 0, n %% %d == 0, k/R %% %d == 0",
+                    m, n, kr, tp_fused_tile_m(), tp_fused_tile_n(), tp_fused_tile_k());
+    if (!x || !w || !out) return fail(CC_ERR_INVALID, "x/w/out arrays are NULL");
+    const size_t mn = static_cast<size_t>(m) * n;
+    std::vector<Span> spans;
+    auto add = [&](const void *ptr, size_t bytes, bool written, const char *name, int r) {
+        if (!ptr) return fail(CC_ERR_INVALID, "%s[%d] is NULL", name, r);
+        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+            return fail(CC_ERR_MISALIGNED, "%s[%d]=%p is not 16-byte aligned", name, r, ptr);
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+        spans.push_back({lo, lo + bytes, written, name, r});
+        return static_cast<int>(CC_OK);
+    };
+    int st;
+    for (int r = 0; r < R; ++r) {
+        if ((st = add(x[r], 2 * static_cast<size_t>(m) * kr, false, "x", r)) != CC_OK) return st;
+        if ((st = add(w[r], 2 * static_cast<size_t>(n) * kr, false, "w", r)) != CC_OK) return st;
+        if ((st = add(out[r], 2 * mn, true, "out", r)) != CC_OK) return st;
+        if (partials && (st = add(partials[r], 4 * mn, true, "partials", r)) != CC_OK)
+            return st;
+    }
+    for (size_t i = 0; i < spans.size(); ++i)
+        for (size_t j = i + 1; j < spans.size(); ++j)
+            if ((spans[i].written || spans[j].written) && spans[i].lo < spans[j].hi &&
+                spans[j].lo < spans[i].hi)
+                return fail(CC_ERR_ALIAS, "%s[%d] overlaps %s[%d]", spans[i].name,
+                            spans[i].index, spans[j].name, spans[j].index);
+    if ((st = ensure_device()) != CC_OK) return st;
+    for (const Span &sp : spans)
+        if ((st = check_device_range(reinterpret_cast<const void *>(sp.lo), sp.hi - sp.lo,
+                                     sp.name)) != CC_OK)
+            return st;
+    return launch_tp_fused(x, w, out, partials, m, n, k, R, 0,
+                           static_cast<cudaStream_t>(stream));
+}

@@ -440,12 +440,45 @@ typedef struct cc_tp_result {
 CC_API int cc_tp_overlap_bench(const cc_tp_cfg *cfg, cc_tp_result *out);
 
 /*
- * cc_device_status -- the bulk-copy engine's status word on the current
- * device: 0, or an or of codes of pipeline waits that ran out (each wait is
- * bounded to one second, after which the kernel abandons its pipeline and
- * returns instead of hanging): 1 consumer, 2 producer, 4 drain of copies in
- * flight.  A non-zero word means some bulk-engine launch did not finish its
- * range.  Synchronises with the device; clear != 0 resets the word.
+ * cc_tp_matmul_allreduce -- the MatMul of a row-parallel layer and the
+ * AllReduce that follows it, for R emulated tensor-parallel ranks, in one
+ * kernel ("LIT-735 (CoCoNet)", Key takeaways: the model-parallel MatMul and
+ * its AllReduce, which CoCoNet overlaps in chunks; here they are fused so
+ * that no partial product reaches HBM).  Rank r computes Y_r = X_r W_r^T on
+ * the tensor cores (tcgen05, bf16 inputs, fp32 accumulation); every rank's
+ * output is the bf16 rounding (nearest-even, once) of the fp32 sum of the R
+ * partial products in rank order r = 0..R-1 -- exactly cc_tp_allreduce
+ * applied to those partial products.
+ *
+ *   x[R]         bf16, m x k/R each, row-major: rank r's activations.
+ *   w[R]         bf16, n x k/R each, row-major (k/R contiguous: a linear
+ *                layer's weight layout): rank r's weight shard.
+ *   out[R]       bf16, m x n each, row-major, written: every rank's copy of
+ *                the reduced output.
+ *   partials     NULL, or [R] fp32 m x n each, written: each rank's partial
+ *                product as the tensor cores accumulated it (for checking
+ *                the reduction; costs 4R bytes per output element).
+ *   m, n, k, R   k % R == 0; m % 128 == 0, n % 128 == 0 and (k/R) % 64 == 0
+ *                (the kernel's tile), else CC_ERR_INVALID.  R in 1..CC_MAX_R.
+ *   stream       cudaStream_t.
+ * Buffers are device memory, 16-byte aligned; written buffers overlap
+ * nothing.  Allocates nothing.  A pipeline wait that runs out (each is
+ * bounded to two seconds) is reported by cc_device_status (codes 8, 16, 32,
+ * 64) instead of hanging.
+ */
+CC_API int cc_tp_matmul_allreduce(const void *const *x, const void *const *w,
+                                  void *const *out, float *const *partials, int m, int n,
+                                  int k, int R, void *stream);
+
+/*
+ * cc_device_status -- the status word of the library's pipelined kernels on
+ * the current device: 0, or an or of codes of pipeline waits that ran out
+ * (every such wait is bounded, after which the kernel abandons its pipeline
+ * and returns instead of hanging).  Bulk-copy engine (one second per wait):
+ * 1 consumer, 2 producer, 4 drain of copies in flight.  Fused tensor-parallel
+ * kernel (two seconds): 8 producer, 16 MMA, 32 epilogue, 64 drain.  A
+ * non-zero word means some launch did not finish its range.  Synchronises
+ * with the device; clear != 0 resets the word.
  */
 CC_API int cc_device_status(unsigned *status, int clear);
 
@@ -460,6 +493,22 @@ CC_API int cc_device_status(unsigned *status, int clear);
  * that call were enqueued, later ones were not.  -1 disarms.
  */
 CC_API int cc_inject_launch_failure(int after_launches);
+
+/*
+ * cc_inject_bulk_stall -- failure injection on the GPU without a fault, for
+ * testing the bulk-copy engine's bounded waits.  Arms a one-shot for the
+ * calling thread: in the next bulk-engine launch it makes (cc_fused_dp_bucket
+ * with max_ctas > 0, or cc_overlap_bench with a CTA budget), the producer
+ * never issues tile `tile` (tiles of 1024, 512 or 256 elements, counted from
+ * the launch's first element; the CTA tile % grid owns it), and that
+ * launch's pipeline waits give up after timeout_us (1..1000000) instead of
+ * one second.  The consumers waiting for the tile then give up (status code
+ * 1); a producer that comes back to the tile's stage gives up too (code 2);
+ * every copy issued still lands before the CTA exits.  The launch returns
+ * with that CTA's range from the skipped tile on not stepped, and
+ * cc_device_status reports the codes.  tile = -1 disarms.
+ */
+CC_API int cc_inject_bulk_stall(long long tile, unsigned timeout_us);
 
 /*
  * cc_l2_flush -- overwrite `bytes` of the caller's device buffer `buf`

@@ -350,3 +350,13 @@ def test_noalloc_size_refusals_name_their_cause():
     for bb in (2 * cap, 2 * cap + 15):
         r = reason(cap + 1000, bb)
         assert "scratch" not in r, r
+
+
+def test_inject_bulk_stall_arguments():
+    with pytest.raises(capi.CCError):
+        capi.cc_inject_bulk_stall(-2, 100)
+    with pytest.raises(capi.CCError):
+        capi.cc_inject_bulk_stall(0, 0)
+    with pytest.raises(capi.CCError):
+        capi.cc_inject_bulk_stall(0, 2000000)
+    capi.cc_inject_bulk_stall(-1, 0)             # disarm

@@ -1,0 +1,130 @@
+"""The fused tensor-parallel MatMul + AllReduce (tcgen05 GEMM whose epilogue
+sums the R ranks' partial products in rank order and stores the bf16 result
+to every rank), through the C ABI.
+
+Two pins: integer-valued operands make every partial product and every sum
+exact in fp32, so the GEMM itself is checked exactly against a float64
+matmul (any layout, descriptor or indexing slip changes an integer); with
+real-valued operands the kernel also stores the fp32 partial products, the
+outputs must equal the oracle's rank-order AllReduce of exactly those
+partials bit for bit, and the partials must lie within the float64 matmul's
+error bound."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gradient_reduce_optimizer_gb300 import build as gbuild
+from gradient_reduce_optimizer_gb300 import capi
+from gpu_common import DEV, assert_bits, f32, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gbuild.build()
+    capi.lib()
+    capi.cc_device_status(clear=True)
+
+
+def operands(R, m, n, k, seed, integer):
+    kr = k // R
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    if integer:
+        x = [torch.randint(-4, 5, (m, kr), generator=g, device=DEV).to(torch.bfloat16)
+             for _ in range(R)]
+        w = [torch.randint(-4, 5, (n, kr), generator=g, device=DEV).to(torch.bfloat16)
+             for _ in range(R)]
+    else:
+        x = [torch.randn(m, kr, generator=g, device=DEV).to(torch.bfloat16) for _ in range(R)]
+        w = [(torch.randn(n, kr, generator=g, device=DEV) * 0.05).to(torch.bfloat16)
+             for _ in range(R)]
+    return x, w
+
+
+def run(x, w, m, n, k, R, with_partials=True):
+    outs = [torch.full((m, n), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+            for _ in range(R)]
+    parts = ([torch.full((m, n), float("nan"), device=DEV) for _ in range(R)]
+             if with_partials else None)
+    capi.cc_tp_matmul_allreduce(x, w, outs, parts, m, n, k, R)
+    torch.cuda.synchronize()
+    assert capi.cc_device_status() == 0
+    return outs, parts
+
+
+def exact_products(x, w):
+    return [x_.double().cpu().numpy() @ w_.double().cpu().numpy().T for x_, w_ in zip(x, w)]
+
+
+# (R, m, n, k): one tile; several tiles and k-blocks; more tiles than SMs
+# with an odd R (the two accumulators alternate across tiles); the widest R.
+SHAPES = [(1, 128, 128, 64), (2, 256, 256, 256), (3, 2560, 1280, 192),
+          (8, 256, 384, 1024), (16, 128, 256, 1024)]
+
+
+@pytest.mark.parametrize("R,m,n,k", SHAPES)
+def test_integer_operands_are_exact(R, m, n, k):
+    x, w = operands(R, m, n, k, seed=11 + R, integer=True)
+    outs, parts = run(x, w, m, n, k, R)
+    Y = exact_products(x, w)
+    total = sum(Y)
+    for r in range(R):
+        np.testing.assert_array_equal(f32(parts[r]).reshape(m, n), Y[r].astype(np.float32),
+                                      err_msg=f"partial {r}")
+    want = torch.from_numpy(total.astype(np.float32)).to(torch.bfloat16)
+    want16 = want.view(torch.int16).numpy().view(np.uint16).ravel()
+    for r in range(R):
+        assert_bits(f"out[{r}]", u16(outs[r]).ravel(), want16, "bf16")
+
+
+@pytest.mark.parametrize("R,m,n,k", SHAPES)
+def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k):
+    x, w = operands(R, m, n, k, seed=21 + R, integer=False)
+    outs, parts = run(x, w, m, n, k, R)
+    P = [f32(p).ravel().copy() for p in parts]
+    ref = oracle.tp_allreduce(P)
+    for r in range(R):
+        assert_bits(f"out[{r}]", u16(outs[r]).ravel(), ref[r], "bf16")
+    kr = k // R
+    for r, Yr in enumerate(exact_products(x, w)):
+        X = x[r].double().cpu().numpy()
+        W = w[r].double().cpu().numpy()
+        bound = kr * 2.0 ** -23 * (np.abs(X) @ np.abs(W).T) + 1e-30
+        err = np.abs(P[r].reshape(m, n) - Yr)
+        assert np.all(err <= bound), f"partial {r}: max excess {np.max(err - bound)}"
+    # the debug store of the partials changes nothing in the outputs
+    outs2, _ = run(x, w, m, n, k, R, with_partials=False)
+    for r in range(R):
+        assert torch.equal(outs2[r].view(torch.int16), outs[r].view(torch.int16))
+
+
+def test_gpt2_mlp_shape_sampled():
+    """The measured shape (R=8, m=8192, n=3072, k=12288): integer operands,
+    so every output is exact; checked on sampled rows against float64."""
+    R, m, n, k = 8, 8192, 3072, 12288
+    x, w = operands(R, m, n, k, seed=5, integer=True)
+    outs, _ = run(x, w, m, n, k, R, with_partials=False)
+    rows = torch.tensor([0, 1, 127, 128, 4095, 4096, 8191], device=DEV)
+    total = sum(x_[rows].double() @ w_.double().T for x_, w_ in zip(x, w))
+    want = total.float().to(torch.bfloat16).view(torch.int16)
+    for r in range(R):
+        assert torch.equal(outs[r][rows].view(torch.int16), want), f"out[{r}]"
+
+
+def test_rejects_bad_shapes_and_aliases():
+    R, m, n, k = 2, 128, 128, 128
+    x, w = operands(R, m, n, k, seed=3, integer=True)
+    outs = [torch.empty(m, n, dtype=torch.bfloat16, device=DEV) for _ in range(R)]
+    for bad in ((m + 8, n, k), (m, n + 16, k), (m, n, k + 2), (m, n, 96)):
+        with pytest.raises(capi.CCError) as ei:
+            capi.cc_tp_matmul_allreduce(x, w, outs, None, *bad, R)
+        assert ei.value.status == capi.CC_ERR_INVALID
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_tp_matmul_allreduce(x, w, [outs[0], outs[0]], None, m, n, k, R)
+    assert ei.value.status == capi.CC_ERR_ALIAS
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_tp_matmul_allreduce(x, w, [outs[0], x[1]], None, m, n, k, R)
+    assert ei.value.status == capi.CC_ERR_ALIAS

@@ -84,10 +84,12 @@ def test_noalloc_refuses_buckets_beyond_its_scratch():
                                         R, 0, step=1, **HP)
     assert ei.value.status == capi.CC_ERR_INVALID
     assert "scratch" in ei.value.reason and "n=" in ei.value.reason
-    # the same refusal when bucket_bytes sets the size: 16 bytes past the edge
-    big = torch.empty(too_many, dtype=torch.float32, device=DEV)
+    # the same refusal when bucket_bytes sets the size (16 bytes past the
+    # edge, on a slab longer than one bucket)
+    longer = capi.CC_NOALLOC_SCRATCH_ELEMS + 1000
+    big = torch.empty(longer, dtype=torch.float32, device=DEV)
     with pytest.raises(capi.CCError) as ei:
-        capi.cc_unfused_dp_step_noalloc([big] * R, big, big, big, [big] * R, too_many, R,
+        capi.cc_unfused_dp_step_noalloc([big] * R, big, big, big, [big] * R, longer, R,
                                         2 * capi.CC_NOALLOC_SCRATCH_ELEMS + 16,
                                         step=1, **HP)
     assert ei.value.status == capi.CC_ERR_INVALID
