@@ -106,6 +106,9 @@ _SIGNATURES = {
     "cc_unfused_dp_step_noalloc": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _f, _f,
                                     _f, _f, _f, _i, _f, _vp], _i),
     "cc_tp_allreduce": ([_vp, _vp, _sz, _i, _vp], _i),
+    "cc_shard_plan": ([_vp, _vp, _i, _i, _vp, _vp, _vp, _vp], _i),
+    "cc_fused_dp_rank_step": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _f, _f, _f, _f, _f,
+                               _i, _f, _vp], _i),
     "cc_tp_matmul_allreduce": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "cc_inject_bulk_stall": ([ctypes.c_longlong, ctypes.c_uint], _i),
     "cc_inject_launch_failure": ([_i], _i),
@@ -351,6 +354,33 @@ def cc_tp_overlap_bench(*, R: int, m: int, n: int, k: int, chunks: int, x, w,
     _check(lib().cc_tp_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
            "cc_tp_overlap_bench")
     return {name: getattr(res, name) for name, _ in res._fields_}
+
+
+def cc_shard_plan(buckets: Sequence[Tuple[int, int]], world: int):
+    """Shards of every bucket for `world` ranks: (shards, state_offsets,
+    state_elems) with shards[b][q] = (begin, end) and state_offsets[b][q]
+    the shard's place in rank q's state arrays."""
+    B = len(buckets)
+    bb = (_sz * max(1, B))(*[b for b, _ in buckets])
+    be = (_sz * max(1, B))(*[e for _, e in buckets])
+    sb = (_sz * max(1, B * world))()
+    se = (_sz * max(1, B * world))()
+    so = (_sz * max(1, B * world))()
+    elems = (_sz * world)()
+    _check(lib().cc_shard_plan(bb, be, B, world, sb, se, so, elems), "cc_shard_plan")
+    shards = [[(sb[b * world + q], se[b * world + q]) for q in range(world)] for b in range(B)]
+    offsets = [[so[b * world + q] for q in range(world)] for b in range(B)]
+    return shards, offsets, list(elems)
+
+
+def cc_fused_dp_rank_step(grad_slices, master, m, v, param_out, length: int, R: int, *,
+                          lr: float, beta1: float, beta2: float, eps: float,
+                          weight_decay: float, step: int, grad_scale: float,
+                          stream=None) -> None:
+    _check(lib().cc_fused_dp_rank_step(
+        _addr_array(grad_slices), _addr(master), _addr(m), _addr(v), _addr(param_out),
+        length, R, lr, beta1, beta2, eps, weight_decay, step, grad_scale, _stream(stream)),
+        "cc_fused_dp_rank_step")
 
 
 def cc_tp_matmul_allreduce(x, w, out, partials, m: int, n: int, k: int, R: int,

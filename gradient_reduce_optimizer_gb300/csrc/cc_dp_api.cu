@@ -402,6 +402,97 @@ int cc_fused_dp_shard(const void *const *grads, const float *const *acc,
                                   beta2, eps, weight_decay, step, grad_scale, 1, stream);
 }
 
+int cc_shard_plan(const size_t *bucket_begin, const size_t *bucket_end, int num_buckets,
+                  int world, size_t *shard_begin_out, size_t *shard_end_out,
+                  size_t *state_offset_out, size_t *state_elems_out) {
+    if (num_buckets < 0 || world < 1)
+        return fail(CC_ERR_INVALID, "num_buckets=%d, world=%d", num_buckets, world);
+    if (!state_elems_out || (num_buckets > 0 && (!bucket_begin || !bucket_end ||
+                                                 !shard_begin_out || !shard_end_out ||
+                                                 !state_offset_out)))
+        return fail(CC_ERR_INVALID, "NULL array");
+    for (int b = 0; b < num_buckets; ++b) {
+        if (bucket_end[b] < bucket_begin[b] || (b > 0 && bucket_begin[b] < bucket_end[b - 1]))
+            return fail(CC_ERR_INVALID, "bucket %d range is reversed or out of order", b);
+        if (bucket_begin[b] % CC_PAD_ELEMS != 0)
+            return fail(CC_ERR_MISALIGNED, "bucket %d begins at %zu, not a multiple of %d", b,
+                        bucket_begin[b], CC_PAD_ELEMS);
+    }
+    for (int q = 0; q < world; ++q) state_elems_out[q] = 0;
+    for (int b = 0; b < num_buckets; ++b) {
+        // Cut the bucket in 8-element units: shard q holds units
+        // [floor(u q / W), floor(u (q+1) / W)); the last shard also takes a
+        // ragged tail.  Sizes differ by at most 8 elements (plus the tail).
+        const size_t lo = bucket_begin[b], hi = bucket_end[b];
+        const size_t units = (hi - lo) / CC_PAD_ELEMS;
+        for (int q = 0; q < world; ++q) {
+            const size_t i = static_cast<size_t>(b) * world + q;
+            const size_t a = lo + CC_PAD_ELEMS * (units * q / world);
+            const size_t e = q + 1 < world ? lo + CC_PAD_ELEMS * (units * (q + 1) / world) : hi;
+            shard_begin_out[i] = a;
+            shard_end_out[i] = e;
+            state_offset_out[i] = state_elems_out[q];
+            state_elems_out[q] += e - a;
+        }
+    }
+    return CC_OK;
+}
+
+int cc_fused_dp_rank_step(const void *const *grad_slices, float *master, float *m, float *v,
+                          void *param_out, size_t len, int R, float lr, float beta1,
+                          float beta2, float eps, float weight_decay, int step,
+                          float grad_scale, void *stream) {
+    TraceRange call("cc_fused_dp_rank_step", len);
+    if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
+    AdamScalars c;
+    int st = make_scalars(lr, beta1, beta2, eps, weight_decay, step, grad_scale, &c);
+    if (st != CC_OK) return st;
+    if (len == 0) return CC_OK;
+    if (!grad_slices) return fail(CC_ERR_INVALID, "grad_slices array is NULL");
+    if (!param_out) return fail(CC_ERR_INVALID, "param_out is NULL");
+    if (!master || !m || !v) return fail(CC_ERR_INVALID, "master/m/v is NULL");
+    if (len > (SIZE_MAX / 8)) return fail(CC_ERR_INVALID, "len=%zu too large", len);
+    std::vector<Range> ranges;
+    auto add = [&](const void *p, size_t bytes, bool written, const char *name, int idx,
+                   bool host_ok) -> int {
+        if (!p) return fail(CC_ERR_INVALID, "%s[%d] is NULL", name, idx);
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+            return fail(CC_ERR_MISALIGNED, "%s[%d]=%p is not 16-byte aligned", name, idx, p);
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+        ranges.push_back({lo, lo + bytes, written, name, idx, host_ok});
+        return CC_OK;
+    };
+    for (int r = 0; r < R; ++r)
+        if ((st = add(grad_slices[r], 2 * len, false, "grad_slices", r, true)) != CC_OK) return st;
+    if ((st = add(param_out, 2 * len, true, "param_out", 0, true)) != CC_OK) return st;
+    if ((st = add(master, 4 * len, true, "master", 0, false)) != CC_OK) return st;
+    if ((st = add(m, 4 * len, true, "m", 0, false)) != CC_OK) return st;
+    if ((st = add(v, 4 * len, true, "v", 0, false)) != CC_OK) return st;
+    for (size_t i = 0; i < ranges.size(); ++i)
+        for (size_t j = i + 1; j < ranges.size(); ++j)
+            if ((ranges[i].written || ranges[j].written) && overlap(ranges[i], ranges[j]))
+                return fail(CC_ERR_ALIAS, "%s[%d] overlaps %s[%d]", ranges[i].name,
+                            ranges[i].index, ranges[j].name, ranges[j].index);
+    if ((st = ensure_device()) != CC_OK) return st;
+    for (const Range &r : ranges)
+        if ((st = check_slab_range(reinterpret_cast<const void *>(r.lo), r.hi - r.lo, r.name,
+                                   r.host_ok)) != CC_OK)
+            return st;
+    Slabs s;
+    s.R = R;
+    for (int r = 0; r < CC_MAX_R; ++r) {
+        s.grads[r] = r < R ? grad_slices[r] : nullptr;
+        s.acc[r] = nullptr;
+        s.out[r] = r == 0 ? param_out : nullptr;
+    }
+    s.master = master;
+    s.m = m;
+    s.v = v;
+    s.one_out = true;
+    const cudaError_t e = launch_fused(s, c, 0, len, 0, false, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CC_OK : fail_cuda(e, "rank step launch");
+}
+
 int cc_accumulate_local(const void *const *grads, float *const *acc, size_t n,
                         int R, int first, void *stream) {
     TraceRange call(first ? "cc_accumulate_local(first)" : "cc_accumulate_local", n);

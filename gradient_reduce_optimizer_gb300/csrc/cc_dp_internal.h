@@ -30,6 +30,8 @@ struct Slabs {
     const float *acc[CC_MAX_R];    // fp32[n] or null
     void *out[CC_MAX_R];           // bf16[n]
     float *master, *m, *v;         // fp32[n]
+    bool one_out = false;          // parameters to out[0] only (the multi-GPU
+                                   // rank step; plain kernel, no accumulators)
 };
 
 // Enqueue the fused reduce + AdamW + redistribute kernel over elements

@@ -88,7 +88,10 @@ struct FusedParams {
     int tail_len;                  // 0..7 elements after the full vectors
 };
 
-template <int R, bool ACC>
+// ONE_OUT: the parameters go to out[0] only (one rank's own slab in the
+// multi-GPU form, from where the AllGather distributes them); otherwise to
+// all R replica slabs.
+template <int R, bool ACC, bool ONE_OUT>
 __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     // Issue every load of this vector before any arithmetic.
     uint4 gq[R];
@@ -148,7 +151,7 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     o.z = pack_bf16x2(pw[4], pw[5]);
     o.w = pack_bf16x2(pw[6], pw[7]);
 #pragma unroll
-    for (int r = 0; r < R; ++r) __stcs(p.out[r] + vi, o);
+    for (int r = 0; r < (ONE_OUT ? 1 : R); ++r) __stcs(p.out[r] + vi, o);
 }
 
 // Half vectors: one thread owns 4 consecutive elements.  A warp's fp32
@@ -160,7 +163,7 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
 // reducing step with accumulators it also halves the registers that the
 // loads in flight take (R = 8: 480 bytes for a full vector, 142 registers
 // and one 256-thread block per SM).
-template <int R, bool ACC>
+template <int R, bool ACC, bool ONE_OUT>
 __device__ __forceinline__ void fused_half(const FusedParams &p, size_t hv) {
     uint2 gq[R];
     float4 aq[ACC ? R : 1];
@@ -214,7 +217,8 @@ __device__ __forceinline__ void fused_half(const FusedParams &p, size_t hv) {
     __stcs(p.v + hv, make_float4(vv[0], vv[1], vv[2], vv[3]));
     const uint2 o = make_uint2(pack_bf16x2(pw[0], pw[1]), pack_bf16x2(pw[2], pw[3]));
 #pragma unroll
-    for (int r = 0; r < R; ++r) __stcs(reinterpret_cast<uint2 *>(p.out[r]) + hv, o);
+    for (int r = 0; r < (ONE_OUT ? 1 : R); ++r)
+        __stcs(reinterpret_cast<uint2 *>(p.out[r]) + hv, o);
 }
 
 // Threads per 8-element vector of the fused kernel.
@@ -224,7 +228,7 @@ __host__ __device__ constexpr int threads_per_vector() {
 }
 
 // One element of the partial last vector (scalar accesses).
-template <int R, bool ACC>
+template <int R, bool ACC, bool ONE_OUT>
 __device__ __forceinline__ void fused_scalar(const FusedParams &p, size_t i) {
     float s = bf16_at(p.g[0], i);
     if constexpr (ACC) s = __fadd_rn(reinterpret_cast<const float *>(p.acc[0])[i], s);
@@ -246,7 +250,7 @@ __device__ __forceinline__ void fused_scalar(const FusedParams &p, size_t i) {
     vv[i] = v;
     const __nv_bfloat16 b = __float2bfloat16_rn(pw);
 #pragma unroll
-    for (int r = 0; r < R; ++r) reinterpret_cast<__nv_bfloat16 *>(p.out[r])[i] = b;
+    for (int r = 0; r < (ONE_OUT ? 1 : R); ++r) reinterpret_cast<__nv_bfloat16 *>(p.out[r])[i] = b;
 }
 
 // Programmatic dependent launch (sm_90+).  Without a programmatic
@@ -258,7 +262,7 @@ __device__ __forceinline__ void wait_for_predecessor_grid() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int R, bool ACC>
+template <int R, bool ACC, bool ONE_OUT>
 __global__ void __launch_bounds__(kThreads, CC_DP_MIN_BLOCKS)
 fused_step_kernel(const __grid_constant__ FusedParams p) {
     allow_dependents_to_launch();
@@ -266,13 +270,13 @@ fused_step_kernel(const __grid_constant__ FusedParams p) {
     const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     if constexpr (threads_per_vector<ACC>() == 2) {
         for (size_t i = first; i < 2 * p.num_vec; i += stride)
-            fused_half<R, ACC>(p, 2 * p.vec_begin + i);
+            fused_half<R, ACC, ONE_OUT>(p, 2 * p.vec_begin + i);
     } else {
         for (size_t i = first; i < p.num_vec; i += stride)
-            fused_vector<R, ACC>(p, p.vec_begin + i);
+            fused_vector<R, ACC, ONE_OUT>(p, p.vec_begin + i);
     }
     if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len)
-        fused_scalar<R, ACC>(p, p.tail_begin + threadIdx.x);
+        fused_scalar<R, ACC, ONE_OUT>(p, p.tail_begin + threadIdx.x);
     wait_for_predecessor_grid();
 }
 
@@ -389,29 +393,32 @@ l2_flush_kernel(uint4 *buf, size_t num_vec, uint32_t salt) {
 
 using FusedKernel = void (*)(FusedParams);
 
+// The one-output form exists without accumulators only (the multi-GPU
+// rank step); with them it is null.
 template <int R>
-FusedKernel pick_fused(bool acc) {
-    return acc ? fused_step_kernel<R, true> : fused_step_kernel<R, false>;
+FusedKernel pick_fused(bool acc, bool one_out) {
+    if (one_out) return acc ? nullptr : fused_step_kernel<R, false, true>;
+    return acc ? fused_step_kernel<R, true, false> : fused_step_kernel<R, false, false>;
 }
 
-FusedKernel fused_kernel_for(int R, bool acc) {
+FusedKernel fused_kernel_for(int R, bool acc, bool one_out = false) {
     switch (R) {
-        case 1: return pick_fused<1>(acc);
-        case 2: return pick_fused<2>(acc);
-        case 3: return pick_fused<3>(acc);
-        case 4: return pick_fused<4>(acc);
-        case 5: return pick_fused<5>(acc);
-        case 6: return pick_fused<6>(acc);
-        case 7: return pick_fused<7>(acc);
-        case 8: return pick_fused<8>(acc);
-        case 9: return pick_fused<9>(acc);
-        case 10: return pick_fused<10>(acc);
-        case 11: return pick_fused<11>(acc);
-        case 12: return pick_fused<12>(acc);
-        case 13: return pick_fused<13>(acc);
-        case 14: return pick_fused<14>(acc);
-        case 15: return pick_fused<15>(acc);
-        case 16: return pick_fused<16>(acc);
+        case 1: return pick_fused<1>(acc, one_out);
+        case 2: return pick_fused<2>(acc, one_out);
+        case 3: return pick_fused<3>(acc, one_out);
+        case 4: return pick_fused<4>(acc, one_out);
+        case 5: return pick_fused<5>(acc, one_out);
+        case 6: return pick_fused<6>(acc, one_out);
+        case 7: return pick_fused<7>(acc, one_out);
+        case 8: return pick_fused<8>(acc, one_out);
+        case 9: return pick_fused<9>(acc, one_out);
+        case 10: return pick_fused<10>(acc, one_out);
+        case 11: return pick_fused<11>(acc, one_out);
+        case 12: return pick_fused<12>(acc, one_out);
+        case 13: return pick_fused<13>(acc, one_out);
+        case 14: return pick_fused<14>(acc, one_out);
+        case 15: return pick_fused<15>(acc, one_out);
+        case 16: return pick_fused<16>(acc, one_out);
         default: return nullptr;
     }
 }
@@ -484,6 +491,8 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     cudaError_t e = device_info(&d);
     if (e != cudaSuccess) return e;
     const bool acc = s.acc[0] != nullptr;
+    FusedKernel kern = fused_kernel_for(s.R, acc, s.one_out);
+    if (!kern) return cudaErrorInvalidValue;
     FusedParams p{};
     for (int r = 0; r < s.R; ++r) {
         p.g[r] = static_cast<const uint4 *>(s.grads[r]);
@@ -519,7 +528,7 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (chain && CC_DP_PDL) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, fused_kernel_for(s.R, acc), p);
+    return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 using AccumKernel = void (*)(AccumParams);

@@ -217,6 +217,61 @@ CC_API int cc_fused_dp_shard(const void *const *grads, const float *const *acc,
                       void *stream);
 
 /*
+ * cc_shard_plan -- the shards of the real multi-GPU form of the step, one
+ * ReduceScatter-AdamW-AllGather per bucket ("LIT-735 (CoCoNet)", Key
+ * takeaways: the fused ReduceScatter-optimizer-AllGather, which shards the
+ * optimizer state; "Communication Overlap": one collective per DDP bucket).
+ * Each planned bucket is cut into `world` shards in rank order; rank q
+ * reduces, updates and gathers shard q of every bucket, and owns the
+ * optimizer state of those shards only, packed in launch order.  Host only.
+ *
+ *   bucket_begin/end[num_buckets]  element ranges in launch order (from
+ *                  cc_plan_buckets: each begins on a multiple of CC_PAD_ELEMS,
+ *                  else CC_ERR_MISALIGNED), non-decreasing.
+ *   world          ranks, >= 1.
+ *   shard_begin_out, shard_end_out [num_buckets * world]: shard q of bucket
+ *                  b at index b * world + q.  The bucket is cut in units of
+ *                  CC_PAD_ELEMS elements: shard q holds units
+ *                  [floor(u q / world), floor(u (q + 1) / world)) of its u
+ *                  units (the last shard also any ragged tail), so every shard
+ *                  begins 16-byte aligned and sizes differ by at most 8.
+ *   state_offset_out [num_buckets * world]: where shard q of bucket b starts
+ *                  in rank q's master/m/v arrays.
+ *   state_elems_out [world]: elements of master/m/v rank q owns.
+ */
+CC_API int cc_shard_plan(const size_t *bucket_begin, const size_t *bucket_end,
+                         int num_buckets, int world, size_t *shard_begin_out,
+                         size_t *shard_end_out, size_t *state_offset_out,
+                         size_t *state_elems_out);
+
+/*
+ * cc_fused_dp_rank_step -- one rank's compute in the real multi-GPU form,
+ * between the two exchanges of one bucket ("LIT-735 (CoCoNet)", Key
+ * takeaways: the optimizer fused between the ReduceScatter and the
+ * AllGather).  After the ReduceScatter exchange the rank holds every
+ * replica's bf16 gradient of its shard; this call sums them in replica
+ * (rank) order in fp32, takes the AdamW step on the rank's own state of
+ * the shard, and writes the bf16 parameters of the shard once, into the
+ * rank's own parameter slab, from where the AllGather exchange sends them
+ * to every rank.  Values are exactly those of cc_fused_dp_step on the same
+ * elements.
+ *
+ *   grad_slices[R]  bf16[len] each, read: replica r's gradient of the shard,
+ *                   r = 0..R-1 (R = world size; the rank's own slice may point
+ *                   into its own gradient slab).  May alias each other.
+ *   master, m, v    fp32[len], read and written: the rank's state of the shard.
+ *   param_out       bf16[len], written: the shard's parameters.
+ *   len             elements of the shard (0 is a no-op).
+ *   the rest        as cc_fused_dp_step.  One kernel launch; allocates nothing.
+ *   Gradient slices and param_out may be page-locked host memory, as replica
+ *   slabs may elsewhere; the state must be device memory.
+ */
+CC_API int cc_fused_dp_rank_step(const void *const *grad_slices, float *master, float *m,
+                                 float *v, void *param_out, size_t len, int R, float lr,
+                                 float beta1, float beta2, float eps, float weight_decay,
+                                 int step, float grad_scale, void *stream);
+
+/*
  * cc_unfused_dp_step -- the same step as cc_fused_dp_step (bit-identical
  * results) in the unfused schedule a framework runs when the collective and
  * the optimizer are separate library calls, kept for comparison ("LIT-735

@@ -14,6 +14,8 @@ Contents
   passages it follows.
 * ``plan_buckets`` / ``bucket_ready_layers``: the bucket planner and the
   readiness rule in plain Python loops.
+* ``shard_plan``: the shards of every bucket in the sharded (multi-GPU)
+  form.
 
 Sources: "Communication Optimization › Communication Overlap"
 (mbrenndoerfer.com), the paragraphs on reverse-order readiness, on DDP
@@ -44,6 +46,7 @@ __all__ = [
     "accumulate_local",
     "plan_buckets",
     "bucket_ready_layers",
+    "shard_plan",
     "tp_allreduce",
     "MAX_R",
 ]
@@ -215,6 +218,41 @@ def plan_buckets(numel: Sequence[int], bucket_bytes: int):
     if cursor > open_begin:
         buckets.append((open_begin, cursor))
     return offsets, buckets, cursor
+
+
+def shard_plan(buckets, world: int):
+    """Who owns what in the sharded form of the step: every bucket is cut
+    into ``world`` shards in rank order, rank q reducing, updating and
+    gathering shard q ("LIT-735" (CoCoNet), Key takeaways: ReduceScatter,
+    the optimizer on each rank's shard, AllGather; one collective per DDP
+    bucket).  Cut in 8-element units (16 bytes of bf16): of a bucket's u
+    whole units, rank q holds units floor(u q / W) .. floor(u (q + 1) / W)
+    - 1 (an even split, sizes differing by at most one unit); the last rank
+    also takes any ragged tail.  Rank q's optimizer state holds its shards
+    of every bucket one after the other, in launch order.
+
+    Returns ``(shards, state_offsets, state_elems)``: ``shards[b][q] =
+    (begin, end)``, ``state_offsets[b][q]`` where that shard starts in rank
+    q's state, ``state_elems[q]`` the length of rank q's state.
+    """
+    shards, offsets = [], []
+    used = [0] * world
+    for begin, end in buckets:
+        units = (end - begin) // PAD_ELEMS
+        row, offs = [], []
+        for q in range(world):
+            first_unit = (units * q) // world
+            stop_unit = (units * (q + 1)) // world
+            lo = begin + PAD_ELEMS * first_unit
+            hi = begin + PAD_ELEMS * stop_unit
+            if q == world - 1:
+                hi = end                     # the ragged tail, if any
+            row.append((lo, hi))
+            offs.append(used[q])
+            used[q] += hi - lo
+        shards.append(row)
+        offsets.append(offs)
+    return shards, offsets, used
 
 
 def bucket_ready_layers(numel: Sequence[int], layer_of: Sequence[int],

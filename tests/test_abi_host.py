@@ -360,3 +360,58 @@ def test_inject_bulk_stall_arguments():
     with pytest.raises(capi.CCError):
         capi.cc_inject_bulk_stall(0, 2000000)
     capi.cc_inject_bulk_stall(-1, 0)             # disarm
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("mib", [1, 25, 500])
+def test_shard_plan_matches_oracle(world, mib):
+    w = wl.bert_large_r8()
+    _, buckets, _ = capi.cc_plan_buckets(w.numel(), mib << 20)
+    assert capi.cc_shard_plan(buckets, world) == tuple(oracle.shard_plan(buckets, world))
+
+
+def test_shard_plan_random_and_ragged_match_oracle():
+    rng = random.Random(17)
+    for _ in range(60):
+        numel = [rng.choice([1, 7, 8, 9, 64, 1000, 4099]) for _ in range(rng.randint(1, 12))]
+        _, buckets, n = capi.cc_plan_buckets(numel, rng.choice([0, 16, 64, 4096]))
+        if rng.random() < 0.5:              # a ragged last bucket, as a uniform cut makes
+            b, e = buckets[-1]
+            buckets[-1] = (b, e - rng.randint(0, 7))
+        world = rng.randint(1, 9)
+        assert capi.cc_shard_plan(buckets, world) == tuple(oracle.shard_plan(buckets, world))
+
+
+def test_shard_plan_rejects_bad_input():
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_shard_plan([(0, 16)], 0)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_shard_plan([(4, 16)], 2)
+    assert ei.value.status == capi.CC_ERR_MISALIGNED
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_shard_plan([(16, 32), (0, 8)], 2)
+    assert ei.value.status == capi.CC_ERR_INVALID
+
+
+def test_rank_step_validation():
+    g, acc, p, m, v, o = fake_slabs(3, 1000)
+    def status(**kw):
+        args = dict(grad_slices=g, master=p, m=m, v=v, param_out=o[0], length=1000, R=3)
+        args.update(kw)
+        try:
+            capi.cc_fused_dp_rank_step(args.pop("grad_slices"), args.pop("master"),
+                                       args.pop("m"), args.pop("v"), args.pop("param_out"),
+                                       args.pop("length"), args.pop("R"), stream=0, **ADAM)
+            return capi.CC_OK
+        except capi.CCError as err:
+            return err.status
+    assert status(R=0) == capi.CC_ERR_INVALID
+    assert status(R=17) == capi.CC_ERR_INVALID
+    assert status(length=0) == capi.CC_OK                      # no-op, pointers unexamined
+    assert status(param_out=o[0] + 2) == capi.CC_ERR_MISALIGNED
+    assert status(param_out=g[1]) == capi.CC_ERR_ALIAS         # writes over a gradient slice
+    assert status(m=p) == capi.CC_ERR_ALIAS
+    assert status(grad_slices=[g[0], g[0], g[0]]) in (capi.CC_ERR_UNSUPPORTED,
+                                                      capi.CC_ERR_INVALID)   # aliasing reads ok
+    assert status() in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID)

@@ -100,3 +100,68 @@ def test_bert_large_25mib_last_bucket_holds_word_embedding():
 def test_gpt2_slice_sizes():
     t = wl.gpt2_slice_tensors()
     assert len(t) == 288 and sum(x[1] for x in t) == 2_718_867_456
+
+
+# ---------------------------------------------------------------------------
+# The shard plan of the sharded (multi-GPU) form
+# ---------------------------------------------------------------------------
+
+# Worked by hand: a bucket of u whole 8-element units gives rank q units
+# floor(u q / W) .. floor(u (q + 1) / W) - 1; the last rank also takes a
+# ragged tail; each rank's state holds its shards back to back.
+SHARD_CASES = [
+    # 5 units over 2 ranks: 2 and 3 units
+    ([(0, 40)], 2, [[(0, 16), (16, 40)]], [[0, 0]], [16, 24]),
+    # 5 units over 3 ranks: 1, 2, 2 units
+    ([(0, 40)], 3, [[(0, 8), (8, 24), (24, 40)]], [[0, 0, 0]], [8, 16, 16]),
+    # a one-unit bucket leaves rank 0 empty; a ragged last bucket:
+    # 119 units + 3 elements over 2 ranks: 59 units, then 60 units + 3
+    ([(0, 40), (40, 48), (48, 1003)], 2,
+     [[(0, 16), (16, 40)], [(40, 40), (40, 48)], [(48, 520), (520, 1003)]],
+     [[0, 0], [16, 24], [16, 32]], [488, 515]),
+    # one unit over three ranks: only the last rank holds anything
+    ([(0, 8)], 3, [[(0, 0), (0, 0), (0, 8)]], [[0, 0, 0]], [0, 0, 8]),
+    # only a tail (5 elements) over two ranks
+    ([(0, 5)], 2, [[(0, 0), (0, 5)]], [[0, 0]], [0, 5]),
+]
+
+
+@pytest.mark.parametrize("buckets,world,shards,offsets,elems", SHARD_CASES)
+def test_shard_plan_hand_worked(buckets, world, shards, offsets, elems):
+    assert oracle.shard_plan(buckets, world) == (shards, offsets, elems)
+
+
+def check_shard_invariants(buckets, world):
+    shards, offsets, elems = oracle.shard_plan(buckets, world)
+    used = [0] * world
+    for (b, e), row, offs in zip(buckets, shards, offsets):
+        # the shards tile the bucket in rank order, each 16-byte aligned
+        assert row[0][0] == b and row[-1][1] == e
+        for (lo, hi), (lo2, _) in zip(row, row[1:]):
+            assert hi == lo2
+        assert all(lo % 8 == 0 and hi >= lo for lo, hi in row)
+        whole = [(hi - lo) // 8 for lo, hi in row]
+        assert max(whole) - min(whole) <= 1          # balanced to one unit
+        for q, (lo, hi) in enumerate(row):
+            assert offs[q] == used[q]
+            used[q] += hi - lo
+    assert elems == used
+    assert sum(elems) == sum(e - b for b, e in buckets)
+    if world == 1:
+        assert shards == [[bk] for bk in buckets]
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("mib", [1, 25, 500])
+def test_shard_plan_invariants_bert_large(world, mib):
+    w = wl.bert_large_r8()
+    _, buckets, _ = oracle.plan_buckets(w.numel(), mib << 20)
+    check_shard_invariants(buckets, world)
+
+
+def test_shard_plan_invariants_random():
+    rng = random.Random(13)
+    for _ in range(40):
+        numel = [rng.choice([1, 7, 8, 9, 64, 1000, 4099]) for _ in range(rng.randint(1, 12))]
+        _, buckets, _ = oracle.plan_buckets(numel, rng.choice([0, 16, 64, 4096]))
+        check_shard_invariants(buckets, rng.randint(1, 9))

@@ -40,6 +40,17 @@ MUTATIONS = {
     "open bucket's bytes not reset":
         ("            open_begin = cursor\n            open_bytes = 0",
          "            open_begin = cursor"),
+    "shard ends rounded up instead of down":
+        ("            stop_unit = (units * (q + 1)) // world",
+         "            stop_unit = -((-units * (q + 1)) // world)"),
+    "shard begins one unit late":
+        ("            first_unit = (units * q) // world",
+         "            first_unit = (units * q + world - 1) // world"),
+    "ragged tail of a bucket dropped":
+        ("            if q == world - 1:\n                hi = end",
+         "            if q == world - 1:\n                hi = hi"),
+    "shard state offsets not accumulated":
+        ("            used[q] += hi - lo", "            used[q] = hi - lo"),
 }
 
 
