@@ -25,10 +25,10 @@ C ABI.  Printed as one JSON line (rank 0):
              split over every host core
 
 `--impl reference` times the oracle alone on the host cores (the reference
-arm).  Under torchrun (N > 1) every rank runs its own independent step on
-its own GPU (replicas only: the emulated R-replica step has no exchange
-between GPUs); the JSON reports the total over ranks against the slowest
-rank's time.
+arm).  Under torchrun (N > 1) the ranks run the real multi-GPU form with
+R = N (one replica per GPU, the optimizer state sharded, per bucket a
+ReduceScatter over NCCL, the fused rank step, an AllGather); the JSON
+reports the parameters stepped per second against the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -509,6 +509,98 @@ def headline_config(args, R, world, n_params, n_slab, bucket_bytes):
     }
 
 
+def run_dist(args):
+    """The real multi-GPU form under torchrun: R = world size ranks, one
+    replica per GPU.  Each rank holds its replica's gradient and parameter
+    slabs of the BERT-large list and the optimizer state of its shards only;
+    per bucket (25 MiB, reverse layer order) a ReduceScatter of the bf16
+    gradients over NCCL into local staging, the library's rank step, and an
+    AllGather of the bf16 parameters.  Units: parameters stepped per second
+    (each of the n parameters once per step), over the slowest rank."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import build as gbuild
+    from gradient_reduce_optimizer_gb300 import capi
+    from gradient_reduce_optimizer_gb300 import workloads as wl
+    from gradient_reduce_optimizer_gb300.dist import ShardedStep
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    if local == 0:
+        gbuild.build()
+    barrier(world)
+    capi.lib()
+    w = wl.bert_large_r8(bucket_bytes=args.bucket_mib * wl.MiB)
+    numel, layer_of = w.numel(), w.layer_of()
+    step = ShardedStep(numel, w.bucket_bytes, rank=rank, world=world, device=dev)
+    n_slab = step.n_slab
+    lay = wl.element_layer_map(numel, layer_of, step.offsets, n_slab, device=dev)
+    per_layer = wl.layer_scales(max(layer_of) + 1, *w.layer_scale, device=dev)
+    scale = per_layer[lay.clamp(min=0).long()]
+    # replica `rank`'s gradient: the emulated workload's seed for replica r
+    g = wl._randn(n_slab, wl.SEED_GRAD + rank, dev).mul_(w.grad_sigma).mul_(scale)
+    g.masked_fill_(lay < 0, 0.0)
+    grads = g.to(torch.bfloat16)
+    del g, lay, scale
+    master, m, v = wl.make_state(n_slab, w.step, w.grad_sigma, master_sigma=w.master_sigma,
+                                 device=dev)
+    # this rank's shards of the state, packed in launch order
+    st = [torch.empty(step.state_elems, device=dev) for _ in range(3)]
+    for (lo, hi), (a, b) in step.shard_state_ranges():
+        for dst, src in zip(st, (master, m, v)):
+            dst[a:b] = src[lo:hi]
+    del master, m, v
+    params = torch.empty(n_slab, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def one(i):
+        step.step(grads, *st, params, stream=stream, **step_args({"w": w}, w.step + i))
+
+    for i in range(args.warmup):
+        one(i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        one(args.warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms_local = e0.elapsed_time(e1) / args.steps
+    # every rank steps its shards: the units of all ranks add up to n
+    mine = sum(b - a for _, (a, b) in step.shard_state_ranges())
+    ms, value = aggregate(ms_local, float(mine) * w.n / n_slab, world, device=dev)
+    result = {
+        "metric": METRIC, "value": round(value), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": (f"BERT-large parameter list (336,226,108 params, 398 tensors), "
+                         f"R={world} real ranks (one replica per GPU), {args.bucket_mib} MiB "
+                         "buckets in reverse layer order: per bucket a ReduceScatter of "
+                         "bf16 gradients (NCCL send/recv), the fused AdamW rank step, an "
+                         "AllGather of bf16 parameters"),
+            "R": world, "n_params": w.n, "n_slab": n_slab, "bucket_bytes": w.bucket_bytes,
+            "num_buckets": len(step.buckets), "state_elems_per_rank": step.state_elems,
+            "parallelism": f"dp{world}, optimizer state sharded",
+            "l2": "inputs larger than the 129 MB L2: no flush"},
+        "clocks": clk,
+        "gpu_launches": len(step.buckets) * args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return result
+
+
 def run_ours(args):
     import torch
     from gradient_reduce_optimizer_gb300 import build as gbuild
@@ -529,7 +621,7 @@ def run_ours(args):
         wk = build_small_workload(dev, args.small)
         args.no_e2e = args.no_overlap = args.no_cpu_baseline = True
         args.no_unfused = args.no_tp = args.no_launch_floor = True
-        args.no_gpt2_slice = args.no_accum = True
+        args.no_gpt2_slice = args.no_accum = args.no_bulk_rates = True
     else:
         wk = build_workload(dev, bucket_mib=args.bucket_mib)
     w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
@@ -565,10 +657,12 @@ def run_ours(args):
         elif args.engine_ctas > 0:
             # the bulk-copy engine on a budget of SMs, bucket by bucket
             for b, e in cuts:
-                capi.cc_fused_dp_bucket(wk["grads"], None, wk["master"], wk["m"],
-                                        wk["v"], wk["outs"], n_slab, R, b, e,
-                                        max_ctas=args.engine_ctas, stream=stream,
-                                        **step_args(wk, step))
+                capi.cc_fused_dp_bucket_ex(wk["grads"], None, wk["master"], wk["m"],
+                                           wk["v"], wk["outs"], n_slab, R, b, e,
+                                           max_ctas=args.engine_ctas,
+                                           arith_flags=(capi.CC_ARITH_FAST if args.fast_arith
+                                                        else 0),
+                                           stream=stream, **step_args(wk, step))
         else:
             capi.cc_fused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"],
                                   wk["outs"], n_slab, R, bb, stream=stream,
@@ -639,6 +733,8 @@ def run_ours(args):
 
     if not args.no_unfused and not args.small:
         result["unfused"] = run_unfused(args, wk, stream, ms)
+    if not args.small and not args.no_bulk_rates:
+        result["bulk_engine_per_sm"] = run_bulk_rates(args, wk, stream)
     if not args.no_tp and not args.small:
         result["tp_matmul_allreduce"] = run_tp(args, dev)
     if not args.no_launch_floor and not args.small:
@@ -671,6 +767,12 @@ def run_ours(args):
                 sweep["rank_share" if share else "all_replicas"] = [
                     {k: r[k] for k in OVERLAP_KEEP} for r in rows]
             result["overlap_sweep"] = sweep
+        # the rank share with the opt-in fast arithmetic: fewer instructions
+        # per element, so the reduction takes less SM time beside the GEMMs
+        result["overlap_rank_share_fast"] = [
+            {k: r[k] for k in OVERLAP_KEEP + ("mode",)}
+            for r in run_overlap(args, wk, dev, [25, 100], rank_share=True,
+                                 arith_flags=capi.CC_ARITH_FAST)]
         if not args.no_accum:
             # the reducing k-th step of accumulation (k = 4) behind the same
             # backward: accumulators that stand for three earlier micro-steps
@@ -905,6 +1007,44 @@ def run_tp_fused(args, dev, x, w, outs, R, m, n, k, sequential_ms=None, reps=20)
     return out
 
 
+def run_bulk_rates(args, wk, stream, elems=1 << 25, ctas_list=(16, 32, 64, 96), reps=5):
+    """What one SM streams through the bulk-copy engine (the engine a CTA
+    budget selects), exact and fast arithmetic: the first 2^25 slab elements
+    of the headline workload stepped on 16..96 persistent CTAs.  GB/s of the
+    step's (4R + 24) algorithmic bytes per parameter, in total and per SM."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    w, n_slab, R = wk["w"], wk["n_slab"], wk["w"].R
+    elems = min(elems, n_slab) // 8 * 8
+    bpp = 4 * R + 24
+    rows = []
+    for ctas in ctas_list:
+        row = {"ctas": ctas}
+        for name, flags in (("exact", 0), ("fast", capi.CC_ARITH_FAST)):
+            def one(i):
+                capi.cc_fused_dp_bucket_ex(wk["grads"], None, wk["master"], wk["m"], wk["v"],
+                                           wk["outs"], n_slab, R, 0, elems, max_ctas=ctas,
+                                           arith_flags=flags, stream=stream,
+                                           **step_args(wk, w.step + i))
+            one(0)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(reps):
+                one(1 + i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            gbs = bpp * elems / (ms * 1e-3) / 1e9
+            row[name] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                         "gbs_per_sm": round(gbs / ctas, 1)}
+        rows.append(row)
+    assert capi.cc_device_status(clear=True) == 0
+    return {"elements": elems, "bytes_per_param": bpp, "rows": rows}
+
+
 def run_accumulation(args, wk, stream, k=4):
     """Gradient accumulation with k micro-steps on the same workload: k-1
     local micro-steps (first: acc = g, 6R bytes per parameter; later:
@@ -1083,19 +1223,8 @@ def run_e2e_staged(args, wk, stream, world, dev, host_grads, host_out):
             "ms_per_step": round(ms, 3), "steps": steps}
 
 
-def shard_range(begin, end, count, index):
-    """Shard `index` of `count` of the bucket [begin, end), cut in 8-element
-    units (sizes differ by at most 8 elements): the part of a bucket one
-    rank reduces and updates in the sharded (ReduceScatter-optimizer-
-    AllGather) form of the step."""
-    units = (end - begin) // 8
-    lo = begin + 8 * (units * index // count)
-    hi = begin + 8 * (units * (index + 1) // count) if index + 1 < count else end
-    return lo, hi
-
-
 def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0, acc=None,
-                num_layers=24):
+                num_layers=24, arith_flags=0):
     """Exposed time of the bucketed step behind a proxy backward of
     num_layers x 3 bf16 GEMMs (M=8192, N=K=1024); buckets planned at each
     size.
@@ -1126,7 +1255,8 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0, acc=None,
         assert n_slab == wk["n_slab"] and offsets == wk["offsets"]
         ready = capi.cc_bucket_ready_layers(wk["numel"], wk["layer_of"], offsets, buckets)
         if rank_share:
-            pairs = [(shard_range(b, e, w.R, 0), rl) for (b, e), rl in zip(buckets, ready)]
+            shards, _, _ = capi.cc_shard_plan(buckets, w.R)     # rank 0's shard of each
+            pairs = [(row[0], rl) for row, rl in zip(shards, ready)]
             pairs = [(br, rl) for br, rl in pairs if br[1] > br[0]]
             buckets, ready = [br for br, _ in pairs], [rl for _, rl in pairs]
         r = capi.cc_overlap_bench(
@@ -1137,12 +1267,13 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0, acc=None,
             warmup=args.warmup, iters=args.overlap_iters,
             max_ctas=args.overlap_ctas, stream_priority=args.stream_priority,
             comm_sms=comm_sms, gemm_algo=args.overlap_gemm_algo,
-            budget_buckets=args.overlap_budget_buckets, acc=acc,
+            budget_buckets=args.overlap_budget_buckets, acc=acc, arith_flags=arith_flags,
             **step_args(wk, w.step))
         r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
         r["bucket_mib"] = mib
         r["mode"] = (("rank share (1/R of each bucket)" if rank_share else "all R replicas")
-                     + (", reducing step with fp32 accumulators" if acc is not None else ""))
+                     + (", reducing step with fp32 accumulators" if acc is not None else "")
+                     + (", fast arithmetic" if arith_flags else ""))
         r["exposed_pct_of_bwd"] = round(100 * r["exposed_ms"] / r["t_bwd_ms"], 1)
         r["bwd_tflops"] = round(num_layers * 3 * 2 * M * N * K / (r["t_bwd_ms"] * 1e-3) / 1e12,
                                 1)
@@ -1244,6 +1375,9 @@ def parse_args(argv=None):
                    help="with --small: time the unfused schedule (reduce, AdamW, copies)")
     p.add_argument("--micro", choices=("first", "later"), default=None,
                    help="with --small: time one local micro-step (acc = g, or acc += g)")
+    p.add_argument("--dist", action="store_true",
+                   help="the real multi-GPU form (one replica per rank, NCCL exchanges); "
+                        "the default under torchrun with more than one rank")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--tp-only", type=int, default=0,
                    help="profile case: only the tensor-parallel path, with this many rows")
@@ -1255,6 +1389,10 @@ def parse_args(argv=None):
                    help="skip the small L2-resident case (single launches, CUDA graph)")
     p.add_argument("--no-accum", action="store_true",
                    help="skip timing gradient accumulation (k=4)")
+    p.add_argument("--no-bulk-rates", action="store_true",
+                   help="skip the bulk engine's per-SM rates (exact and fast arithmetic)")
+    p.add_argument("--fast-arith", action="store_true",
+                   help="with --small --engine-ctas: the opt-in fast arithmetic")
     p.add_argument("--no-unfused", action="store_true",
                    help="skip timing the unfused (reduce, AdamW, copies) schedule")
     p.add_argument("--e2e-steps", type=int, default=20)
@@ -1296,8 +1434,11 @@ def main(argv=None):
                                                         m=args.tp_only, chunk_list=(1, 4))}),
               flush=True)
         return
+    _, world, _ = dist_env()
     if args.impl == "reference":
         run_reference(args)
+    elif world > 1 or args.dist:
+        run_dist(args)
     else:
         run_ours(args)
     _, world, _ = dist_env()

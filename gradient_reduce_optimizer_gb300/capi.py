@@ -22,6 +22,7 @@ LIBRARY = os.path.join(PKG, "libcc_dp.so")
 CC_MAX_R = 16
 CC_PAD_ELEMS = 8
 CC_NOALLOC_SCRATCH_ELEMS = 16 * 1024 * 1024   # fixed scratch of the allocation-free entry point
+CC_ARITH_FAST = 1                             # opt-in fast arithmetic of the bucket kernels
 CC_OK = 0
 CC_ERR_INVALID = -1
 CC_ERR_ALIAS = -2
@@ -57,7 +58,7 @@ class cc_overlap_cfg(ctypes.Structure):
         ("gemm_a", _vp), ("gemm_b", _vp), ("gemm_c", _vp),
         ("warmup", _i), ("iters", _i), ("max_ctas", _i),
         ("stream_priority", _i), ("comm_sms", _i), ("budget_buckets", _i),
-        ("gemm_algo", _i),
+        ("gemm_algo", _i), ("arith_flags", ctypes.c_uint),
     ]
 
 
@@ -106,6 +107,8 @@ _SIGNATURES = {
     "cc_unfused_dp_step_noalloc": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _f, _f,
                                     _f, _f, _f, _i, _f, _vp], _i),
     "cc_tp_allreduce": ([_vp, _vp, _sz, _i, _vp], _i),
+    "cc_fused_dp_bucket_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _sz, _sz,
+                               _f, _f, _f, _f, _f, _i, _f, _i, ctypes.c_uint, _vp], _i),
     "cc_shard_plan": ([_vp, _vp, _i, _i, _vp, _vp, _vp, _vp], _i),
     "cc_fused_dp_rank_step": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _f, _f, _f, _f, _f,
                                _i, _f, _vp], _i),
@@ -211,6 +214,18 @@ def cc_fused_dp_bucket(grads, acc, master, m, v, params_out, n: int, R: int,
         "cc_fused_dp_bucket")
 
 
+def cc_fused_dp_bucket_ex(grads, acc, master, m, v, params_out, n: int, R: int,
+                          begin: int, end: int, lr: float, beta1: float,
+                          beta2: float, eps: float, weight_decay: float,
+                          step: int, grad_scale: float, max_ctas: int = 0,
+                          arith_flags: int = 0, stream=None) -> None:
+    _check(lib().cc_fused_dp_bucket_ex(
+        _addr_array(grads), _addr_array(acc), _addr(master), _addr(m),
+        _addr(v), _addr_array(params_out), n, R, begin, end, lr, beta1, beta2,
+        eps, weight_decay, step, grad_scale, max_ctas, arith_flags, _stream(stream)),
+        "cc_fused_dp_bucket_ex")
+
+
 def cc_fused_dp_shard(grads, acc, master, m, v, params_out, n: int, R: int,
                       shard_begin: int, shard_end: int, bucket_bytes: int,
                       lr: float, beta1: float, beta2: float, eps: float,
@@ -300,7 +315,7 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
                      gemm_c, warmup: int = 3, iters: int = 20,
                      max_ctas: int = 0, stream_priority: int = 0, comm_sms: int = 0,
                      budget_buckets: int = 0, gemm_algo: int = 0,
-                     acc=None) -> Dict[str, float]:
+                     acc=None, arith_flags: int = 0) -> Dict[str, float]:
     B = len(buckets)
     keep = dict(
         g=_addr_array(grads), o=_addr_array(params_out),
@@ -322,7 +337,7 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
         gemm_k=gemm_k, gemm_a=_addr(gemm_a), gemm_b=_addr(gemm_b),
         gemm_c=_addr(gemm_c), warmup=warmup, iters=iters, max_ctas=max_ctas,
         stream_priority=stream_priority, comm_sms=comm_sms,
-        budget_buckets=budget_buckets, gemm_algo=gemm_algo)
+        budget_buckets=budget_buckets, gemm_algo=gemm_algo, arith_flags=arith_flags)
     res = cc_overlap_result()
     _check(lib().cc_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
            "cc_overlap_bench")

@@ -176,6 +176,8 @@ int make_scalars(float lr, float beta1, float beta2, float eps,
         return fail(CC_ERR_INVALID, "bias correction underflows (beta too close to 1)");
     if (!finite(c->inv_scale))
         return fail(CC_ERR_INVALID, "1/grad_scale overflows (grad_scale=%g)", grad_scale);
+    c->inv_bias_corr1 = 1.0f / c->bias_corr1;
+    c->inv_bias_corr2 = 1.0f / c->bias_corr2;
     return CC_OK;
 }
 
@@ -344,7 +346,21 @@ int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
                        size_t end, float lr, float beta1, float beta2,
                        float eps, float weight_decay, int step,
                        float grad_scale, int max_ctas, void *stream) {
+    return cc_fused_dp_bucket_ex(grads, acc, master, m, v, params_out, n, R, begin, end, lr,
+                                 beta1, beta2, eps, weight_decay, step, grad_scale, max_ctas,
+                                 0u, stream);
+}
+
+int cc_fused_dp_bucket_ex(const void *const *grads, const float *const *acc,
+                          float *master, float *m, float *v,
+                          void *const *params_out, size_t n, int R, size_t begin,
+                          size_t end, float lr, float beta1, float beta2,
+                          float eps, float weight_decay, int step,
+                          float grad_scale, int max_ctas, unsigned arith_flags,
+                          void *stream) {
     TraceRange call("cc_fused_dp_bucket", begin);
+    if (arith_flags & ~CC_ARITH_FAST)
+        return fail(CC_ERR_INVALID, "arith_flags=%#x has unknown bits", arith_flags);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     if (begin > end || end > n)
         return fail(CC_ERR_INVALID, "range [%zu, %zu) not inside [0, %zu)", begin, end, n);
@@ -358,6 +374,7 @@ int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
     Slabs s;
     st = validate_slabs(grads, acc, master, m, v, params_out, n, R, acc != nullptr, &s);
     if (st != CC_OK) return st;
+    s.fast = (arith_flags & CC_ARITH_FAST) != 0;
     const cudaError_t e =
         launch_step_range(s, c, begin, end, max_ctas, false, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused bucket launch");

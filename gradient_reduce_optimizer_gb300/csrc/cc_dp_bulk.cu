@@ -157,7 +157,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 // Four consecutive elements of one tile: operands from shared memory,
 // results straight to global memory (element e = tile start + j).
-template <int R, bool ACC>
+template <int R, bool ACC, bool FAST>
 __device__ __forceinline__ void consume4(const unsigned char *st, const StageLayout &L,
                                          int T, int j, size_t e, const BulkParams &p) {
     uint2 gq[R];
@@ -189,10 +189,10 @@ __device__ __forceinline__ void consume4(const unsigned char *st, const StageLay
     float4 p4 = *reinterpret_cast<const float4 *>(st + L.master + 4u * j);
     float4 m4 = *reinterpret_cast<const float4 *>(st + L.m + 4u * j);
     float4 v4 = *reinterpret_cast<const float4 *>(st + L.v + 4u * j);
-    adamw(s[0], p4.x, m4.x, v4.x, p.c);
-    adamw(s[1], p4.y, m4.y, v4.y, p.c);
-    adamw(s[2], p4.z, m4.z, v4.z, p.c);
-    adamw(s[3], p4.w, m4.w, v4.w, p.c);
+    adamw_step<FAST>(s[0], p4.x, m4.x, v4.x, p.c);
+    adamw_step<FAST>(s[1], p4.y, m4.y, v4.y, p.c);
+    adamw_step<FAST>(s[2], p4.z, m4.z, v4.z, p.c);
+    adamw_step<FAST>(s[3], p4.w, m4.w, v4.w, p.c);
     __stcs(reinterpret_cast<float4 *>(p.master + e), p4);
     __stcs(reinterpret_cast<float4 *>(p.m + e), m4);
     __stcs(reinterpret_cast<float4 *>(p.v + e), v4);
@@ -202,7 +202,7 @@ __device__ __forceinline__ void consume4(const unsigned char *st, const StageLay
 }
 
 // One element after the tiled range, straight from global memory.
-template <int R, bool ACC>
+template <int R, bool ACC, bool FAST>
 __device__ void tail_element(const BulkParams &p, size_t i) {
     float s = bf16_at(p.g[0], i);
     if constexpr (ACC) s = __fadd_rn(p.acc[0][i], s);
@@ -215,7 +215,7 @@ __device__ void tail_element(const BulkParams &p, size_t i) {
             s = __fadd_rn(s, t);
     }
     float pw = p.master[i], m = p.m[i], v = p.v[i];
-    adamw(s, pw, m, v, p.c);
+    adamw_step<FAST>(s, pw, m, v, p.c);
     p.master[i] = pw;
     p.m[i] = m;
     p.v[i] = v;
@@ -224,7 +224,7 @@ __device__ void tail_element(const BulkParams &p, size_t i) {
     for (int r = 0; r < R; ++r) reinterpret_cast<__nv_bfloat16 *>(p.out[r])[i] = b;
 }
 
-template <int R, bool ACC>
+template <int R, bool ACC, bool FAST>
 __global__ void __launch_bounds__(kBulkThreads, 1)
 fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -319,39 +319,40 @@ fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
         const unsigned char *st = smem + static_cast<size_t>(s) * L.bytes;
         const size_t e0 = p.begin + t * static_cast<size_t>(T);
         for (int jj = j; jj < len; jj += 4 * kConsumers)
-            consume4<R, ACC>(st, L, T, jj, e0 + jj, p);
+            consume4<R, ACC, FAST>(st, L, T, jj, e0 + jj, p);
         __syncwarp();
         if ((ct & 31) == 0) mbar_arrive(smem_addr(&empty_bar[s]));
     }
     if (blockIdx.x == gridDim.x - 1 && ct < p.tail_len)
-        tail_element<R, ACC>(p, p.tail_begin + ct);
+        tail_element<R, ACC, FAST>(p, p.tail_begin + ct);
 }
 
 using BulkKernel = void (*)(BulkParams);
 
 template <int R>
-BulkKernel pick_bulk(bool acc) {
-    return acc ? fused_step_bulk_kernel<R, true> : fused_step_bulk_kernel<R, false>;
+BulkKernel pick_bulk(bool acc, bool fast) {
+    if (fast) return acc ? fused_step_bulk_kernel<R, true, true> : fused_step_bulk_kernel<R, false, true>;
+    return acc ? fused_step_bulk_kernel<R, true, false> : fused_step_bulk_kernel<R, false, false>;
 }
 
-BulkKernel bulk_kernel_for(int R, bool acc) {
+BulkKernel bulk_kernel_for(int R, bool acc, bool fast) {
     switch (R) {
-        case 1: return pick_bulk<1>(acc);
-        case 2: return pick_bulk<2>(acc);
-        case 3: return pick_bulk<3>(acc);
-        case 4: return pick_bulk<4>(acc);
-        case 5: return pick_bulk<5>(acc);
-        case 6: return pick_bulk<6>(acc);
-        case 7: return pick_bulk<7>(acc);
-        case 8: return pick_bulk<8>(acc);
-        case 9: return pick_bulk<9>(acc);
-        case 10: return pick_bulk<10>(acc);
-        case 11: return pick_bulk<11>(acc);
-        case 12: return pick_bulk<12>(acc);
-        case 13: return pick_bulk<13>(acc);
-        case 14: return pick_bulk<14>(acc);
-        case 15: return pick_bulk<15>(acc);
-        case 16: return pick_bulk<16>(acc);
+        case 1: return pick_bulk<1>(acc, fast);
+        case 2: return pick_bulk<2>(acc, fast);
+        case 3: return pick_bulk<3>(acc, fast);
+        case 4: return pick_bulk<4>(acc, fast);
+        case 5: return pick_bulk<5>(acc, fast);
+        case 6: return pick_bulk<6>(acc, fast);
+        case 7: return pick_bulk<7>(acc, fast);
+        case 8: return pick_bulk<8>(acc, fast);
+        case 9: return pick_bulk<9>(acc, fast);
+        case 10: return pick_bulk<10>(acc, fast);
+        case 11: return pick_bulk<11>(acc, fast);
+        case 12: return pick_bulk<12>(acc, fast);
+        case 13: return pick_bulk<13>(acc, fast);
+        case 14: return pick_bulk<14>(acc, fast);
+        case 15: return pick_bulk<15>(acc, fast);
+        case 16: return pick_bulk<16>(acc, fast);
         default: return nullptr;
     }
 }
@@ -370,7 +371,7 @@ void choose_tiling(int R, bool acc, int *tile, int *stages) {
 }
 
 constexpr int kMaxDevices = 64;
-bool g_smem_attr_set[kMaxDevices][CC_MAX_R + 1][2];
+bool g_smem_attr_set[kMaxDevices][CC_MAX_R + 1][2][2];
 std::mutex g_smem_attr_mutex;
 
 // One-shot failure injection of the next bulk-engine launch on this thread
@@ -396,17 +397,18 @@ cudaError_t launch_fused_bulk(const Slabs &s, const AdamScalars &c, size_t begin
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if ((e = device_sm_count(&sms)) != cudaSuccess) return e;
     const bool acc = s.acc[0] != nullptr;
-    BulkKernel kern = bulk_kernel_for(s.R, acc);
+    if (s.one_out) return cudaErrorInvalidValue;   // the bulk engine writes all R slabs
+    BulkKernel kern = bulk_kernel_for(s.R, acc, s.fast);
     int T = 0, S = 0;
     choose_tiling(s.R, acc, &T, &S);
     const unsigned smem = static_cast<unsigned>(S) * stage_layout(s.R, acc, T).bytes;
     {
         std::lock_guard<std::mutex> lock(g_smem_attr_mutex);
-        if (!g_smem_attr_set[dev][s.R][acc ? 1 : 0]) {
+        if (!g_smem_attr_set[dev][s.R][acc ? 1 : 0][s.fast ? 1 : 0]) {
             e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kern),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
             if (e != cudaSuccess) return e;
-            g_smem_attr_set[dev][s.R][acc ? 1 : 0] = true;
+            g_smem_attr_set[dev][s.R][acc ? 1 : 0][s.fast ? 1 : 0] = true;
         }
     }
     BulkParams p{};

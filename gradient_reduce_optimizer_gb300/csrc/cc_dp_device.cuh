@@ -88,5 +88,37 @@ __device__ __forceinline__ void adamw(float s, float &p, float &m, float &v,
     v = v_new;
 }
 
+// The opt-in fast form of the same step (CC_ARITH_FAST): m and v exactly as
+// above; the two bias-correction divisions become multiplications by
+// reciprocals rounded once on the host, the square root stays IEEE, and the
+// quotient m^/(sqrt(v^) + eps) is CUDA's fast division __fdividef (2 ulp
+// for normal denominators; eps > 0 keeps the denominator normal).  The
+// parameter then differs from the correctly rounded step by a few ulp of the
+// update, the bf16 copy by at most one bf16 ulp.
+__device__ __forceinline__ void adamw_fast(float s, float &p, float &m, float &v,
+                                           const AdamScalars &c) {
+    const float g = __fmul_rn(s, c.inv_scale);
+    const float m_new = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.one_minus_b1, g));
+    const float v_new = __fadd_rn(__fmul_rn(c.beta2, v),
+                                  __fmul_rn(c.one_minus_b2, __fmul_rn(g, g)));
+    const float m_hat = __fmul_rn(m_new, c.inv_bias_corr1);
+    const float v_hat = __fmul_rn(v_new, c.inv_bias_corr2);
+    const float denom = __fadd_rn(__fsqrt_rn(v_hat), c.eps);
+    const float update = __fmul_rn(c.lr, __fdividef(m_hat, denom));
+    p = __fsub_rn(__fmul_rn(p, c.decay), update);
+    m = m_new;
+    v = v_new;
+}
+
+// The step in the arithmetic the kernel was instantiated for.
+template <bool FAST>
+__device__ __forceinline__ void adamw_step(float s, float &p, float &m, float &v,
+                                           const AdamScalars &c) {
+    if constexpr (FAST)
+        adamw_fast(s, p, m, v, c);
+    else
+        adamw(s, p, m, v, c);
+}
+
 }  // namespace dev
 }  // namespace ccdp

@@ -20,6 +20,7 @@ struct AdamScalars {
     float lr, eps;
     float decay;      // 1 - lr*wd  (decoupled weight decay factor)
     float inv_scale;  // 1 / grad_scale
+    float inv_bias_corr1, inv_bias_corr2;   // 1 / bias_corrX (fast arithmetic only)
 };
 
 // The slabs of one step.  Pointers are whole-slab bases; kernels index them
@@ -32,6 +33,7 @@ struct Slabs {
     float *master, *m, *v;         // fp32[n]
     bool one_out = false;          // parameters to out[0] only (the multi-GPU
                                    // rank step; plain kernel, no accumulators)
+    bool fast = false;             // the opt-in fast arithmetic (CC_ARITH_FAST)
 };
 
 // Enqueue the fused reduce + AdamW + redistribute kernel over elements
@@ -84,9 +86,9 @@ cudaError_t read_bulk_status(unsigned *status, bool clear);
 int launch_tp_fused(const void *const *x, const void *const *w, void *const *out,
                     float *const *partials, int m, int n, int k, int R, int max_ctas,
                     cudaStream_t stream);
-int tp_fused_tile_m();
-int tp_fused_tile_n();
-int tp_fused_tile_k();
+// Whether the fused kernel tiles m x n with k/R per rank: m % 128 == 0,
+// (k/R) % 64 == 0, and n a multiple of 128 or 192.
+bool tp_fused_shape_ok(int m, int n, int kr);
 
 // Read (and optionally clear) the fused tensor-parallel kernel's status word:
 // 0, or codes of waits that ran out (8 producer, 16 MMA, 32 epilogue, 64

@@ -91,7 +91,7 @@ struct FusedParams {
 // ONE_OUT: the parameters go to out[0] only (one rank's own slab in the
 // multi-GPU form, from where the AllGather distributes them); otherwise to
 // all R replica slabs.
-template <int R, bool ACC, bool ONE_OUT>
+template <int R, bool ACC, bool ONE_OUT, bool FAST>
 __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     // Issue every load of this vector before any arithmetic.
     uint4 gq[R];
@@ -137,7 +137,7 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
     float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) adamw(s[k], pw[k], mm[k], vv[k], p.c);
+    for (int k = 0; k < 8; ++k) adamw_step<FAST>(s[k], pw[k], mm[k], vv[k], p.c);
 
     __stcs(p.master + 2 * vi, make_float4(pw[0], pw[1], pw[2], pw[3]));
     __stcs(p.master + 2 * vi + 1, make_float4(pw[4], pw[5], pw[6], pw[7]));
@@ -163,7 +163,7 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
 // reducing step with accumulators it also halves the registers that the
 // loads in flight take (R = 8: 480 bytes for a full vector, 142 registers
 // and one 256-thread block per SM).
-template <int R, bool ACC, bool ONE_OUT>
+template <int R, bool ACC, bool ONE_OUT, bool FAST>
 __device__ __forceinline__ void fused_half(const FusedParams &p, size_t hv) {
     uint2 gq[R];
     float4 aq[ACC ? R : 1];
@@ -210,7 +210,7 @@ __device__ __forceinline__ void fused_half(const FusedParams &p, size_t hv) {
     float mm[4] = {m.x, m.y, m.z, m.w};
     float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) adamw(s[k], pw[k], mm[k], vv[k], p.c);
+    for (int k = 0; k < 4; ++k) adamw_step<FAST>(s[k], pw[k], mm[k], vv[k], p.c);
 
     __stcs(p.master + hv, make_float4(pw[0], pw[1], pw[2], pw[3]));
     __stcs(p.m + hv, make_float4(mm[0], mm[1], mm[2], mm[3]));
@@ -228,7 +228,7 @@ __host__ __device__ constexpr int threads_per_vector() {
 }
 
 // One element of the partial last vector (scalar accesses).
-template <int R, bool ACC, bool ONE_OUT>
+template <int R, bool ACC, bool ONE_OUT, bool FAST>
 __device__ __forceinline__ void fused_scalar(const FusedParams &p, size_t i) {
     float s = bf16_at(p.g[0], i);
     if constexpr (ACC) s = __fadd_rn(reinterpret_cast<const float *>(p.acc[0])[i], s);
@@ -244,7 +244,7 @@ __device__ __forceinline__ void fused_scalar(const FusedParams &p, size_t i) {
     float *mm = reinterpret_cast<float *>(p.m);
     float *vv = reinterpret_cast<float *>(p.v);
     float pw = pm[i], m = mm[i], v = vv[i];
-    adamw(s, pw, m, v, p.c);
+    adamw_step<FAST>(s, pw, m, v, p.c);
     pm[i] = pw;
     mm[i] = m;
     vv[i] = v;
@@ -262,7 +262,7 @@ __device__ __forceinline__ void wait_for_predecessor_grid() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int R, bool ACC, bool ONE_OUT>
+template <int R, bool ACC, bool ONE_OUT, bool FAST>
 __global__ void __launch_bounds__(kThreads, CC_DP_MIN_BLOCKS)
 fused_step_kernel(const __grid_constant__ FusedParams p) {
     allow_dependents_to_launch();
@@ -270,13 +270,13 @@ fused_step_kernel(const __grid_constant__ FusedParams p) {
     const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     if constexpr (threads_per_vector<ACC>() == 2) {
         for (size_t i = first; i < 2 * p.num_vec; i += stride)
-            fused_half<R, ACC, ONE_OUT>(p, 2 * p.vec_begin + i);
+            fused_half<R, ACC, ONE_OUT, FAST>(p, 2 * p.vec_begin + i);
     } else {
         for (size_t i = first; i < p.num_vec; i += stride)
-            fused_vector<R, ACC, ONE_OUT>(p, p.vec_begin + i);
+            fused_vector<R, ACC, ONE_OUT, FAST>(p, p.vec_begin + i);
     }
     if (blockIdx.x == gridDim.x - 1 && static_cast<int>(threadIdx.x) < p.tail_len)
-        fused_scalar<R, ACC, ONE_OUT>(p, p.tail_begin + threadIdx.x);
+        fused_scalar<R, ACC, ONE_OUT, FAST>(p, p.tail_begin + threadIdx.x);
     wait_for_predecessor_grid();
 }
 
@@ -393,32 +393,37 @@ l2_flush_kernel(uint4 *buf, size_t num_vec, uint32_t salt) {
 
 using FusedKernel = void (*)(FusedParams);
 
-// The one-output form exists without accumulators only (the multi-GPU
-// rank step); with them it is null.
+// The one-output form exists without accumulators and in the exact
+// arithmetic only (the multi-GPU rank step); other combinations with it are
+// null.
 template <int R>
-FusedKernel pick_fused(bool acc, bool one_out) {
-    if (one_out) return acc ? nullptr : fused_step_kernel<R, false, true>;
-    return acc ? fused_step_kernel<R, true, false> : fused_step_kernel<R, false, false>;
+FusedKernel pick_fused(bool acc, bool one_out, bool fast) {
+    if (one_out) return (acc || fast) ? nullptr : fused_step_kernel<R, false, true, false>;
+    if (fast)
+        return acc ? fused_step_kernel<R, true, false, true>
+                   : fused_step_kernel<R, false, false, true>;
+    return acc ? fused_step_kernel<R, true, false, false>
+               : fused_step_kernel<R, false, false, false>;
 }
 
-FusedKernel fused_kernel_for(int R, bool acc, bool one_out = false) {
+FusedKernel fused_kernel_for(int R, bool acc, bool one_out = false, bool fast = false) {
     switch (R) {
-        case 1: return pick_fused<1>(acc, one_out);
-        case 2: return pick_fused<2>(acc, one_out);
-        case 3: return pick_fused<3>(acc, one_out);
-        case 4: return pick_fused<4>(acc, one_out);
-        case 5: return pick_fused<5>(acc, one_out);
-        case 6: return pick_fused<6>(acc, one_out);
-        case 7: return pick_fused<7>(acc, one_out);
-        case 8: return pick_fused<8>(acc, one_out);
-        case 9: return pick_fused<9>(acc, one_out);
-        case 10: return pick_fused<10>(acc, one_out);
-        case 11: return pick_fused<11>(acc, one_out);
-        case 12: return pick_fused<12>(acc, one_out);
-        case 13: return pick_fused<13>(acc, one_out);
-        case 14: return pick_fused<14>(acc, one_out);
-        case 15: return pick_fused<15>(acc, one_out);
-        case 16: return pick_fused<16>(acc, one_out);
+        case 1: return pick_fused<1>(acc, one_out, fast);
+        case 2: return pick_fused<2>(acc, one_out, fast);
+        case 3: return pick_fused<3>(acc, one_out, fast);
+        case 4: return pick_fused<4>(acc, one_out, fast);
+        case 5: return pick_fused<5>(acc, one_out, fast);
+        case 6: return pick_fused<6>(acc, one_out, fast);
+        case 7: return pick_fused<7>(acc, one_out, fast);
+        case 8: return pick_fused<8>(acc, one_out, fast);
+        case 9: return pick_fused<9>(acc, one_out, fast);
+        case 10: return pick_fused<10>(acc, one_out, fast);
+        case 11: return pick_fused<11>(acc, one_out, fast);
+        case 12: return pick_fused<12>(acc, one_out, fast);
+        case 13: return pick_fused<13>(acc, one_out, fast);
+        case 14: return pick_fused<14>(acc, one_out, fast);
+        case 15: return pick_fused<15>(acc, one_out, fast);
+        case 16: return pick_fused<16>(acc, one_out, fast);
         default: return nullptr;
     }
 }
@@ -491,7 +496,7 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     cudaError_t e = device_info(&d);
     if (e != cudaSuccess) return e;
     const bool acc = s.acc[0] != nullptr;
-    FusedKernel kern = fused_kernel_for(s.R, acc, s.one_out);
+    FusedKernel kern = fused_kernel_for(s.R, acc, s.one_out, s.fast);
     if (!kern) return cudaErrorInvalidValue;
     FusedParams p{};
     for (int r = 0; r < s.R; ++r) {

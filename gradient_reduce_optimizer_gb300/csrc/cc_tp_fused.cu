@@ -23,12 +23,19 @@
 //     accumulate) from those stages into one of two TMEM accumulators: rank
 //     r of the CTA's j-th job goes to accumulator (j*R + r) % 2, so the next
 //     rank's MMAs run while the epilogue drains the previous one;
-//   * eight epilogue warps read each finished accumulator from TMEM
-//     (tcgen05.ld), add it to a running fp32 sum in registers in rank order,
-//     release the accumulator, and after the last rank round the sum to bf16
-//     once and store it to all R outputs -- the AllReduce's broadcast --
-//     while the MMA warp already works on the next tile.
-// Only the operands are read and only the R bf16 outputs are written.
+//   * eight epilogue warps keep the running fp32 sum in TMEM as well: once
+//     rank r's product Y_r is complete in its accumulator, they read it and
+//     the sum S_{r-1} (held in the other accumulator), add in rank order
+//     and write S_r = S_{r-1} + Y_r back over Y_r (tcgen05.ld/st).  The
+//     other accumulator is then free for rank r+1, whose MMAs run while the
+//     next sum is formed; two accumulators of 128 x BN fp32 suffice.  After
+//     the last rank they round the sum to bf16 once and store it to all R
+//     outputs -- the AllReduce's broadcast -- while the MMA warp already
+//     works on the next tile.
+// Only the operands are read and only the R bf16 outputs are written.  The
+// producer also prefetches the operands into L2 several k-blocks ahead: all
+// CTAs work on the same k-block at about the same time, so without it every
+// stage would wait for DRAM.
 //
 // Every wait on an mbarrier is bounded by the global timer.  A wait that
 // runs out records a code in this file's status word (read through
@@ -54,30 +61,42 @@ __device__ unsigned int g_tp_status = 0;
 
 namespace {
 
-#ifndef CC_TP_BN
-#define CC_TP_BN 128   // output columns per tile (tcgen05 N)
-#endif
-
 constexpr int kBM = 128;                 // output rows per tile (MMA M)
-constexpr int kBN = CC_TP_BN;            // output columns per tile (MMA N)
 constexpr int kBK = 64;                  // K per stage: 128 bytes of bf16
 constexpr int kUmmaK = 16;               // K of one tcgen05.mma for 16-bit inputs
 constexpr int kTileA = kBM * kBK * 2;    // 16 KiB
-constexpr int kTileB = kBN * kBK * 2;
-constexpr int kStageBytes = kTileA + kTileB;
-// As many stages as fit beside the alignment slack (at most 8).
-constexpr int kStages = (220 * 1024) / kStageBytes < 8 ? (220 * 1024) / kStageBytes : 8;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kAccCols = 256;            // TMEM columns per accumulator
 constexpr int kTmemCols = 2 * kAccCols;  // two accumulators: all 512 columns
-constexpr int kColsPerThread = kBN / 2;  // each epilogue warp covers half a row
-constexpr int kChunks = kColsPerThread / 16;
-static_assert(kBN % 32 == 0 && kColsPerThread % 16 == 0, "epilogue chunks of 16 columns");
-static_assert(kBN % 16 == 0 && kBN <= 256, "tcgen05 N for M = 128");
-static_assert(kBN <= kAccCols, "an accumulator must fit its TMEM columns");
-static_assert(kTileA % 1024 == 0 && kTileB % 1024 == 0, "128B-swizzle atoms are 1 KiB");
+constexpr int kChunk = 32;               // TMEM columns per epilogue load
+
+#ifndef CC_TP_PREFETCH
+#define CC_TP_PREFETCH 0    // k-blocks of L2 prefetch ahead of the loads (0: none;
+                            // 8-32 measured no faster on the GPT-2 MLP shape)
+#endif
+constexpr int kPrefetch = CC_TP_PREFETCH;
+
+// Shapes of one tile width BN (output columns per tile, the MMA's N).
+template <int BN>
+struct TileCfg {
+    static_assert(BN % 64 == 0 && BN <= kAccCols, "BN: 128, 192 or 256");
+    static constexpr int kTileB = BN * kBK * 2;
+    static constexpr int kStageBytes = kTileA + kTileB;
+    static constexpr int kStages = (220 * 1024) / kStageBytes < 8 ? (220 * 1024) / kStageBytes
+                                                                   : 8;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
+    static constexpr int kCols = BN / 2;        // each epilogue warp covers half a row
+    static constexpr int kChunks = kCols / kChunk;
+    static_assert(kCols % kChunk == 0 && kTileB % 1024 == 0, "chunking and swizzle atoms");
+    // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, both
+    // K-major, fp32 accumulator, M = 128, N = BN.
+    static constexpr uint32_t kInstrDesc = (1u << 4)                     // D: f32
+                                         | (1u << 7)                     // A: bf16
+                                         | (1u << 10)                    // B: bf16
+                                         | (static_cast<uint32_t>(BN >> 3) << 17)
+                                         | (static_cast<uint32_t>(kBM >> 4) << 24);
+};
 
 constexpr unsigned kStatusProducer = 8u;
 constexpr unsigned kStatusMma = 16u;
@@ -128,13 +147,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase of this parity to complete, at most kTimeoutNs.
+// Wait for the phase of this parity to complete, at most about kTimeoutNs.
+// The timer is read once every 256 tries, so a wait that succeeds soon
+// costs only the tries.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_test(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_test(bar, parity))
-        if (global_ns() - t0 > kTimeoutNs) return false;
-    return true;
+    unsigned long long t0 = 0;
+    for (uint32_t tries = 1;; ++tries) {
+        if (mbar_test(bar, parity)) return true;
+        if ((tries & 255u) == 0) {
+            const unsigned long long now = global_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kTimeoutNs) return false;
+        }
+    }
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x,
@@ -144,6 +169,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Bring a box of the tensor into L2 ahead of its load (no shared memory).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_map(const CUtensorMap *map) {
@@ -163,19 +194,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, both
-// K-major, fp32 accumulator, M = 128, N = kBN.
-constexpr uint32_t kInstrDesc = (1u << 4)                    // D: f32
-                              | (1u << 7)                    // A: bf16
-                              | (1u << 10)                   // B: bf16
-                              | (static_cast<uint32_t>(kBN >> 3) << 17)
-                              | (static_cast<uint32_t>(kBM >> 4) << 24);
-
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                         uint32_t accumulate) {
+                                         uint32_t idesc, uint32_t accumulate) {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(kInstrDesc), "r"(accumulate)
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
 
@@ -193,29 +216,58 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes: lane i of the
-// warp gets row (lane base + i), columns [col, col + 16).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+#define CC_TMEM_REGS32(r)                                                                  \
+    "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),    \
+    "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),             \
+    "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),          \
+    "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),          \
+    "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+
+// Start loading 32 consecutive fp32 columns of this warp's 32 TMEM lanes:
+// lane i of the warp gets row (lane base + i), columns [col, col + 32).
+// The values are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-          "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-          "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : CC_TMEM_REGS32(r)
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Store 32 fp32 columns of this warp's 32 lanes (the layout of tmem_ld32).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
+          "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+          "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t a, uint32_t b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(a), __uint_as_float(b));
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
 tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
+    using C = TileCfg<BN>;
+    constexpr int kStages = C::kStages;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -270,9 +322,22 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 const int m0 = (tile / p.tiles_n) * kBM;
-                const int n0 = (tile % p.tiles_n) * kBN;
+                const int n0 = (tile % p.tiles_n) * BN;
+                // L2 prefetch kPrefetch k-blocks ahead of the loads, within
+                // the tile.
+                int pf_r = 0, pf_kb = 0;
+                for (int ahead = 0; ahead < kPrefetch && pf_r < R; ++ahead) {
+                    tma_prefetch_2d(&p.tx[pf_r], pf_kb * kBK, m0);
+                    tma_prefetch_2d(&p.tw[pf_r], pf_kb * kBK, n0);
+                    if (++pf_kb == kb_per_rank) { pf_kb = 0; ++pf_r; }
+                }
                 for (int r = 0; ok && r < R; ++r) {
                     for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
+                        if (pf_r < R) {
+                            tma_prefetch_2d(&p.tx[pf_r], pf_kb * kBK, m0);
+                            tma_prefetch_2d(&p.tw[pf_r], pf_kb * kBK, n0);
+                            if (++pf_kb == kb_per_rank) { pf_kb = 0; ++pf_r; }
+                        }
                         const int s = static_cast<int>(it % kStages);
                         const int use = static_cast<int>(it / kStages);
                         if (use > 0 && !mbar_wait(smem_u32(&empty_bar[s]), (use - 1) & 1)) {
@@ -280,9 +345,9 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                             ok = false;
                             break;
                         }
-                        const uint32_t sa = base + static_cast<uint32_t>(s) * kStageBytes;
+                        const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
                         const uint32_t bar = smem_u32(&full_bar[s]);
-                        mbar_arrive_expect_tx(bar, kStageBytes);
+                        mbar_arrive_expect_tx(bar, C::kStageBytes);
                         tma_load_2d(sa, &p.tx[r], kb * kBK, m0, bar);
                         tma_load_2d(sa + kTileA, &p.tw[r], kb * kBK, n0, bar);
                         issued_use[s] = use;
@@ -304,6 +369,8 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
                 for (int r = 0; ok && r < R; ++r, ++job) {
+                    // Job j accumulates into buffer j % 2; that buffer's
+                    // previous content (job j - 2's sum) must have been read.
                     const uint32_t acc = job & 1u;
                     const uint32_t acc_use = job >> 1;
                     if (acc_use > 0 && !mbar_wait(smem_u32(&acc_empty[acc]), (acc_use - 1) & 1)) {
@@ -322,20 +389,20 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sa = base + static_cast<uint32_t>(s) * kStageBytes;
+                        const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
                         const uint64_t da = smem_desc_sw128(sa);
                         const uint64_t db = smem_desc_sw128(sa + kTileA);
 #pragma unroll
                         for (int j = 0; j < kBK / kUmmaK; ++j) {
                             // K step j: 16 elements = 32 bytes further along the
                             // 128-byte swizzled rows (2 in 16-byte units).
-                            mma_bf16(d_tmem, da + 2u * j, db + 2u * j,
+                            mma_bf16(d_tmem, da + 2u * j, db + 2u * j, C::kInstrDesc,
                                      (kb > 0 || j > 0) ? 1u : 0u);
                         }
                         mma_commit(smem_u32(&empty_bar[s]));   // stage free once read
                     }
                     if (!ok) break;
-                    mma_commit(smem_u32(&acc_full[acc]));      // accumulator complete
+                    mma_commit(smem_u32(&acc_full[acc]));      // rank r's product complete
                 }
             }
             // Every MMA issued completes before the TMEM is freed.
@@ -344,24 +411,26 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue: rank-order sum, bf16, R stores ---------
+        // ---------------- epilogue: rank-order sum in TMEM, bf16, R stores --
         const int e = warp - 2;                   // 0..7
         const int quarter = warp % 4;             // TMEM lanes 32*quarter.. (hardware rule)
         const int half = e / 4;                   // column half of the tile
         const int row_in_tile = 32 * quarter + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
+        const uint32_t col_off = static_cast<uint32_t>(half * C::kCols);
         // Rank-indexed pointers read through the parameter's own address
         // (a __grid_constant__ parameter is never copied).
         __nv_bfloat16 *const *outs = p.out;
         float *const *partials = p.partials;
+        const bool keep_partials = partials[0] != nullptr;
+        const size_t n = static_cast<size_t>(p.n);
         uint32_t job = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
             const int m0 = (tile / p.tiles_n) * kBM;
-            const int n0 = (tile % p.tiles_n) * kBN;
+            const int n0 = (tile % p.tiles_n) * BN;
             const size_t row = static_cast<size_t>(m0 + row_in_tile);
-            const int col0 = n0 + half * kColsPerThread;
-            float sum[kColsPerThread];
+            const size_t off = row * n + n0 + col_off;
             for (int r = 0; r < R; ++r, ++job) {
                 const uint32_t acc = job & 1u;
                 const bool ready = mbar_wait(smem_u32(&acc_full[acc]), (job >> 1) & 1);
@@ -371,40 +440,67 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                     break;
                 }
                 tc_fence_after();
-                const uint32_t t0 = tmem + lane_addr + acc * kAccCols + half * kColsPerThread;
+                const uint32_t y_addr = tmem + lane_addr + acc * kAccCols + col_off;
+                const uint32_t s_addr = tmem + lane_addr + (acc ^ 1u) * kAccCols + col_off;
+                if (keep_partials) {
+                    // Rank r's partial product as the tensor cores made it.
+#pragma unroll 1
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        uint32_t y[32];
+                        tmem_ld32(y_addr + kChunk * c, y);
+                        tmem_wait_ld();
+                        float4 *dst = reinterpret_cast<float4 *>(partials[r] + off + kChunk * c);
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    float v[16];
-                    tmem_ld16(t0 + 16 * c, v);
-                    if (partials[0] != nullptr) {
-                        float4 *dst = reinterpret_cast<float4 *>(
-                            partials[r] + row * p.n + col0 + 16 * c);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
-                                                 v[4 * q + 3]);
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(y[4 * q]),
+                                                 __uint_as_float(y[4 * q + 1]),
+                                                 __uint_as_float(y[4 * q + 2]),
+                                                 __uint_as_float(y[4 * q + 3]));
                     }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        sum[16 * c + i] = (r == 0) ? v[i] : __fadd_rn(sum[16 * c + i], v[i]);
                 }
-                // This warp is done with the accumulator: hand it back.
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
-            }
-            if (!ok) break;
-            // Round once to bf16 and store the same 16 bytes to every rank's
-            // output (the AllReduce's result on every rank).
-            const size_t off = row * p.n + col0;
+                if (r > 0) {
+                    // S_r = S_{r-1} + Y_r, written over Y_r; the buffer that
+                    // held S_{r-1} is then free for rank r + 1.
+#pragma unroll 1
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        uint32_t sv[32], y[32];
+                        tmem_ld32(s_addr + kChunk * c, sv);
+                        tmem_ld32(y_addr + kChunk * c, y);
+                        tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < kColsPerThread / 8; ++q) {
-                const uint4 pk = make_uint4(pack_bf16x2(sum[8 * q], sum[8 * q + 1]),
-                                            pack_bf16x2(sum[8 * q + 2], sum[8 * q + 3]),
-                                            pack_bf16x2(sum[8 * q + 4], sum[8 * q + 5]),
-                                            pack_bf16x2(sum[8 * q + 6], sum[8 * q + 7]));
-                for (int r = 0; r < R; ++r)
-                    reinterpret_cast<uint4 *>(outs[r] + off)[q] = pk;
+                        for (int i = 0; i < 32; ++i)
+                            sv[i] = __float_as_uint(__fadd_rn(__uint_as_float(sv[i]),
+                                                              __uint_as_float(y[i])));
+                        tmem_st32(y_addr + kChunk * c, sv);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc ^ 1u]));
+                }
+                if (r == R - 1) {
+                    // Round the sum once to bf16 and store the same bytes to
+                    // every rank's output (the AllReduce's result on every
+                    // rank); then the buffer is free.
+#pragma unroll 1
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        uint32_t sv[32];
+                        tmem_ld32(y_addr + kChunk * c, sv);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 pk = make_uint4(pack_bf16x2(sv[8 * q], sv[8 * q + 1]),
+                                                        pack_bf16x2(sv[8 * q + 2], sv[8 * q + 3]),
+                                                        pack_bf16x2(sv[8 * q + 4], sv[8 * q + 5]),
+                                                        pack_bf16x2(sv[8 * q + 6], sv[8 * q + 7]));
+                            for (int o = 0; o < R; ++o)
+                                reinterpret_cast<uint4 *>(outs[o] + off + kChunk * c)[q] = pk;
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+                }
             }
         }
     }
@@ -461,30 +557,19 @@ int encode_bf16_map(CUtensorMap *map, const void *ptr, int rows, int cols, int b
 }
 
 constexpr int kMaxDevices = 64;
-bool g_attr_set[kMaxDevices];
 std::mutex g_attr_mutex;
 
-}  // namespace
-
-int launch_tp_fused(const void *const *x, const void *const *w, void *const *out,
-                    float *const *partials, int m, int n, int k, int R, int max_ctas,
-                    cudaStream_t stream) {
-    TpFusedParams p{};
-    const int kr = k / R;
+template <int BN>
+int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
+              int kr, int R, int max_ctas, cudaStream_t stream) {
+    static bool attr_set[kMaxDevices];
     int st;
     for (int r = 0; r < R; ++r) {
         if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM, "x", r)) != CC_OK) return st;
-        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, kBN, "w", r)) != CC_OK) return st;
-        p.out[r] = static_cast<__nv_bfloat16 *>(out[r]);
-        p.partials[r] = partials ? partials[r] : nullptr;
+        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, BN, "w", r)) != CC_OK) return st;
     }
-    p.R = R;
-    p.m = m;
-    p.n = n;
-    p.kb_per_rank = kr / kBK;
-    p.tiles_n = n / kBN;
+    p.tiles_n = n / BN;
     p.num_tiles = (m / kBM) * p.tiles_n;
-
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
@@ -493,25 +578,60 @@ int launch_tp_fused(const void *const *x, const void *const *w, void *const *out
     if ((e = device_sm_count(&sms)) != cudaSuccess) return fail_cuda(e, "SM count");
     {
         std::lock_guard<std::mutex> lock(g_attr_mutex);
-        if (!g_attr_set[dev]) {
-            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(tp_fused_kernel),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (!attr_set[dev]) {
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(tp_fused_kernel<BN>),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     TileCfg<BN>::kSmemBytes);
             if (e != cudaSuccess) return fail_cuda(e, "shared memory attribute");
-            g_attr_set[dev] = true;
+            attr_set[dev] = true;
         }
     }
     int grid = sms;
     if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
     if (grid > p.num_tiles) grid = p.num_tiles;
     if (grid < 1) grid = 1;
-    tp_fused_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+    tp_fused_kernel<BN><<<grid, kThreads, TileCfg<BN>::kSmemBytes, stream>>>(p);
     e = cudaGetLastError();
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused tensor-parallel launch");
 }
 
-int tp_fused_tile_n() { return kBN; }
-int tp_fused_tile_m() { return kBM; }
-int tp_fused_tile_k() { return kBK; }
+// The tile width for n output columns: 192 where it divides n (n = 3072
+// gives 16 column tiles), else 256, else 128.
+int pick_bn(int n) {
+#ifdef CC_TP_BN
+    return n % CC_TP_BN == 0 ? CC_TP_BN : 0;
+#else
+    return n % 192 == 0 ? 192 : n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 0;
+#endif
+}
+
+}  // namespace
+
+int launch_tp_fused(const void *const *x, const void *const *w, void *const *out,
+                    float *const *partials, int m, int n, int k, int R, int max_ctas,
+                    cudaStream_t stream) {
+    TpFusedParams p{};
+    const int kr = k / R;
+    for (int r = 0; r < R; ++r) {
+        p.out[r] = static_cast<__nv_bfloat16 *>(out[r]);
+        p.partials[r] = partials ? partials[r] : nullptr;
+    }
+    p.R = R;
+    p.m = m;
+    p.n = n;
+    p.kb_per_rank = kr / kBK;
+    switch (pick_bn(n)) {
+        case 128: return launch_bn<128>(p, x, w, m, n, kr, R, max_ctas, stream);
+        case 192: return launch_bn<192>(p, x, w, m, n, kr, R, max_ctas, stream);
+        case 256: return launch_bn<256>(p, x, w, m, n, kr, R, max_ctas, stream);
+        default: return fail(CC_ERR_INVALID, "n=%d is not a multiple of 128 or 192", n);
+    }
+}
+
+bool tp_fused_shape_ok(int m, int n, int kr) {
+    return m % kBM == 0 && kr % kBK == 0 && pick_bn(n) != 0;
+}
+
 
 cudaError_t read_tp_status(unsigned *status, bool clear) {
     cudaError_t e = cudaMemcpyFromSymbol(status, g_tp_status, sizeof(unsigned));
@@ -548,10 +668,10 @@ extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w
     if (m <= 0 || n <= 0 || k <= 0) return fail(CC_ERR_INVALID, "m, n, k must be > 0");
     if (k % R != 0) return fail(CC_ERR_INVALID, "k=%d is not a multiple of R=%d", k, R);
     const int kr = k / R;
-    if (m % tp_fused_tile_m() != 0 || n % tp_fused_tile_n() != 0 || kr % tp_fused_tile_k() != 0)
+    if (!tp_fused_shape_ok(m, n, kr))
         return fail(CC_ERR_INVALID,
-                    "shape m=%d n=%d k/R=%d: needs m %% %d == 0, n %% %d == 0, k/R %% %d == 0",
-                    m, n, kr, tp_fused_tile_m(), tp_fused_tile_n(), tp_fused_tile_k());
+                    "shape m=%d n=%d k/R=%d: needs m %% 128 == 0, n a multiple of 128 or "
+                    "192, and k/R %% 64 == 0", m, n, kr);
     if (!x || !w || !out) return fail(CC_ERR_INVALID, "x/w/out arrays are NULL");
     const size_t mn = static_cast<size_t>(m) * n;
     std::vector<Span> spans;

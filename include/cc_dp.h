@@ -185,6 +185,31 @@ CC_API int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
                        float grad_scale, int max_ctas, void *stream);
 
 /*
+ * cc_fused_dp_bucket_ex -- cc_fused_dp_bucket with a choice of arithmetic.
+ *   arith_flags  0: the exact step above (every operation one IEEE rounding,
+ *                bit-identical to any correctly rounded evaluation).
+ *                CC_ARITH_FAST: a cheaper form for launches that share the
+ *                GPU with compute (fewer instructions per element, so fewer
+ *                SMs stream the bucket at HBM speed).  The sum, m and v are
+ *                exactly as above; the bias corrections become
+ *                multiplications by fl(1/bc1), fl(1/bc2), the square root
+ *                stays IEEE, and m^/(sqrt(v^) + eps) is a fast division
+ *                (2 ulp).  The parameter then differs from the exact step by
+ *                a few ulp of its update (well inside a relative 1e-5 of the
+ *                parameter unless the update cancels it), the bf16 copies by
+ *                at most one bf16 ulp.  Requires eps > 0 for that bound.
+ *                Other bits: CC_ERR_INVALID.
+ */
+#define CC_ARITH_FAST 1u
+CC_API int cc_fused_dp_bucket_ex(const void *const *grads, const float *const *acc,
+                                 float *master, float *m, float *v,
+                                 void *const *params_out, size_t n, int R, size_t begin,
+                                 size_t end, float lr, float beta1, float beta2,
+                                 float eps, float weight_decay, int step,
+                                 float grad_scale, int max_ctas, unsigned arith_flags,
+                                 void *stream);
+
+/*
  * cc_fused_dp_shard -- one rank's share of the sharded step, with the
  * optimizer state sharded ("LIT-735 (CoCoNet)", Key takeaways: the fused
  * ReduceScatter-optimizer-AllGather fits larger micro-batches by sharding
@@ -434,6 +459,8 @@ typedef struct cc_overlap_cfg {
     int gemm_algo;                 /* 0: the proxy GEMMs through cublasGemmEx (cuBLAS's
                                       choice); k > 0: through cuBLASLt with the k-th
                                       candidate of its heuristic (no workspace) */
+    unsigned arith_flags;          /* the buckets' arithmetic: 0 exact, CC_ARITH_FAST
+                                      (see cc_fused_dp_bucket_ex) */
 } cc_overlap_cfg;
 
 typedef struct cc_overlap_result {
@@ -513,8 +540,9 @@ CC_API int cc_tp_overlap_bench(const cc_tp_cfg *cfg, cc_tp_result *out);
  *   partials     NULL, or [R] fp32 m x n each, written: each rank's partial
  *                product as the tensor cores accumulated it (for checking
  *                the reduction; costs 4R bytes per output element).
- *   m, n, k, R   k % R == 0; m % 128 == 0, n % 128 == 0 and (k/R) % 64 == 0
- *                (the kernel's tile), else CC_ERR_INVALID.  R in 1..CC_MAX_R.
+ *   m, n, k, R   k % R == 0; m % 128 == 0, n a multiple of 128 or 192, and
+ *                (k/R) % 64 == 0 (the kernel's tiles), else CC_ERR_INVALID.
+ *                R in 1..CC_MAX_R.
  *   stream       cudaStream_t.
  * Buffers are device memory, 16-byte aligned; written buffers overlap
  * nothing.  Allocates nothing.  A pipeline wait that runs out (each is

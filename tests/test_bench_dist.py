@@ -62,20 +62,6 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["e2e"]["h2d_bytes_per_step"] == 0
 
 
-def test_shard_ranges_partition_each_bucket():
-    sys.path.insert(0, ROOT)
-    import bench
-    for begin, end in [(0, 8), (0, 64), (16, 16 + 8 * 1001), (40, 40 + 8 * 7 + 5)]:
-        for count in (1, 2, 3, 8, 16):
-            parts = [bench.shard_range(begin, end, count, k) for k in range(count)]
-            assert parts[0][0] == begin and parts[-1][1] == end
-            for (a, b), (c, _) in zip(parts, parts[1:]):
-                assert b == c and a <= b and (a - begin) % 8 == 0
-            sizes = [b - a for a, b in parts[:-1]]
-            if sizes:
-                assert max(sizes) - min(sizes) <= 8
-
-
 def test_oracle_split_over_threads_gives_the_same_bits():
     """The CPU baseline's threaded form (contiguous chunks, one oracle call
     each) leaves master/m/v bit-identical to one call over the sample."""
