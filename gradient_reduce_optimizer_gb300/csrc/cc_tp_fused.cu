@@ -23,15 +23,13 @@
 //     accumulate) from those stages into one of two TMEM accumulators: rank
 //     r of the CTA's j-th job goes to accumulator (j*R + r) % 2, so the next
 //     rank's MMAs run while the epilogue drains the previous one;
-//   * eight epilogue warps keep the running fp32 sum in TMEM as well: once
-//     rank r's product Y_r is complete in its accumulator, they read it and
-//     the sum S_{r-1} (held in the other accumulator), add in rank order
-//     and write S_r = S_{r-1} + Y_r back over Y_r (tcgen05.ld/st).  The
-//     other accumulator is then free for rank r+1, whose MMAs run while the
-//     next sum is formed; two accumulators of 128 x BN fp32 suffice.  After
-//     the last rank they round the sum to bf16 once and store it to all R
-//     outputs -- the AllReduce's broadcast -- while the MMA warp already
-//     works on the next tile.
+//   * 4 * BN / 64 epilogue warps (each thread one row and 64 columns) read
+//     each finished accumulator from TMEM (tcgen05.ld), add it to a running
+//     fp32 sum in registers in rank order, and hand the accumulator back at
+//     once, so the MMAs of rank r+2 never wait for more than that read.
+//     After the last rank they round the sum to bf16 once and store it to
+//     all R outputs -- the AllReduce's broadcast -- while the MMA warp
+//     already works on the next tile.
 // Only the operands are read and only the R bf16 outputs are written.  The
 // producer also prefetches the operands into L2 several k-blocks ahead: all
 // CTAs work on the same k-block at about the same time, so without it every
@@ -65,8 +63,7 @@ constexpr int kBM = 128;                 // output rows per tile (MMA M)
 constexpr int kBK = 64;                  // K per stage: 128 bytes of bf16
 constexpr int kUmmaK = 16;               // K of one tcgen05.mma for 16-bit inputs
 constexpr int kTileA = kBM * kBK * 2;    // 16 KiB
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiCols = 64;             // output columns per epilogue thread
 constexpr int kAccCols = 256;            // TMEM columns per accumulator
 constexpr int kTmemCols = 2 * kAccCols;  // two accumulators: all 512 columns
 constexpr int kChunk = 32;               // TMEM columns per epilogue load
@@ -77,18 +74,29 @@ constexpr int kChunk = 32;               // TMEM columns per epilogue load
 #endif
 constexpr int kPrefetch = CC_TP_PREFETCH;
 
+#ifndef CC_TP_STAGE_FENCE
+#define CC_TP_STAGE_FENCE 1   // tcgen05 fence after each stage's full-barrier wait
+#endif
+
 // Shapes of one tile width BN (output columns per tile, the MMA's N).
 template <int BN>
 struct TileCfg {
     static_assert(BN % 64 == 0 && BN <= kAccCols, "BN: 128, 192 or 256");
     static constexpr int kTileB = BN * kBK * 2;
     static constexpr int kStageBytes = kTileA + kTileB;
-    static constexpr int kStages = (220 * 1024) / kStageBytes < 8 ? (220 * 1024) / kStageBytes
-                                                                   : 8;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + alignment slack
-    static constexpr int kCols = BN / 2;        // each epilogue warp covers half a row
-    static constexpr int kChunks = kCols / kChunk;
-    static_assert(kCols % kChunk == 0 && kTileB % 1024 == 0, "chunking and swizzle atoms");
+    // Epilogue: one warp per 32 TMEM lanes and 64 columns, so that every
+    // thread holds 64 running sums: 4 * BN / 64 warps, plus the producer and
+    // MMA warps.  Each epilogue warp stages its 32 x 64 bf16 output block
+    // (4 KiB) in shared memory for the TMA stores.
+    static constexpr int kEpiWarps = 4 * (BN / kEpiCols);
+    static constexpr int kThreads = 32 * (2 + kEpiWarps);
+    static constexpr int kOutBox = 32 * kEpiCols * 2;
+    static constexpr int kOutBytes = kEpiWarps * kOutBox;
+    static constexpr int kStages =
+        (220 * 1024 - kOutBytes) / kStageBytes < 8 ? (220 * 1024 - kOutBytes) / kStageBytes : 8;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;   // + align
+    static constexpr int kChunks = kEpiCols / kChunk;
+    static_assert(BN % kEpiCols == 0 && kTileB % 1024 == 0, "epilogue groups and swizzle atoms");
     // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, both
     // K-major, fp32 accumulator, M = 128, N = BN.
     static constexpr uint32_t kInstrDesc = (1u << 4)                     // D: f32
@@ -105,8 +113,9 @@ constexpr unsigned kStatusDrain = 64u;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // two seconds per wait
 
 struct TpFusedParams {
-    CUtensorMap tx[CC_MAX_R];     // X_r: {k/R, m}, box {64, 128}
-    CUtensorMap tw[CC_MAX_R];     // W_r: {k/R, n}, box {64, BN}
+    CUtensorMap tx[CC_MAX_R];     // X_r: {k/R, m}, box {64, 128 / CN}
+    CUtensorMap tw[CC_MAX_R];     // W_r: {k/R, n}, box {64, BN / CM}
+    CUtensorMap tout[CC_MAX_R];   // out[r]: {n, m}, box {64, 32}
     __nv_bfloat16 *out[CC_MAX_R]; // m x n each
     float *partials[CC_MAX_R];    // m x n each, or all null
     int R, m, n, kb_per_rank;     // kb_per_rank = (k/R) / 64
@@ -171,6 +180,56 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// The same box delivered to the same shared-memory offset of every CTA in
+// cta_mask (this GPU's own memory, within one cluster), each signalling its
+// own mbarrier at the same offset.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map,
+                                                      int x, int y, uint32_t bar,
+                                                      uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar),
+          "h"(cta_mask)
+        : "memory");
+}
+
+// Shared -> global tensor store of one box (bulk async group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y,
+                                             uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the bulk groups committed so far have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until they have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Make this thread's shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; orders shared-memory set-up
+// (mbarrier initialisation) before any peer's use of it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Bring a box of the tensor into L2 ahead of its load (no shared memory).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];"
@@ -207,6 +266,13 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(bar) : "memory");
+}
+
+// The same, arriving on the mbarrier at this offset in every CTA of cta_mask.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster"
+                 ".multicast::cluster.b64 [%0], %1;"
+                 ::"r"(bar), "h"(cta_mask) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -263,11 +329,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+// CM x CN CTAs form a cluster working on CM x CN neighbouring tiles: CTA
+// (a, b) (cluster rank a + CM b) computes the tile in row a and column b of
+// the group.  The tiles of one row share their X tile and those of one
+// column their W tile, so each CTA loads 1/CN of its X tile and 1/CM of its
+// W tile and multicasts them to the CTAs that share them: every shared-
+// memory stage is filled by the CTAs of its row and column.  A stage may be
+// refilled only once all of those CTAs' MMAs have read it, so each MMA
+// commit arrives on the empty barriers of its whole row and column.
+// CM = CN = 1 is the plain single-CTA kernel.
+template <int BN, int CM, int CN>
+__global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
 tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
     using C = TileCfg<BN>;
     constexpr int kStages = C::kStages;
+    constexpr int kCluster = CM * CN;
+    constexpr int kSliceA = kBM / CN;          // rows of the X tile this CTA loads
+    constexpr int kSliceB = BN / CM;           // rows of the W tile this CTA loads
+    static_assert(kSliceA % 8 == 0 && kSliceB % 8 == 0, "slices of whole 1 KiB atoms");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -283,19 +362,29 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
     const int lane = threadIdx.x % 32;
     const int R = p.R;
     const int kb_per_rank = p.kb_per_rank;
+    const uint32_t crank = kCluster > 1 ? cluster_ctarank() : 0u;
+    const int ca = static_cast<int>(crank) % CM;     // row of the group
+    const int cb = static_cast<int>(crank) / CM;     // column of the group
+    uint16_t row_set = 0, col_set = 0;
+#pragma unroll
+    for (int b = 0; b < CN; ++b) row_set |= static_cast<uint16_t>(1u << (ca + CM * b));
+#pragma unroll
+    for (int a = 0; a < CM; ++a) col_set |= static_cast<uint16_t>(1u << (a + CM * cb));
+    const uint16_t peers = row_set | col_set;         // who fills, and reads, this stage
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), CM + CN - 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&acc_full[a]), 1);
-            mbar_init(smem_u32(&acc_empty[a]), kEpiWarps);
+            mbar_init(smem_u32(&acc_empty[a]), C::kEpiWarps);
         }
         mbar_init(smem_u32(&mma_done), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if constexpr (kCluster > 1) cluster_sync();       // peers' barriers exist
     if (warp == 0 && lane == 0) {
         for (int r = 0; r < R; ++r) {
             prefetch_map(&p.tx[r]);
@@ -312,6 +401,11 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_slot;
+    // Groups of CM x CN tiles, one per cluster at a time.
+    const int groups_n = p.tiles_n / CN;
+    const int num_groups = (p.num_tiles / p.tiles_n / CM) * groups_n;
+    const int first_group = static_cast<int>(blockIdx.x) / kCluster;
+    const int group_stride = static_cast<int>(gridDim.x) / kCluster;
 
     if (warp == 0) {
         // ---------------- producer: TMA loads of X_r and W_r tiles --------
@@ -320,9 +414,9 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
             for (int s = 0; s < kStages; ++s) issued_use[s] = -1;
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const int m0 = (tile / p.tiles_n) * kBM;
-                const int n0 = (tile % p.tiles_n) * BN;
+            for (int g = first_group; ok && g < num_groups; g += group_stride) {
+                const int m0 = ((g / groups_n) * CM + ca) * kBM;
+                const int n0 = ((g % groups_n) * CN + cb) * BN;
                 // L2 prefetch kPrefetch k-blocks ahead of the loads, within
                 // the tile.
                 int pf_r = 0, pf_kb = 0;
@@ -347,19 +441,39 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                         }
                         const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
                         const uint32_t bar = smem_u32(&full_bar[s]);
+                        // the whole stage arrives: this CTA's slices and its
+                        // row's and column's multicasts
                         mbar_arrive_expect_tx(bar, C::kStageBytes);
-                        tma_load_2d(sa, &p.tx[r], kb * kBK, m0, bar);
-                        tma_load_2d(sa + kTileA, &p.tw[r], kb * kBK, n0, bar);
+                        const uint32_t dst_a = sa + static_cast<uint32_t>(cb * kSliceA * 128);
+                        const uint32_t dst_b =
+                            sa + kTileA + static_cast<uint32_t>(ca * kSliceB * 128);
+                        if constexpr (CN > 1)
+                            tma_load_2d_multicast(dst_a, &p.tx[r], kb * kBK, m0 + cb * kSliceA,
+                                                  bar, row_set);
+                        else
+                            tma_load_2d(dst_a, &p.tx[r], kb * kBK, m0, bar);
+                        if constexpr (CM > 1)
+                            tma_load_2d_multicast(dst_b, &p.tw[r], kb * kBK, n0 + ca * kSliceB,
+                                                  bar, col_set);
+                        else
+                            tma_load_2d(dst_b, &p.tw[r], kb * kBK, n0, bar);
                         issued_use[s] = use;
                     }
                 }
             }
-            // Every copy issued lands before the CTA may exit (it writes this
-            // CTA's shared memory).  Issued copies always land.
+            // Every copy into this CTA's shared memory lands, and every
+            // peer MMA's arrival on its empty barriers happens, before the
+            // CTA may exit.  Issued copies always land.
             for (int s = 0; s < kStages; ++s)
                 if (issued_use[s] >= 0 &&
                     !mbar_wait(smem_u32(&full_bar[s]), issued_use[s] & 1))
                     atomicOr(&g_tp_status, kStatusDrain);
+            if constexpr (kCluster > 1) {
+                for (int s = 0; s < kStages; ++s)
+                    if (issued_use[s] >= 0 &&
+                        !mbar_wait(smem_u32(&empty_bar[s]), issued_use[s] & 1))
+                        atomicOr(&g_tp_status, kStatusDrain);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -367,7 +481,7 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
         if (lane == 0) {
             uint32_t it = 0, job = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int g = first_group; ok && g < num_groups; g += group_stride) {
                 for (int r = 0; ok && r < R; ++r, ++job) {
                     // Job j accumulates into buffer j % 2; that buffer's
                     // previous content (job j - 2's sum) must have been read.
@@ -388,7 +502,9 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                             ok = false;
                             break;
                         }
+#if CC_TP_STAGE_FENCE
                         tc_fence_after();
+#endif
                         const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
                         const uint64_t da = smem_desc_sw128(sa);
                         const uint64_t db = smem_desc_sw128(sa + kTileA);
@@ -399,7 +515,11 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                             mma_bf16(d_tmem, da + 2u * j, db + 2u * j, C::kInstrDesc,
                                      (kb > 0 || j > 0) ? 1u : 0u);
                         }
-                        mma_commit(smem_u32(&empty_bar[s]));   // stage free once read
+                        // the stage is free in every CTA that fills it once read
+                        if constexpr (kCluster > 1)
+                            mma_commit_multicast(smem_u32(&empty_bar[s]), peers);
+                        else
+                            mma_commit(smem_u32(&empty_bar[s]));
                     }
                     if (!ok) break;
                     mma_commit(smem_u32(&acc_full[acc]));      // rank r's product complete
@@ -411,26 +531,27 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue: rank-order sum in TMEM, bf16, R stores --
-        const int e = warp - 2;                   // 0..7
+        // ---------------- epilogue: rank-order sum, bf16, R stores ---------
+        const int e = warp - 2;                   // 0 .. kEpiWarps-1
         const int quarter = warp % 4;             // TMEM lanes 32*quarter.. (hardware rule)
-        const int half = e / 4;                   // column half of the tile
+        const int group = e / 4;                  // 64-column group of the tile
         const int row_in_tile = 32 * quarter + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
-        const uint32_t col_off = static_cast<uint32_t>(half * C::kCols);
+        const uint32_t col_off = static_cast<uint32_t>(group * kEpiCols);
+        const uint32_t out_box = base + static_cast<uint32_t>(kStages * C::kStageBytes) +
+                                 static_cast<uint32_t>(e * C::kOutBox);
         // Rank-indexed pointers read through the parameter's own address
         // (a __grid_constant__ parameter is never copied).
-        __nv_bfloat16 *const *outs = p.out;
         float *const *partials = p.partials;
         const bool keep_partials = partials[0] != nullptr;
         const size_t n = static_cast<size_t>(p.n);
         uint32_t job = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            const int m0 = (tile / p.tiles_n) * kBM;
-            const int n0 = (tile % p.tiles_n) * BN;
-            const size_t row = static_cast<size_t>(m0 + row_in_tile);
-            const size_t off = row * n + n0 + col_off;
+        for (int g = first_group; ok && g < num_groups; g += group_stride) {
+            const int m0 = ((g / groups_n) * CM + ca) * kBM;
+            const int n0 = ((g % groups_n) * CN + cb) * BN;
+            const size_t off = static_cast<size_t>(m0 + row_in_tile) * n + n0 + col_off;
+            float sum[kEpiCols];
             for (int r = 0; r < R; ++r, ++job) {
                 const uint32_t acc = job & 1u;
                 const bool ready = mbar_wait(smem_u32(&acc_full[acc]), (job >> 1) & 1);
@@ -441,14 +562,13 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                 }
                 tc_fence_after();
                 const uint32_t y_addr = tmem + lane_addr + acc * kAccCols + col_off;
-                const uint32_t s_addr = tmem + lane_addr + (acc ^ 1u) * kAccCols + col_off;
-                if (keep_partials) {
-                    // Rank r's partial product as the tensor cores made it.
-#pragma unroll 1
-                    for (int c = 0; c < C::kChunks; ++c) {
-                        uint32_t y[32];
-                        tmem_ld32(y_addr + kChunk * c, y);
-                        tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    uint32_t y[32];
+                    tmem_ld32(y_addr + kChunk * c, y);
+                    tmem_wait_ld();
+                    if (keep_partials) {
+                        // rank r's partial product as the tensor cores made it
                         float4 *dst = reinterpret_cast<float4 *>(partials[r] + off + kChunk * c);
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
@@ -457,56 +577,55 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
                                                  __uint_as_float(y[4 * q + 2]),
                                                  __uint_as_float(y[4 * q + 3]));
                     }
-                }
-                if (r > 0) {
-                    // S_r = S_{r-1} + Y_r, written over Y_r; the buffer that
-                    // held S_{r-1} is then free for rank r + 1.
-#pragma unroll 1
-                    for (int c = 0; c < C::kChunks; ++c) {
-                        uint32_t sv[32], y[32];
-                        tmem_ld32(s_addr + kChunk * c, sv);
-                        tmem_ld32(y_addr + kChunk * c, y);
-                        tmem_wait_ld();
+                    // rank order: S_0 = Y_0, S_r = S_{r-1} + Y_r
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            sv[i] = __float_as_uint(__fadd_rn(__uint_as_float(sv[i]),
-                                                              __uint_as_float(y[i])));
-                        tmem_st32(y_addr + kChunk * c, sv);
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc ^ 1u]));
+                    for (int i = 0; i < 32; ++i)
+                        sum[kChunk * c + i] = r == 0 ? __uint_as_float(y[i])
+                                                     : __fadd_rn(sum[kChunk * c + i],
+                                                                 __uint_as_float(y[i]));
                 }
-                if (r == R - 1) {
-                    // Round the sum once to bf16 and store the same bytes to
-                    // every rank's output (the AllReduce's result on every
-                    // rank); then the buffer is free.
-#pragma unroll 1
-                    for (int c = 0; c < C::kChunks; ++c) {
-                        uint32_t sv[32];
-                        tmem_ld32(y_addr + kChunk * c, sv);
-                        tmem_wait_ld();
+                // The accumulator has been read: rank r + 2 may reuse it.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
+            }
+            if (!ok) break;
+            // Round the sum once to bf16 into this warp's 32 x 64 staging box
+            // (the 128-byte swizzle: 16-byte chunk j of row i at chunk
+            // j ^ (i % 8), no bank conflicts beyond the minimum), then TMA
+            // stores the box to every rank's output -- the AllReduce's
+            // result on every rank -- in whole lines, while the MMA warp
+            // already accumulates the next tile.
+            if (lane == 0) bulk_wait_read_all();     // the last tile's stores have read it
+            __syncwarp();
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 pk = make_uint4(pack_bf16x2(sv[8 * q], sv[8 * q + 1]),
-                                                        pack_bf16x2(sv[8 * q + 2], sv[8 * q + 3]),
-                                                        pack_bf16x2(sv[8 * q + 4], sv[8 * q + 5]),
-                                                        pack_bf16x2(sv[8 * q + 6], sv[8 * q + 7]));
-                            for (int o = 0; o < R; ++o)
-                                reinterpret_cast<uint4 *>(outs[o] + off + kChunk * c)[q] = pk;
-                        }
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[acc]));
-                }
+            for (int q = 0; q < kEpiCols / 8; ++q) {
+                const uint4 pk = make_uint4(
+                    pack_bf16x2(__float_as_uint(sum[8 * q]), __float_as_uint(sum[8 * q + 1])),
+                    pack_bf16x2(__float_as_uint(sum[8 * q + 2]), __float_as_uint(sum[8 * q + 3])),
+                    pack_bf16x2(__float_as_uint(sum[8 * q + 4]), __float_as_uint(sum[8 * q + 5])),
+                    pack_bf16x2(__float_as_uint(sum[8 * q + 6]), __float_as_uint(sum[8 * q + 7])));
+                const uint32_t chunk = static_cast<uint32_t>(q) ^ static_cast<uint32_t>(lane & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                             ::"r"(out_box + static_cast<uint32_t>(lane) * 128u + chunk * 16u),
+                               "r"(pk.x), "r"(pk.y), "r"(pk.z), "r"(pk.w) : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int x = n0 + static_cast<int>(col_off);
+                const int y = m0 + 32 * quarter;
+                for (int o = 0; o < R; ++o) tma_store_2d(&p.tout[o], x, y, out_box);
+                bulk_commit_group();
             }
         }
+        if (lane == 0) bulk_wait_all();               // stores done before exit
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (kCluster > 1) cluster_sync();       // no peer still writes here
     tc_fence_after();
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
@@ -559,17 +678,21 @@ int encode_bf16_map(CUtensorMap *map, const void *ptr, int rows, int cols, int b
 constexpr int kMaxDevices = 64;
 std::mutex g_attr_mutex;
 
-template <int BN>
-int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
-              int kr, int R, int max_ctas, cudaStream_t stream) {
+template <int BN, int CM, int CN>
+int launch_cfg(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
+               int kr, int R, int max_ctas, cudaStream_t stream) {
     static bool attr_set[kMaxDevices];
+    constexpr int kCluster = CM * CN;
+    auto kernel = tp_fused_kernel<BN, CM, CN>;
     int st;
     for (int r = 0; r < R; ++r) {
-        if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM, "x", r)) != CC_OK) return st;
-        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, BN, "w", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM / CN, "x", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, BN / CM, "w", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tout[r], p.out[r], m, n, 32, "out", r)) != CC_OK) return st;
     }
     p.tiles_n = n / BN;
     p.num_tiles = (m / kBM) * p.tiles_n;
+    const int num_groups = p.num_tiles / kCluster;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
@@ -579,21 +702,66 @@ int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int 
     {
         std::lock_guard<std::mutex> lock(g_attr_mutex);
         if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(tp_fused_kernel<BN>),
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      TileCfg<BN>::kSmemBytes);
             if (e != cudaSuccess) return fail_cuda(e, "shared memory attribute");
             attr_set[dev] = true;
         }
     }
-    int grid = sms;
-    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-    if (grid > p.num_tiles) grid = p.num_tiles;
-    if (grid < 1) grid = 1;
-    tp_fused_kernel<BN><<<grid, kThreads, TileCfg<BN>::kSmemBytes, stream>>>(p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(TileCfg<BN>::kThreads);
+    cfg.dynamicSmemBytes = TileCfg<BN>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // One CTA per SM: as many clusters as the GPU holds at once (clusters
+    // need their CTAs on SMs of one GPC), at most one per group.
+    int clusters = sms / kCluster;
+    if (kCluster > 1) {
+        cfg.gridDim = dim3(static_cast<unsigned>(kCluster * clusters));
+        int active = 0;
+        e = cudaOccupancyMaxActiveClusters(&active, kernel, &cfg);
+        if (e != cudaSuccess) return fail_cuda(e, "cluster occupancy");
+        if (active > 0 && active < clusters) clusters = active;
+    }
+    if (max_ctas > 0 && clusters * kCluster > max_ctas) clusters = max_ctas / kCluster;
+    if (clusters > num_groups) clusters = num_groups;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(kCluster * clusters));
+    e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused tensor-parallel launch");
 }
+
+// The cluster shape for a tile grid: pairs along M (2 x 1, sharing the W
+// tile) where the row-tile count is even, else one CTA.  Measured on the
+// GPT-2 MLP shape (R = 8, m = 8192, n = 3072, k = 12288, BN = 192): 1 x 1,
+// 2 x 1 and 1 x 2 all 0.597 ms, 2 x 2 0.682 ms (fewer 4-CTA clusters fit at
+// once than 152 / 4), so multicast halves the W tile's L2 reads at no cost
+// but buys no time: one SM's operand intake, not L2, is the bound.
+#if defined(CC_TP_CLUSTER_M) && defined(CC_TP_CLUSTER_N)
+template <int BN>
+int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
+              int kr, int R, int max_ctas, cudaStream_t stream) {
+    if ((m / kBM) % CC_TP_CLUSTER_M != 0 || (n / BN) % CC_TP_CLUSTER_N != 0)
+        return launch_cfg<BN, 1, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
+    return launch_cfg<BN, CC_TP_CLUSTER_M, CC_TP_CLUSTER_N>(p, x, w, m, n, kr, R, max_ctas,
+                                                            stream);
+}
+#else
+template <int BN>
+int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
+              int kr, int R, int max_ctas, cudaStream_t stream) {
+    if ((m / kBM) % 2 == 0) return launch_cfg<BN, 2, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
+    return launch_cfg<BN, 1, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
+}
+#endif
 
 // The tile width for n output columns: 192 where it divides n (n = 3072
 // gives 16 column tiles), else 256, else 128.
