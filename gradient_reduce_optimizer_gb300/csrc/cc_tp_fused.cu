@@ -217,6 +217,53 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+
+// A TMA load into this CTA's shared memory that signals an mbarrier of
+// either CTA of the pair (the MMA pair's leader).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x,
+                                                 int y, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+        : "memory");
+}
+
+// Arrive on an mbarrier given by its cluster address (here: the leader's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// The leader's own mbarrier, once every pair MMA issued before has
+// completed (a kernel uses one CTA-group form throughout).
+__device__ __forceinline__ void mma_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+// Arrive on the mbarrier at this offset in both CTAs of the pair once every
+// pair MMA issued before has completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster"
+                 ".multicast::cluster.b64 [%0], %1;"
+                 ::"r"(bar), "h"(static_cast<uint16_t>(3)) : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -304,24 +351,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Store 32 fp32 columns of this warp's 32 lanes (the layout of tmem_ld32).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
-          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
-          "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
-          "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-          "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t a, uint32_t b) {
@@ -633,6 +662,278 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// The pair form: one MMA over two SMs (tcgen05 cta_group::2, M = 256).
+//
+// Two CTAs of a cluster compute two vertically adjacent 128 x BN tiles as
+// one 256 x BN product.  Each CTA loads its own 128 rows of X and half of the
+// W tile (BN/2 rows) into its own shared memory; the leader CTA (rank 0)
+// issues the MMAs, which read A from each CTA's own stage and B from both,
+// and accumulate each CTA's 128 rows in that CTA's TMEM.  So each SM takes in
+// 16 KiB of X and BN/2 x 128 bytes of W per k-block of 64, against 16 KiB +
+// BN x 128 bytes for the single-CTA kernel: 30% fewer operand bytes per
+// FLOP at BN = 192, where one SM's operand intake is the bound.
+//   * Both CTAs' TMA loads signal the leader's "full" barrier (expecting both
+//     CTAs' bytes); the leader's MMA commits arrive on the "empty" barriers
+//     and the accumulator barriers of both CTAs.
+//   * Each CTA's epilogue reads its own TMEM lanes, keeps the rank-order sum
+//     in registers and hands the accumulator back on the leader's barrier
+//     (both CTAs' epilogue warps must arrive); the output leaves through the
+//     same per-warp TMA stores as the single-CTA kernel.
+// TMEM is allocated for the pair (both CTAs' allocating warps take part).
+// ---------------------------------------------------------------------------
+
+template <int BN>
+struct PairCfg {
+    static_assert(BN % 64 == 0 && BN <= kAccCols, "BN: 128, 192 or 256");
+    static constexpr int kHalfB = BN / 2;                 // W rows this CTA loads
+    static constexpr int kTileB = kHalfB * kBK * 2;
+    static constexpr int kStageBytes = kTileA + kTileB;
+    static constexpr int kEpiWarps = 4 * (BN / kEpiCols);
+    static constexpr int kThreads = 32 * (2 + kEpiWarps);
+    static constexpr int kOutBox = 32 * kEpiCols * 2;
+    static constexpr int kOutBytes = kEpiWarps * kOutBox;
+    static constexpr int kStages =
+        (220 * 1024 - kOutBytes) / kStageBytes < 8 ? (220 * 1024 - kOutBytes) / kStageBytes : 8;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;
+    static constexpr int kChunks = kEpiCols / kChunk;
+    static_assert(kTileB % 1024 == 0, "swizzle atoms");
+    // tcgen05.mma kind::f16, bf16 A and B (K-major), fp32 accumulator,
+    // M = 256 (the pair), N = BN.
+    static constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10)
+                                         | (static_cast<uint32_t>(BN >> 3) << 17)
+                                         | (static_cast<uint32_t>(256 >> 4) << 24);
+};
+
+template <int BN>
+__global__ void __launch_bounds__(PairCfg<BN>::kThreads, 1)
+tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
+    using C = PairCfg<BN>;
+    constexpr int kStages = C::kStages;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];    // the leader's is used
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];         // the leader's is used
+    __shared__ __align__(8) uint64_t mma_done;
+    __shared__ uint32_t tmem_base_slot;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int R = p.R;
+    const int kb_per_rank = p.kb_per_rank;
+    const uint32_t crank = cluster_ctarank();               // 0: the leader
+    const bool leader = crank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&acc_full[a]), 1);
+            mbar_init(smem_u32(&acc_empty[a]), 2 * C::kEpiWarps);
+        }
+        mbar_init(smem_u32(&mma_done), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    cluster_sync();                                          // the pair's barriers exist
+    if (warp == 0 && lane == 0) {
+        for (int r = 0; r < R; ++r) {
+            prefetch_map(&p.tx[r]);
+            prefetch_map(&p.tw[r]);
+        }
+    }
+    if (warp == 1) {
+        // One warp of each CTA of the pair allocates, together, all 512
+        // columns in both CTAs.
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&tmem_base_slot)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_slot;
+    // Pairs of row tiles, one pair per cluster at a time.
+    const int num_groups = (p.num_tiles / p.tiles_n / 2) * p.tiles_n;
+    const int first_group = static_cast<int>(blockIdx.x) / 2;
+    const int group_stride = static_cast<int>(gridDim.x) / 2;
+
+    if (warp == 0) {
+        // ---------------- producer (both CTAs) --------------------------
+        if (lane == 0) {
+            int issued_use[kStages];
+            for (int s = 0; s < kStages; ++s) issued_use[s] = -1;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int g = first_group; ok && g < num_groups; g += group_stride) {
+                const int m0 = ((g / p.tiles_n) * 2 + static_cast<int>(crank)) * kBM;
+                const int n0 = (g % p.tiles_n) * BN;
+                for (int r = 0; ok && r < R; ++r) {
+                    for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
+                        const int s = static_cast<int>(it % kStages);
+                        const int use = static_cast<int>(it / kStages);
+                        if (use > 0 && !mbar_wait(smem_u32(&empty_bar[s]), (use - 1) & 1)) {
+                            atomicOr(&g_tp_status, kStatusProducer);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
+                        const uint32_t leader_full = map_to_cta(smem_u32(&full_bar[s]), 0);
+                        if (leader)   // both CTAs' bytes land before the stage is full
+                            mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * C::kStageBytes);
+                        tma_load_2d_pair(sa, &p.tx[r], kb * kBK, m0, leader_full);
+                        tma_load_2d_pair(sa + kTileA, &p.tw[r], kb * kBK,
+                                         n0 + static_cast<int>(crank) * C::kHalfB, leader_full);
+                        issued_use[s] = use;
+                    }
+                }
+            }
+            // The leader's MMAs have read every stage this CTA filled (and so
+            // every copy into it has landed) before the CTA may exit.
+            for (int s = 0; s < kStages; ++s)
+                if (issued_use[s] >= 0 &&
+                    !mbar_wait(smem_u32(&empty_bar[s]), issued_use[s] & 1))
+                    atomicOr(&g_tp_status, kStatusDrain);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (the leader only) ------------------
+        if (leader && lane == 0) {
+            uint32_t it = 0, job = 0;
+            bool ok = true;
+            for (int g = first_group; ok && g < num_groups; g += group_stride) {
+                for (int r = 0; ok && r < R; ++r, ++job) {
+                    const uint32_t acc = job & 1u;
+                    const uint32_t acc_use = job >> 1;
+                    if (acc_use > 0 && !mbar_wait(smem_u32(&acc_empty[acc]), (acc_use - 1) & 1)) {
+                        atomicOr(&g_tp_status, kStatusMma);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + acc * kAccCols;
+                    for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
+                        const int s = static_cast<int>(it % kStages);
+                        const int use = static_cast<int>(it / kStages);
+                        if (!mbar_wait(smem_u32(&full_bar[s]), use & 1)) {
+                            atomicOr(&g_tp_status, kStatusMma);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
+                        const uint64_t da = smem_desc_sw128(sa);
+                        const uint64_t db = smem_desc_sw128(sa + kTileA);
+#pragma unroll
+                        for (int j = 0; j < kBK / kUmmaK; ++j)
+                            mma_bf16_pair(d_tmem, da + 2u * j, db + 2u * j, C::kInstrDesc,
+                                          (kb > 0 || j > 0) ? 1u : 0u);
+                        mma_commit_pair(smem_u32(&empty_bar[s]));   // free in both CTAs
+                    }
+                    if (!ok) break;
+                    mma_commit_pair(smem_u32(&acc_full[acc]));      // both halves complete
+                }
+            }
+            mma_commit_pair_local(smem_u32(&mma_done));
+            if (!mbar_wait(smem_u32(&mma_done), 0)) atomicOr(&g_tp_status, kStatusDrain);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue (both CTAs, own rows) -----------------
+        const int e = warp - 2;
+        const int quarter = warp % 4;
+        const int group = e / 4;
+        const int row_in_tile = 32 * quarter + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
+        const uint32_t col_off = static_cast<uint32_t>(group * kEpiCols);
+        const uint32_t out_box = base + static_cast<uint32_t>(kStages * C::kStageBytes) +
+                                 static_cast<uint32_t>(e * C::kOutBox);
+        float *const *partials = p.partials;
+        const bool keep_partials = partials[0] != nullptr;
+        const size_t n = static_cast<size_t>(p.n);
+        const uint32_t leader_acc_empty[2] = {map_to_cta(smem_u32(&acc_empty[0]), 0),
+                                              map_to_cta(smem_u32(&acc_empty[1]), 0)};
+        uint32_t job = 0;
+        bool ok = true;
+        for (int g = first_group; ok && g < num_groups; g += group_stride) {
+            const int m0 = ((g / p.tiles_n) * 2 + static_cast<int>(crank)) * kBM;
+            const int n0 = (g % p.tiles_n) * BN;
+            const size_t off = static_cast<size_t>(m0 + row_in_tile) * n + n0 + col_off;
+            float sum[kEpiCols];
+            for (int r = 0; r < R; ++r, ++job) {
+                const uint32_t acc = job & 1u;
+                const bool ready = mbar_wait(smem_u32(&acc_full[acc]), (job >> 1) & 1);
+                if (!__all_sync(0xFFFFFFFFu, ready)) {
+                    if (lane == 0) atomicOr(&g_tp_status, kStatusEpilogue);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t y_addr = tmem + lane_addr + acc * kAccCols + col_off;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    uint32_t y[32];
+                    tmem_ld32(y_addr + kChunk * c, y);
+                    tmem_wait_ld();
+                    if (keep_partials) {
+                        float4 *dst = reinterpret_cast<float4 *>(partials[r] + off + kChunk * c);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_float4(__uint_as_float(y[4 * q]),
+                                                 __uint_as_float(y[4 * q + 1]),
+                                                 __uint_as_float(y[4 * q + 2]),
+                                                 __uint_as_float(y[4 * q + 3]));
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        sum[kChunk * c + i] = r == 0 ? __uint_as_float(y[i])
+                                                     : __fadd_rn(sum[kChunk * c + i],
+                                                                 __uint_as_float(y[i]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(leader_acc_empty[acc]);
+            }
+            if (!ok) break;
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < kEpiCols / 8; ++q) {
+                const uint4 pk = make_uint4(
+                    pack_bf16x2(__float_as_uint(sum[8 * q]), __float_as_uint(sum[8 * q + 1])),
+                    pack_bf16x2(__float_as_uint(sum[8 * q + 2]), __float_as_uint(sum[8 * q + 3])),
+                    pack_bf16x2(__float_as_uint(sum[8 * q + 4]), __float_as_uint(sum[8 * q + 5])),
+                    pack_bf16x2(__float_as_uint(sum[8 * q + 6]), __float_as_uint(sum[8 * q + 7])));
+                const uint32_t chunk = static_cast<uint32_t>(q) ^ static_cast<uint32_t>(lane & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                             ::"r"(out_box + static_cast<uint32_t>(lane) * 128u + chunk * 16u),
+                               "r"(pk.x), "r"(pk.y), "r"(pk.z), "r"(pk.w) : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int x = n0 + static_cast<int>(col_off);
+                const int y = m0 + 32 * quarter;
+                for (int o = 0; o < R; ++o) tma_store_2d(&p.tout[o], x, y, out_box);
+                bulk_commit_group();
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                                          // the peer is done with us
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem), "r"(kTmemCols) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Host side: tensor maps and the launch
 // ---------------------------------------------------------------------------
 
@@ -739,6 +1040,67 @@ int launch_cfg(TpFusedParams &p, const void *const *x, const void *const *w, int
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused tensor-parallel launch");
 }
 
+template <int BN>
+int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
+                int kr, int R, int max_ctas, cudaStream_t stream) {
+    static bool attr_set[kMaxDevices];
+    using C = PairCfg<BN>;
+    auto kernel = tp_fused_pair_kernel<BN>;
+    int st;
+    for (int r = 0; r < R; ++r) {
+        if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM, "x", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, C::kHalfB, "w", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tout[r], p.out[r], m, n, 32, "out", r)) != CC_OK) return st;
+    }
+    p.tiles_n = n / BN;
+    p.num_tiles = (m / kBM) * p.tiles_n;
+    const int num_groups = p.num_tiles / 2;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(CC_ERR_UNSUPPORTED, "device %d beyond the %d supported", dev, kMaxDevices);
+    if ((e = device_sm_count(&sms)) != cudaSuccess) return fail_cuda(e, "SM count");
+    {
+        std::lock_guard<std::mutex> lock(g_attr_mutex);
+        if (!attr_set[dev]) {
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::kSmemBytes);
+            if (e != cudaSuccess) return fail_cuda(e, "shared memory attribute");
+            attr_set[dev] = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = sms / 2;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    int active = 0;
+    e = cudaOccupancyMaxActiveClusters(&active, kernel, &cfg);
+    if (e != cudaSuccess) return fail_cuda(e, "cluster occupancy");
+    if (active > 0 && active < clusters) clusters = active;
+    if (max_ctas > 0 && 2 * clusters > max_ctas) clusters = max_ctas / 2;
+    if (clusters > num_groups) clusters = num_groups;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused tensor-parallel launch");
+}
+
+#ifndef CC_TP_PAIR
+#define CC_TP_PAIR 1   // 1: the pair form (cta_group::2) wherever row tiles pair up
+#endif
+
 // The cluster shape for a tile grid: pairs along M (2 x 1, sharing the W
 // tile) where the row-tile count is even, else one CTA.  Measured on the
 // GPT-2 MLP shape (R = 8, m = 8192, n = 3072, k = 12288, BN = 192): 1 x 1,
@@ -758,7 +1120,10 @@ int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int 
 template <int BN>
 int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
               int kr, int R, int max_ctas, cudaStream_t stream) {
-    if ((m / kBM) % 2 == 0) return launch_cfg<BN, 2, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
+    if ((m / kBM) % 2 == 0) {
+        if (CC_TP_PAIR) return launch_pair<BN>(p, x, w, m, n, kr, R, max_ctas, stream);
+        return launch_cfg<BN, 2, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
+    }
     return launch_cfg<BN, 1, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
 }
 #endif
