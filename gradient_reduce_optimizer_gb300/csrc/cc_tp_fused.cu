@@ -74,6 +74,10 @@ constexpr int kChunk = 32;               // TMEM columns per epilogue load
 #endif
 constexpr int kPrefetch = CC_TP_PREFETCH;
 
+#ifndef CC_TP_PAIR_BOX_COLS
+#define CC_TP_PAIR_BOX_COLS 32   // columns of the pair kernel's output staging boxes
+#endif
+
 #ifndef CC_TP_STAGE_FENCE
 #define CC_TP_STAGE_FENCE 1   // tcgen05 fence after each stage's full-barrier wait
 #endif
@@ -690,13 +694,18 @@ struct PairCfg {
     static constexpr int kStageBytes = kTileA + kTileB;
     static constexpr int kEpiWarps = 4 * (BN / kEpiCols);
     static constexpr int kThreads = 32 * (2 + kEpiWarps);
-    static constexpr int kOutBox = 32 * kEpiCols * 2;
+    // Each epilogue warp stages 32 rows x kBoxCols of bf16 output at a time
+    // (64-byte swizzle for 32 columns, 128-byte for 64), stored twice per
+    // tile with 32 columns: the smaller boxes leave room for one more stage.
+    static constexpr int kBoxCols = CC_TP_PAIR_BOX_COLS;
+    static constexpr int kOutBox = 32 * kBoxCols * 2;
     static constexpr int kOutBytes = kEpiWarps * kOutBox;
     static constexpr int kStages =
         (220 * 1024 - kOutBytes) / kStageBytes < 8 ? (220 * 1024 - kOutBytes) / kStageBytes : 8;
     static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;
     static constexpr int kChunks = kEpiCols / kChunk;
     static_assert(kTileB % 1024 == 0, "swizzle atoms");
+    static_assert(kBoxCols == 32 || kBoxCols == 64, "output boxes of 32 or 64 columns");
     // tcgen05.mma kind::f16, bf16 A and B (K-major), fp32 accumulator,
     // M = 256 (the pair), N = BN.
     static constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10)
@@ -897,27 +906,42 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
                 if (lane == 0) mbar_arrive_cluster(leader_acc_empty[acc]);
             }
             if (!ok) break;
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+            // Round the sum once to bf16 into this warp's staging box and
+            // TMA-store it to every rank's output, kBoxCols columns at a time.
+            // Swizzle: 16-byte chunk j of row i at chunk j ^ (i % 8) in
+            // 128-byte rows, j ^ ((i / 2) % 4) in 64-byte rows.
 #pragma unroll
-            for (int q = 0; q < kEpiCols / 8; ++q) {
-                const uint4 pk = make_uint4(
-                    pack_bf16x2(__float_as_uint(sum[8 * q]), __float_as_uint(sum[8 * q + 1])),
-                    pack_bf16x2(__float_as_uint(sum[8 * q + 2]), __float_as_uint(sum[8 * q + 3])),
-                    pack_bf16x2(__float_as_uint(sum[8 * q + 4]), __float_as_uint(sum[8 * q + 5])),
-                    pack_bf16x2(__float_as_uint(sum[8 * q + 6]), __float_as_uint(sum[8 * q + 7])));
-                const uint32_t chunk = static_cast<uint32_t>(q) ^ static_cast<uint32_t>(lane & 7);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                             ::"r"(out_box + static_cast<uint32_t>(lane) * 128u + chunk * 16u),
-                               "r"(pk.x), "r"(pk.y), "r"(pk.z), "r"(pk.w) : "memory");
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                const int x = n0 + static_cast<int>(col_off);
-                const int y = m0 + 32 * quarter;
-                for (int o = 0; o < R; ++o) tma_store_2d(&p.tout[o], x, y, out_box);
-                bulk_commit_group();
+            for (int h = 0; h < kEpiCols / C::kBoxCols; ++h) {
+                if (lane == 0) bulk_wait_read_all();         // the box is free again
+                __syncwarp();
+                constexpr int kq = C::kBoxCols / 8;          // 16-byte chunks per row
+#pragma unroll
+                for (int j = 0; j < kq; ++j) {
+                    const int q = h * kq + j;
+                    const uint4 pk = make_uint4(
+                        pack_bf16x2(__float_as_uint(sum[8 * q]), __float_as_uint(sum[8 * q + 1])),
+                        pack_bf16x2(__float_as_uint(sum[8 * q + 2]),
+                                    __float_as_uint(sum[8 * q + 3])),
+                        pack_bf16x2(__float_as_uint(sum[8 * q + 4]),
+                                    __float_as_uint(sum[8 * q + 5])),
+                        pack_bf16x2(__float_as_uint(sum[8 * q + 6]),
+                                    __float_as_uint(sum[8 * q + 7])));
+                    const uint32_t sw = C::kBoxCols == 64 ? static_cast<uint32_t>(lane & 7)
+                                                          : static_cast<uint32_t>((lane >> 1) & 3);
+                    const uint32_t chunk = static_cast<uint32_t>(j) ^ sw;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(out_box + static_cast<uint32_t>(lane * C::kBoxCols * 2) +
+                                       chunk * 16u),
+                                   "r"(pk.x), "r"(pk.y), "r"(pk.z), "r"(pk.w) : "memory");
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int x = n0 + static_cast<int>(col_off) + h * C::kBoxCols;
+                    const int y = m0 + 32 * quarter;
+                    for (int o = 0; o < R; ++o) tma_store_2d(&p.tout[o], x, y, out_box);
+                    bulk_commit_group();
+                }
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -956,19 +980,23 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// A bf16 row-major matrix of `rows` x `cols` (cols contiguous), read in
-// boxes of 64 columns x box_rows rows with the 128-byte swizzle.
+// A bf16 row-major matrix of `rows` x `cols` (cols contiguous), moved in
+// boxes of box_cols columns x box_rows rows: 64 columns (128 bytes) with the
+// 128-byte swizzle, or 32 columns (64 bytes) with the 64-byte swizzle.
 int encode_bf16_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows,
-                    const char *name, int r) {
+                    const char *name, int r, int box_cols = kBK) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return fail(CC_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled unavailable");
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols),
+                               static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t elem_strides[2] = {1, 1};
     const CUresult res = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr),
                             dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                           : CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (res != CUDA_SUCCESS)
         return fail(CC_ERR_INVALID, "%s[%d]: tensor map rejected (CUresult %d)", name, r,
@@ -1050,7 +1078,9 @@ int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, in
     for (int r = 0; r < R; ++r) {
         if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM, "x", r)) != CC_OK) return st;
         if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, C::kHalfB, "w", r)) != CC_OK) return st;
-        if ((st = encode_bf16_map(&p.tout[r], p.out[r], m, n, 32, "out", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tout[r], p.out[r], m, n, 32, "out", r, C::kBoxCols)) !=
+            CC_OK)
+            return st;
     }
     p.tiles_n = n / BN;
     p.num_tiles = (m / kBM) * p.tiles_n;
@@ -1128,12 +1158,16 @@ int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int 
 }
 #endif
 
-// The tile width for n output columns: 192 where it divides n (n = 3072
-// gives 16 column tiles), else 256, else 128.
-int pick_bn(int n) {
+// The tile width for n output columns.  The pair kernel prefers 256 (fewer
+// operand bytes per FLOP: 0.464 ms on the GPT-2 MLP shape against 0.478 ms
+// at 192, despite 384 tile pairs filling 76 clusters only 5.05 times); the
+// single-CTA kernel 192 (16 column tiles for n = 3072), then 256, then 128.
+int pick_bn(int n, bool pair) {
 #ifdef CC_TP_BN
+    (void)pair;
     return n % CC_TP_BN == 0 ? CC_TP_BN : 0;
 #else
+    if (pair && n % 256 == 0) return 256;
     return n % 192 == 0 ? 192 : n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 0;
 #endif
 }
@@ -1153,7 +1187,7 @@ int launch_tp_fused(const void *const *x, const void *const *w, void *const *out
     p.m = m;
     p.n = n;
     p.kb_per_rank = kr / kBK;
-    switch (pick_bn(n)) {
+    switch (pick_bn(n, CC_TP_PAIR && (m / kBM) % 2 == 0)) {
         case 128: return launch_bn<128>(p, x, w, m, n, kr, R, max_ctas, stream);
         case 192: return launch_bn<192>(p, x, w, m, n, kr, R, max_ctas, stream);
         case 256: return launch_bn<256>(p, x, w, m, n, kr, R, max_ctas, stream);
@@ -1162,7 +1196,7 @@ int launch_tp_fused(const void *const *x, const void *const *w, void *const *out
 }
 
 bool tp_fused_shape_ok(int m, int n, int kr) {
-    return m % kBM == 0 && kr % kBK == 0 && pick_bn(n) != 0;
+    return m % kBM == 0 && kr % kBK == 0 && pick_bn(n, false) != 0;
 }
 
 

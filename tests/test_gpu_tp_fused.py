@@ -61,11 +61,14 @@ def exact_products(x, w):
 
 # (R, m, n, k): one tile; several tiles and k-blocks; more tiles than SMs
 # with an odd R (the two accumulators alternate across tiles); the widest R.
-# Tile widths 128, 256, 256, 192, 256, 192; the default cluster shapes (CTA
-# pairs sharing the W tile by multicast) 1x1, 2x1, 2x1, 2x1, 1x1, 1x1.  The
-# 1x2 and 2x2 shapes are built for sweeps (CC_TP_CLUSTER_M/N).
+# Where the row tiles pair up, the pair kernel (one MMA over two SMs); else
+# the single-CTA kernel.  Single 128, pair 256, pair 256, pair 192, single
+# 256, single 192, pair 128 (tile widths).  The single-CTA kernel's cluster
+# shapes with multicast (1x2, 2x1, 2x2) are built for sweeps
+# (CC_TP_PAIR=0, CC_TP_CLUSTER_M/N).
 SHAPES = [(1, 128, 128, 64), (2, 256, 256, 256), (3, 2560, 1280, 192),
-          (8, 256, 384, 1024), (16, 128, 256, 1024), (2, 384, 768, 128)]
+          (8, 256, 384, 1024), (16, 128, 256, 1024), (2, 384, 768, 128),
+          (4, 512, 640, 256)]
 
 
 @pytest.mark.parametrize("R,m,n,k", SHAPES)
