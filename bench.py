@@ -978,32 +978,40 @@ def run_tp_fused(args, dev, x, w, outs, R, m, n, k, sequential_ms=None, reps=20)
     kr = k // R
     wt = [wr.view(kr, n).t().contiguous() for wr in w]
     stream = torch.cuda.current_stream()
+    ws_bytes = capi.cc_tp_matmul_allreduce_workspace(m, n, k, R)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
-    def call():
-        capi.cc_tp_matmul_allreduce(x, wt, outs, None, m, n, k, R, stream=stream)
+    def timed(call):
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
 
-    for _ in range(max(3, args.warmup)):
-        call()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / reps
+    # the last wave split over every CTA pair (the workspace form), and
+    # every group of output tiles whole (no workspace)
+    ms = timed(lambda: capi.cc_tp_matmul_allreduce_ex(x, wt, outs, None, m, n, k, R, ws,
+                                                      ws_bytes, 0, stream=stream))
+    ms_whole = timed(lambda: capi.cc_tp_matmul_allreduce(x, wt, outs, None, m, n, k, R,
+                                                         stream=stream))
     status = capi.cc_device_status(clear=True)
     tflops = 2 * m * n * k / (ms * 1e-3) / 1e12
     bf16_peak = measured_bf16_peak()
-    out = {"kernel": "tp_fused_kernel (tcgen05, TMA, TMEM accumulators)",
+    out = {"kernel": "tp_fused_pair_kernel (tcgen05 cta_group::2, TMA, TMEM accumulators)",
            "ms": round(ms, 4), "tflops": round(tflops, 1),
            "frac_of_measured_bf16": round(tflops / bf16_peak, 3) if bf16_peak else None,
+           "workspace_bytes": ws_bytes, "ms_without_workspace": round(ms_whole, 4),
            "hbm_bytes_algorithmic": 2 * (m * k + n * k) + 2 * R * m * n,
-           "status_word": status, "launches": reps}
+           "status_word": status, "launches": 2 * reps}
     if sequential_ms:
         out["speedup_vs_cublas_then_allreduce"] = round(sequential_ms / ms, 3)
-    del wt
+    del wt, ws
     return out
 
 

@@ -113,6 +113,9 @@ _SIGNATURES = {
     "cc_fused_dp_rank_step": ([_vp, _vp, _vp, _vp, _vp, _sz, _i, _f, _f, _f, _f, _f,
                                _i, _f, _vp], _i),
     "cc_tp_matmul_allreduce": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "cc_tp_matmul_allreduce_ex": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _i, _vp],
+                                  _i),
+    "cc_tp_matmul_allreduce_workspace": ([_i, _i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "cc_inject_bulk_stall": ([ctypes.c_longlong, ctypes.c_uint], _i),
     "cc_inject_launch_failure": ([_i], _i),
     "cc_tp_overlap_bench": ([ctypes.POINTER(cc_tp_cfg), ctypes.POINTER(cc_tp_result)], _i),
@@ -407,6 +410,27 @@ def cc_tp_matmul_allreduce(x, w, out, partials, m: int, n: int, k: int, R: int,
         _addr_array(x), _addr_array(w), _addr_array(out),
         _addr_array(partials) if partials is not None else None, m, n, k, R,
         _stream(stream)), "cc_tp_matmul_allreduce")
+
+
+def cc_tp_matmul_allreduce_ex(x, w, out, partials, m: int, n: int, k: int, R: int,
+                              workspace=None, workspace_bytes: int = 0, max_ctas: int = 0,
+                              stream=None) -> None:
+    """cc_tp_matmul_allreduce with a workspace (a device tensor, or None) in
+    which the last wave's groups may be split, and a CTA budget (0: all)."""
+    _check(lib().cc_tp_matmul_allreduce_ex(
+        _addr_array(x), _addr_array(w), _addr_array(out),
+        _addr_array(partials) if partials is not None else None, m, n, k, R,
+        _addr(workspace) if workspace is not None else None, workspace_bytes, max_ctas,
+        _stream(stream)), "cc_tp_matmul_allreduce_ex")
+
+
+def cc_tp_matmul_allreduce_workspace(m: int, n: int, k: int, R: int, max_ctas: int = 0) -> int:
+    """Workspace bytes cc_tp_matmul_allreduce_ex uses for this shape and CTA
+    budget on the current device (0: it splits nothing)."""
+    out = _sz(0)
+    _check(lib().cc_tp_matmul_allreduce_workspace(m, n, k, R, max_ctas, ctypes.byref(out)),
+           "cc_tp_matmul_allreduce_workspace")
+    return out.value
 
 
 def cc_inject_launch_failure(after_launches: int) -> None:

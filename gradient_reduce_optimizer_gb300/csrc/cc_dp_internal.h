@@ -81,11 +81,15 @@ void arm_bulk_stall(long long tile, unsigned long long timeout_ns);
 cudaError_t read_bulk_status(unsigned *status, bool clear);
 
 // The fused tensor-parallel MatMul + AllReduce (cc_tp_fused.cu) on shapes
-// already validated; max_ctas > 0 caps the persistent grid.  Returns a
-// cc_status (the reason recorded with fail()).
+// already validated; max_ctas > 0 caps the persistent grid; ws (ws_bytes,
+// at least tp_fused_workspace's figure) lets the last wave be split, NULL
+// keeps it whole.  Returns a cc_status (the reason recorded with fail()).
 int launch_tp_fused(const void *const *x, const void *const *w, void *const *out,
                     float *const *partials, int m, int n, int k, int R, int max_ctas,
-                    cudaStream_t stream);
+                    void *ws, size_t ws_bytes, cudaStream_t stream);
+// Workspace bytes launch_tp_fused uses on the current device for this shape
+// and CTA cap (0: it splits nothing).
+int tp_fused_workspace(int m, int n, int R, int max_ctas, size_t *bytes);
 // Whether the fused kernel tiles m x n with k/R per rank: m % 128 == 0,
 // (k/R) % 64 == 0, and n a multiple of 128 or 192.
 bool tp_fused_shape_ok(int m, int n, int kr);

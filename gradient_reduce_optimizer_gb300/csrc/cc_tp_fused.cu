@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 #include <vector>
@@ -124,6 +125,41 @@ struct TpFusedParams {
     float *partials[CC_MAX_R];    // m x n each, or all null
     int R, m, n, kb_per_rank;     // kb_per_rank = (k/R) / 64
     int tiles_n, num_tiles;
+    // The pair kernel's last wave, balanced: groups [full_groups, all) are
+    // cut into their R rank phases, spread over every cluster; each phase's
+    // product goes to tail_ws as fp32 and the last phase of a group to
+    // finish (tail_count) sums them in rank order.  tail_phases = 0: none.
+    float *tail_ws;
+    unsigned *tail_count;
+    int full_groups, tail_phases;
+};
+
+// The (group, rank) phases one cluster works through, numbered 0, 1, ...:
+// first its whole groups (every rank of group first, then first + stride,
+// ...), then its share of the split groups' single phases (q = first,
+// first + stride, ... of full_groups * R + q).  Kept as one counter so that
+// the schedule costs the epilogue no registers.
+struct Phases {
+    int first, stride, whole_jobs, jobs;
+    __device__ Phases(const TpFusedParams &p, int first_, int stride_)
+        : first(first_), stride(stride_) {
+        const int whole = p.full_groups > first ? (p.full_groups - first + stride - 1) / stride : 0;
+        const int split = p.tail_phases > first ? (p.tail_phases - first + stride - 1) / stride : 0;
+        whole_jobs = whole * p.R;
+        jobs = whole_jobs + split;
+    }
+    // group g and rank r of job j; whether the group is split
+    __device__ bool at(const TpFusedParams &p, int j, int &g, int &r) const {
+        if (j < whole_jobs) {
+            g = first + (j / p.R) * stride;
+            r = j % p.R;
+            return false;
+        }
+        const int q = first + (j - whole_jobs) * stride;
+        g = p.full_groups + q / p.R;
+        r = q % p.R;
+        return true;
+    }
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -713,18 +749,136 @@ struct PairCfg {
                                          | (static_cast<uint32_t>(256 >> 4) << 24);
 };
 
+// Columns 4q .. 4q+3 of a TMEM load as a float4.
+__device__ __forceinline__ float4 quad(const uint32_t (&y)[32], int q) {
+    return make_float4(__uint_as_float(y[4 * q]), __uint_as_float(y[4 * q + 1]),
+                       __uint_as_float(y[4 * q + 2]), __uint_as_float(y[4 * q + 3]));
+}
+
+// Round 64 running sums of one row to bf16 into this warp's staging box and
+// TMA-store it to every rank's output, kBoxCols columns at a time.  Swizzle:
+// 16-byte chunk j of row i at chunk j ^ (i % 8) in 128-byte rows, j ^ ((i /
+// 2) % 4) in 64-byte rows.
+template <int kBoxCols>
+__device__ __forceinline__ void store_sums_bf16(const float (&sum)[kEpiCols], int lane,
+                                                uint32_t out_box, const CUtensorMap *tout,
+                                                int R, int x0, int y) {
+#pragma unroll
+    for (int h = 0; h < kEpiCols / kBoxCols; ++h) {
+        if (lane == 0) bulk_wait_read_all();         // the box is free again
+        __syncwarp();
+        constexpr int kq = kBoxCols / 8;             // 16-byte chunks per row
+#pragma unroll
+        for (int j = 0; j < kq; ++j) {
+            const int q = h * kq + j;
+            const uint4 pk = make_uint4(
+                pack_bf16x2(__float_as_uint(sum[8 * q]), __float_as_uint(sum[8 * q + 1])),
+                pack_bf16x2(__float_as_uint(sum[8 * q + 2]), __float_as_uint(sum[8 * q + 3])),
+                pack_bf16x2(__float_as_uint(sum[8 * q + 4]), __float_as_uint(sum[8 * q + 5])),
+                pack_bf16x2(__float_as_uint(sum[8 * q + 6]), __float_as_uint(sum[8 * q + 7])));
+            const uint32_t sw = kBoxCols == 64 ? static_cast<uint32_t>(lane & 7)
+                                               : static_cast<uint32_t>((lane >> 1) & 3);
+            const uint32_t chunk = static_cast<uint32_t>(j) ^ sw;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         ::"r"(out_box + static_cast<uint32_t>(lane * kBoxCols * 2) + chunk * 16u),
+                           "r"(pk.x), "r"(pk.y), "r"(pk.z), "r"(pk.w) : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            for (int o = 0; o < R; ++o) tma_store_2d(&tout[o], x0 + h * kBoxCols, y, out_box);
+            bulk_commit_group();
+        }
+    }
+}
+
+#ifndef CC_TP_FIXUP_RANKS
+#define CC_TP_FIXUP_RANKS 1   // ranks' loads in flight per thread in a fixup
+#endif
+
+// The fixup of a split group: this thread's 64 output columns of one row
+// are the rank-order sums of the R fp32 products in the workspace (slot r at
+// slot0 + r * rank_stride float4s; column quad c of the row at c * 128).
+// Sixteen columns at a time, with up to four ranks' loads in flight, packed
+// to bf16 straight into the warp's staging box and TMA-stored to every
+// rank's output as store_sums_bf16 does.
+template <int kBoxCols>
+__device__ __forceinline__ void fixup_store_bf16(const float4 *slot0, size_t rank_stride, int lane,
+                                                 uint32_t out_box, const CUtensorMap *tout,
+                                                 int R, int x0, int y) {
+    constexpr int kRanksInFlight = CC_TP_FIXUP_RANKS;
+#pragma unroll 1
+    for (int h = 0; h < kEpiCols / kBoxCols; ++h) {
+        if (lane == 0) bulk_wait_read_all();         // the box is free again
+        __syncwarp();
+#pragma unroll 1
+        for (int part = 0; part < kBoxCols / 16; ++part) {
+            const float4 *base = slot0 + static_cast<size_t>(h * kBoxCols / 4 + part * 4) * kBM;
+            float acc[16];
+#pragma unroll 1
+            for (int r0 = 0; r0 < R; r0 += kRanksInFlight) {
+                float4 v[kRanksInFlight][4];
+#pragma unroll
+                for (int i = 0; i < kRanksInFlight; ++i)
+                    if (r0 + i < R) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            v[i][q] = __ldcg(base + (r0 + i) * rank_stride + q * kBM);
+                    }
+#pragma unroll
+                for (int i = 0; i < kRanksInFlight; ++i)
+                    if (r0 + i < R) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float e4[4] = {v[i][q].x, v[i][q].y, v[i][q].z, v[i][q].w};
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                acc[4 * q + c] = r0 + i == 0 ? e4[c]
+                                                             : __fadd_rn(acc[4 * q + c], e4[c]);
+                        }
+                    }
+            }
+            const uint32_t sw = kBoxCols == 64 ? static_cast<uint32_t>(lane & 7)
+                                               : static_cast<uint32_t>((lane >> 1) & 3);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const uint32_t chunk = static_cast<uint32_t>(part * 2 + jj) ^ sw;
+                const float *a = acc + 8 * jj;
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                             ::"r"(out_box + static_cast<uint32_t>(lane * kBoxCols * 2) +
+                                   chunk * 16u),
+                               "r"(pack_bf16x2(__float_as_uint(a[0]), __float_as_uint(a[1]))),
+                               "r"(pack_bf16x2(__float_as_uint(a[2]), __float_as_uint(a[3]))),
+                               "r"(pack_bf16x2(__float_as_uint(a[4]), __float_as_uint(a[5]))),
+                               "r"(pack_bf16x2(__float_as_uint(a[6]), __float_as_uint(a[7])))
+                             : "memory");
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            for (int o = 0; o < R; ++o) tma_store_2d(&tout[o], x0 + h * kBoxCols, y, out_box);
+            bulk_commit_group();
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(PairCfg<BN>::kThreads, 1)
 tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
     using C = PairCfg<BN>;
     constexpr int kStages = C::kStages;
+    constexpr int kSlotFloats = kBM * BN;                  // one CTA's half of a tile
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kStages];    // the leader's is used
     __shared__ __align__(8) uint64_t empty_bar[kStages];
     __shared__ __align__(8) uint64_t acc_full[2];
     __shared__ __align__(8) uint64_t acc_empty[2];         // the leader's is used
     __shared__ __align__(8) uint64_t mma_done;
+    __shared__ __align__(8) uint64_t tail_in;              // epilogue warps wrote a phase
+    __shared__ __align__(8) uint64_t tail_out;             // ... and whether it was the last
     __shared__ uint32_t tmem_base_slot;
+    __shared__ int tail_last;
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -745,6 +899,8 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
             mbar_init(smem_u32(&acc_empty[a]), 2 * C::kEpiWarps);
         }
         mbar_init(smem_u32(&mma_done), 1);
+        mbar_init(smem_u32(&tail_in), C::kEpiWarps);
+        mbar_init(smem_u32(&tail_out), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     cluster_sync();                                          // the pair's barriers exist
@@ -765,8 +921,7 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_slot;
-    // Pairs of row tiles, one pair per cluster at a time.
-    const int num_groups = (p.num_tiles / p.tiles_n / 2) * p.tiles_n;
+    // Pairs of row tiles ("groups"), one pair per cluster at a time.
     const int first_group = static_cast<int>(blockIdx.x) / 2;
     const int group_stride = static_cast<int>(gridDim.x) / 2;
 
@@ -777,27 +932,28 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
             for (int s = 0; s < kStages; ++s) issued_use[s] = -1;
             uint32_t it = 0;
             bool ok = true;
-            for (int g = first_group; ok && g < num_groups; g += group_stride) {
+            const Phases ph(p, first_group, group_stride);
+            for (int j = 0; ok && j < ph.jobs; ++j) {
+                int g, r;
+                ph.at(p, j, g, r);
                 const int m0 = ((g / p.tiles_n) * 2 + static_cast<int>(crank)) * kBM;
                 const int n0 = (g % p.tiles_n) * BN;
-                for (int r = 0; ok && r < R; ++r) {
-                    for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
-                        const int s = static_cast<int>(it % kStages);
-                        const int use = static_cast<int>(it / kStages);
-                        if (use > 0 && !mbar_wait(smem_u32(&empty_bar[s]), (use - 1) & 1)) {
-                            atomicOr(&g_tp_status, kStatusProducer);
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
-                        const uint32_t leader_full = map_to_cta(smem_u32(&full_bar[s]), 0);
-                        if (leader)   // both CTAs' bytes land before the stage is full
-                            mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * C::kStageBytes);
-                        tma_load_2d_pair(sa, &p.tx[r], kb * kBK, m0, leader_full);
-                        tma_load_2d_pair(sa + kTileA, &p.tw[r], kb * kBK,
-                                         n0 + static_cast<int>(crank) * C::kHalfB, leader_full);
-                        issued_use[s] = use;
+                for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
+                    const int s = static_cast<int>(it % kStages);
+                    const int use = static_cast<int>(it / kStages);
+                    if (use > 0 && !mbar_wait(smem_u32(&empty_bar[s]), (use - 1) & 1)) {
+                        atomicOr(&g_tp_status, kStatusProducer);
+                        ok = false;
+                        break;
                     }
+                    const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
+                    const uint32_t leader_full = map_to_cta(smem_u32(&full_bar[s]), 0);
+                    if (leader)   // both CTAs' bytes land before the stage is full
+                        mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * C::kStageBytes);
+                    tma_load_2d_pair(sa, &p.tx[r], kb * kBK, m0, leader_full);
+                    tma_load_2d_pair(sa + kTileA, &p.tw[r], kb * kBK,
+                                     n0 + static_cast<int>(crank) * C::kHalfB, leader_full);
+                    issued_use[s] = use;
                 }
             }
             // The leader's MMAs have read every stage this CTA filled (and so
@@ -811,39 +967,38 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
     } else if (warp == 1) {
         // ---------------- MMA issuer (the leader only) ------------------
         if (leader && lane == 0) {
-            uint32_t it = 0, job = 0;
+            uint32_t it = 0;
             bool ok = true;
-            for (int g = first_group; ok && g < num_groups; g += group_stride) {
-                for (int r = 0; ok && r < R; ++r, ++job) {
-                    const uint32_t acc = job & 1u;
-                    const uint32_t acc_use = job >> 1;
-                    if (acc_use > 0 && !mbar_wait(smem_u32(&acc_empty[acc]), (acc_use - 1) & 1)) {
+            const Phases ph(p, first_group, group_stride);
+            for (uint32_t job = 0; ok && job < static_cast<uint32_t>(ph.jobs); ++job) {
+                const uint32_t acc = job & 1u;
+                const uint32_t acc_use = job >> 1;
+                if (acc_use > 0 && !mbar_wait(smem_u32(&acc_empty[acc]), (acc_use - 1) & 1)) {
+                    atomicOr(&g_tp_status, kStatusMma);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * kAccCols;
+                for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
+                    const int s = static_cast<int>(it % kStages);
+                    const int use = static_cast<int>(it / kStages);
+                    if (!mbar_wait(smem_u32(&full_bar[s]), use & 1)) {
                         atomicOr(&g_tp_status, kStatusMma);
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem + acc * kAccCols;
-                    for (int kb = 0; kb < kb_per_rank; ++kb, ++it) {
-                        const int s = static_cast<int>(it % kStages);
-                        const int use = static_cast<int>(it / kStages);
-                        if (!mbar_wait(smem_u32(&full_bar[s]), use & 1)) {
-                            atomicOr(&g_tp_status, kStatusMma);
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
-                        const uint64_t da = smem_desc_sw128(sa);
-                        const uint64_t db = smem_desc_sw128(sa + kTileA);
+                    const uint32_t sa = base + static_cast<uint32_t>(s) * C::kStageBytes;
+                    const uint64_t da = smem_desc_sw128(sa);
+                    const uint64_t db = smem_desc_sw128(sa + kTileA);
 #pragma unroll
-                        for (int j = 0; j < kBK / kUmmaK; ++j)
-                            mma_bf16_pair(d_tmem, da + 2u * j, db + 2u * j, C::kInstrDesc,
-                                          (kb > 0 || j > 0) ? 1u : 0u);
-                        mma_commit_pair(smem_u32(&empty_bar[s]));   // free in both CTAs
-                    }
-                    if (!ok) break;
-                    mma_commit_pair(smem_u32(&acc_full[acc]));      // both halves complete
+                    for (int j = 0; j < kBK / kUmmaK; ++j)
+                        mma_bf16_pair(d_tmem, da + 2u * j, db + 2u * j, C::kInstrDesc,
+                                      (kb > 0 || j > 0) ? 1u : 0u);
+                    mma_commit_pair(smem_u32(&empty_bar[s]));   // free in both CTAs
                 }
+                if (!ok) break;
+                mma_commit_pair(smem_u32(&acc_full[acc]));      // both halves complete
             }
             mma_commit_pair_local(smem_u32(&mma_done));
             if (!mbar_wait(smem_u32(&mma_done), 0)) atomicOr(&g_tp_status, kStatusDrain);
@@ -864,23 +1019,43 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
         const size_t n = static_cast<size_t>(p.n);
         const uint32_t leader_acc_empty[2] = {map_to_cta(smem_u32(&acc_empty[0]), 0),
                                               map_to_cta(smem_u32(&acc_empty[1]), 0)};
-        uint32_t job = 0;
+        // A tail slot holds one CTA's 128 x BN fp32 product as BN / 4 column
+        // quads, each 128 rows of float4: a warp's lanes (rows) touch 512
+        // consecutive bytes.  This thread's first quad:
+        const size_t slot_off = (static_cast<size_t>(col_off / 4) * kBM + row_in_tile) * 4;
+        const Phases ph(p, first_group, group_stride);
         bool ok = true;
-        for (int g = first_group; ok && g < num_groups; g += group_stride) {
-            const int m0 = ((g / p.tiles_n) * 2 + static_cast<int>(crank)) * kBM;
-            const int n0 = (g % p.tiles_n) * BN;
-            const size_t off = static_cast<size_t>(m0 + row_in_tile) * n + n0 + col_off;
+        int job = 0;
+        // Wait for job j's accumulator; its TMEM address (this warp's lanes
+        // and columns), or false if the wait ran out.
+        auto wait_acc = [&](int j, uint32_t &y_addr) {
+            const uint32_t acc = static_cast<uint32_t>(j) & 1u;
+            const bool ready = mbar_wait(smem_u32(&acc_full[acc]), (j >> 1) & 1);
+            if (!__all_sync(0xFFFFFFFFu, ready)) {
+                if (lane == 0) atomicOr(&g_tp_status, kStatusEpilogue);
+                return false;
+            }
+            tc_fence_after();
+            y_addr = tmem + lane_addr + acc * kAccCols + col_off;
+            return true;
+        };
+        auto release_acc = [&](int j) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_acc_empty[j & 1]);
+        };
+        {
+            // Whole groups: the running sum over the R ranks in registers,
+            // stored once the last rank is in.
             float sum[kEpiCols];
-            for (int r = 0; r < R; ++r, ++job) {
-                const uint32_t acc = job & 1u;
-                const bool ready = mbar_wait(smem_u32(&acc_full[acc]), (job >> 1) & 1);
-                if (!__all_sync(0xFFFFFFFFu, ready)) {
-                    if (lane == 0) atomicOr(&g_tp_status, kStatusEpilogue);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t y_addr = tmem + lane_addr + acc * kAccCols + col_off;
+            for (; ok && job < ph.whole_jobs; ++job) {
+                int g, r;
+                ph.at(p, job, g, r);
+                const int m0 = ((g / p.tiles_n) * 2 + static_cast<int>(crank)) * kBM;
+                const int n0 = (g % p.tiles_n) * BN;
+                const size_t off = static_cast<size_t>(m0 + row_in_tile) * n + n0 + col_off;
+                uint32_t y_addr;
+                if (!(ok = wait_acc(job, y_addr))) break;
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c) {
                     uint32_t y[32];
@@ -889,11 +1064,7 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
                     if (keep_partials) {
                         float4 *dst = reinterpret_cast<float4 *>(partials[r] + off + kChunk * c);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_float4(__uint_as_float(y[4 * q]),
-                                                 __uint_as_float(y[4 * q + 1]),
-                                                 __uint_as_float(y[4 * q + 2]),
-                                                 __uint_as_float(y[4 * q + 3]));
+                        for (int q = 0; q < 8; ++q) dst[q] = quad(y, q);
                     }
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -901,48 +1072,70 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
                                                      : __fadd_rn(sum[kChunk * c + i],
                                                                  __uint_as_float(y[i]));
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(leader_acc_empty[acc]);
+                release_acc(job);
+                if (r == R - 1)
+                    store_sums_bf16<C::kBoxCols>(sum, lane, out_box, p.tout, R,
+                                                 n0 + static_cast<int>(col_off), m0 + 32 * quarter);
             }
-            if (!ok) break;
-            // Round the sum once to bf16 into this warp's staging box and
-            // TMA-store it to every rank's output, kBoxCols columns at a time.
-            // Swizzle: 16-byte chunk j of row i at chunk j ^ (i % 8) in
-            // 128-byte rows, j ^ ((i / 2) % 4) in 64-byte rows.
+        }
+        // Split groups: each phase's product, as is, to its workspace slot;
+        // the group's last phase to finish (an atomic ticket per group half)
+        // sums the R slots in rank order.  No CTA waits for another: only
+        // this CTA's epilogue warps meet, on bounded waits.
+        uint32_t tail_parity = 0;
+        for (; ok && job < ph.jobs; ++job) {
+            int g, r;
+            ph.at(p, job, g, r);
+            const int tg = g - p.full_groups;
+            const int m0 = ((g / p.tiles_n) * 2 + static_cast<int>(crank)) * kBM;
+            const int n0 = (g % p.tiles_n) * BN;
+            const size_t off = static_cast<size_t>(m0 + row_in_tile) * n + n0 + col_off;
+            const float *slots = p.tail_ws + static_cast<size_t>(tg) * R * 2 * kSlotFloats +
+                                 static_cast<size_t>(crank) * kSlotFloats + slot_off;
+            float *slot = const_cast<float *>(slots) + static_cast<size_t>(r) * 2 * kSlotFloats;
+            uint32_t y_addr;
+            if (!(ok = wait_acc(job, y_addr))) break;
 #pragma unroll
-            for (int h = 0; h < kEpiCols / C::kBoxCols; ++h) {
-                if (lane == 0) bulk_wait_read_all();         // the box is free again
-                __syncwarp();
-                constexpr int kq = C::kBoxCols / 8;          // 16-byte chunks per row
+            for (int c = 0; c < C::kChunks; ++c) {
+                uint32_t y[32];
+                tmem_ld32(y_addr + kChunk * c, y);
+                tmem_wait_ld();
+                if (keep_partials) {
+                    float4 *dst = reinterpret_cast<float4 *>(partials[r] + off + kChunk * c);
 #pragma unroll
-                for (int j = 0; j < kq; ++j) {
-                    const int q = h * kq + j;
-                    const uint4 pk = make_uint4(
-                        pack_bf16x2(__float_as_uint(sum[8 * q]), __float_as_uint(sum[8 * q + 1])),
-                        pack_bf16x2(__float_as_uint(sum[8 * q + 2]),
-                                    __float_as_uint(sum[8 * q + 3])),
-                        pack_bf16x2(__float_as_uint(sum[8 * q + 4]),
-                                    __float_as_uint(sum[8 * q + 5])),
-                        pack_bf16x2(__float_as_uint(sum[8 * q + 6]),
-                                    __float_as_uint(sum[8 * q + 7])));
-                    const uint32_t sw = C::kBoxCols == 64 ? static_cast<uint32_t>(lane & 7)
-                                                          : static_cast<uint32_t>((lane >> 1) & 3);
-                    const uint32_t chunk = static_cast<uint32_t>(j) ^ sw;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(out_box + static_cast<uint32_t>(lane * C::kBoxCols * 2) +
-                                       chunk * 16u),
-                                   "r"(pk.x), "r"(pk.y), "r"(pk.z), "r"(pk.w) : "memory");
+                    for (int q = 0; q < 8; ++q) dst[q] = quad(y, q);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int x = n0 + static_cast<int>(col_off) + h * C::kBoxCols;
-                    const int y = m0 + 32 * quarter;
-                    for (int o = 0; o < R; ++o) tma_store_2d(&p.tout[o], x, y, out_box);
-                    bulk_commit_group();
-                }
+                float4 *dst = reinterpret_cast<float4 *>(slot) + (kChunk / 4) * c * kBM;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dst[q * kBM] = quad(y, q);
             }
+            release_acc(job);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tail_in));
+            if (e == 0 && lane == 0) {
+                int last = 0;
+                if (mbar_wait(smem_u32(&tail_in), tail_parity)) {
+                    const unsigned ticket = atomicAdd(&p.tail_count[tg * 2 + crank], 1u);
+                    last = ticket == static_cast<unsigned>(R - 1);
+                    __threadfence();
+                } else {
+                    atomicOr(&g_tp_status, kStatusEpilogue);
+                }
+                tail_last = last;
+                mbar_arrive(smem_u32(&tail_out));
+            }
+            const bool told = mbar_wait(smem_u32(&tail_out), tail_parity);
+            tail_parity ^= 1u;
+            if (!__all_sync(0xFFFFFFFFu, told)) {
+                if (lane == 0) atomicOr(&g_tp_status, kStatusEpilogue);
+                ok = false;
+                break;
+            }
+            if (tail_last)
+                fixup_store_bf16<C::kBoxCols>(reinterpret_cast<const float4 *>(slots),
+                                              2 * kSlotFloats / 4, lane, out_box, p.tout, R,
+                                              n0 + static_cast<int>(col_off), m0 + 32 * quarter);
         }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -1068,23 +1261,27 @@ int launch_cfg(TpFusedParams &p, const void *const *x, const void *const *w, int
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused tensor-parallel launch");
 }
 
+// Bytes of the tail workspace before the slots: one arrival counter per
+// (split group, CTA of the pair), rounded up to 256.
+size_t tail_counter_bytes(int tail_groups) {
+    return (static_cast<size_t>(tail_groups) * 2 * sizeof(unsigned) + 255) / 256 * 256;
+}
+
+// The pair kernel's schedule: how many clusters run, and which groups are
+// split into rank phases.  The last wave is split when its groups do not
+// fill every cluster and splitting shortens it: ceil(tail * R / clusters)
+// phases per cluster instead of R (so never for R = 1).
+struct PairPlan {
+    int clusters, full_groups, tail_phases;
+    size_t ws_bytes;                                     // 0: nothing split
+};
+
 template <int BN>
-int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
-                int kr, int R, int max_ctas, cudaStream_t stream) {
+int pair_plan(int m, int n, int R, int max_ctas, bool split, PairPlan *plan) {
     static bool attr_set[kMaxDevices];
     using C = PairCfg<BN>;
     auto kernel = tp_fused_pair_kernel<BN>;
-    int st;
-    for (int r = 0; r < R; ++r) {
-        if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM, "x", r)) != CC_OK) return st;
-        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, C::kHalfB, "w", r)) != CC_OK) return st;
-        if ((st = encode_bf16_map(&p.tout[r], p.out[r], m, n, 32, "out", r, C::kBoxCols)) !=
-            CC_OK)
-            return st;
-    }
-    p.tiles_n = n / BN;
-    p.num_tiles = (m / kBM) * p.tiles_n;
-    const int num_groups = p.num_tiles / 2;
+    const int num_groups = (m / kBM / 2) * (n / BN);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
@@ -1104,7 +1301,6 @@ int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, in
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -1119,10 +1315,67 @@ int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, in
     if (e != cudaSuccess) return fail_cuda(e, "cluster occupancy");
     if (active > 0 && active < clusters) clusters = active;
     if (max_ctas > 0 && 2 * clusters > max_ctas) clusters = max_ctas / 2;
-    if (clusters > num_groups) clusters = num_groups;
     if (clusters < 1) clusters = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    e = cudaLaunchKernelEx(&cfg, kernel, p);
+    const int tail = num_groups % clusters;
+    if (split && tail > 0 && tail * R <= (R - 1) * clusters) {
+        plan->full_groups = num_groups - tail;
+        plan->tail_phases = tail * R;
+        plan->clusters = plan->full_groups > 0 ? clusters : std::min(clusters, tail * R);
+        plan->ws_bytes = tail_counter_bytes(tail) +
+                         static_cast<size_t>(tail) * R * 2 * kBM * BN * sizeof(float);
+    } else {
+        plan->full_groups = num_groups;
+        plan->tail_phases = 0;
+        plan->clusters = std::min(clusters, num_groups);
+        plan->ws_bytes = 0;
+    }
+    return CC_OK;
+}
+
+template <int BN>
+int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
+                int kr, int R, int max_ctas, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    using C = PairCfg<BN>;
+    int st;
+    for (int r = 0; r < R; ++r) {
+        if ((st = encode_bf16_map(&p.tx[r], x[r], m, kr, kBM, "x", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tw[r], w[r], n, kr, C::kHalfB, "w", r)) != CC_OK) return st;
+        if ((st = encode_bf16_map(&p.tout[r], p.out[r], m, n, 32, "out", r, C::kBoxCols)) !=
+            CC_OK)
+            return st;
+    }
+    p.tiles_n = n / BN;
+    p.num_tiles = (m / kBM) * p.tiles_n;
+    PairPlan plan;
+    if ((st = pair_plan<BN>(m, n, R, max_ctas, ws != nullptr, &plan)) != CC_OK) return st;
+    p.full_groups = plan.full_groups;
+    p.tail_phases = plan.tail_phases;
+    cudaError_t e;
+    if (plan.tail_phases > 0) {
+        if (ws_bytes < plan.ws_bytes)
+            return fail(CC_ERR_INVALID, "workspace of %zu bytes, this shape needs %zu", ws_bytes,
+                        plan.ws_bytes);
+        const int tail_groups = plan.tail_phases / R;
+        p.tail_count = static_cast<unsigned *>(ws);
+        p.tail_ws = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) +
+                                              tail_counter_bytes(tail_groups));
+        e = cudaMemsetAsync(ws, 0, static_cast<size_t>(tail_groups) * 2 * sizeof(unsigned),
+                            stream);
+        if (e != cudaSuccess) return fail_cuda(e, "tail counters");
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * plan.clusters));
+    e = cudaLaunchKernelEx(&cfg, tp_fused_pair_kernel<BN>, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused tensor-parallel launch");
 }
@@ -1140,7 +1393,7 @@ int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, in
 #if defined(CC_TP_CLUSTER_M) && defined(CC_TP_CLUSTER_N)
 template <int BN>
 int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
-              int kr, int R, int max_ctas, cudaStream_t stream) {
+              int kr, int R, int max_ctas, void *, size_t, cudaStream_t stream) {
     if ((m / kBM) % CC_TP_CLUSTER_M != 0 || (n / BN) % CC_TP_CLUSTER_N != 0)
         return launch_cfg<BN, 1, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
     return launch_cfg<BN, CC_TP_CLUSTER_M, CC_TP_CLUSTER_N>(p, x, w, m, n, kr, R, max_ctas,
@@ -1149,9 +1402,10 @@ int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int 
 #else
 template <int BN>
 int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int m, int n,
-              int kr, int R, int max_ctas, cudaStream_t stream) {
+              int kr, int R, int max_ctas, void *ws, size_t ws_bytes, cudaStream_t stream) {
     if ((m / kBM) % 2 == 0) {
-        if (CC_TP_PAIR) return launch_pair<BN>(p, x, w, m, n, kr, R, max_ctas, stream);
+        if (CC_TP_PAIR)
+            return launch_pair<BN>(p, x, w, m, n, kr, R, max_ctas, ws, ws_bytes, stream);
         return launch_cfg<BN, 2, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
     }
     return launch_cfg<BN, 1, 1>(p, x, w, m, n, kr, R, max_ctas, stream);
@@ -1176,7 +1430,7 @@ int pick_bn(int n, bool pair) {
 
 int launch_tp_fused(const void *const *x, const void *const *w, void *const *out,
                     float *const *partials, int m, int n, int k, int R, int max_ctas,
-                    cudaStream_t stream) {
+                    void *ws, size_t ws_bytes, cudaStream_t stream) {
     TpFusedParams p{};
     const int kr = k / R;
     for (int r = 0; r < R; ++r) {
@@ -1188,15 +1442,30 @@ int launch_tp_fused(const void *const *x, const void *const *w, void *const *out
     p.n = n;
     p.kb_per_rank = kr / kBK;
     switch (pick_bn(n, CC_TP_PAIR && (m / kBM) % 2 == 0)) {
-        case 128: return launch_bn<128>(p, x, w, m, n, kr, R, max_ctas, stream);
-        case 192: return launch_bn<192>(p, x, w, m, n, kr, R, max_ctas, stream);
-        case 256: return launch_bn<256>(p, x, w, m, n, kr, R, max_ctas, stream);
+        case 128: return launch_bn<128>(p, x, w, m, n, kr, R, max_ctas, ws, ws_bytes, stream);
+        case 192: return launch_bn<192>(p, x, w, m, n, kr, R, max_ctas, ws, ws_bytes, stream);
+        case 256: return launch_bn<256>(p, x, w, m, n, kr, R, max_ctas, ws, ws_bytes, stream);
         default: return fail(CC_ERR_INVALID, "n=%d is not a multiple of 128 or 192", n);
     }
 }
 
 bool tp_fused_shape_ok(int m, int n, int kr) {
     return m % kBM == 0 && kr % kBK == 0 && pick_bn(n, false) != 0;
+}
+
+int tp_fused_workspace(int m, int n, int R, int max_ctas, size_t *bytes) {
+    *bytes = 0;
+    if (!CC_TP_PAIR || (m / kBM) % 2 != 0) return CC_OK;   // the single-CTA kernel
+    PairPlan plan;
+    int st = CC_OK;
+    switch (pick_bn(n, true)) {
+        case 128: st = pair_plan<128>(m, n, R, max_ctas, true, &plan); break;
+        case 192: st = pair_plan<192>(m, n, R, max_ctas, true, &plan); break;
+        case 256: st = pair_plan<256>(m, n, R, max_ctas, true, &plan); break;
+        default: return fail(CC_ERR_INVALID, "n=%d is not a multiple of 128 or 192", n);
+    }
+    if (st == CC_OK) *bytes = plan.ws_bytes;
+    return st;
 }
 
 
@@ -1226,11 +1495,10 @@ struct Span {
 
 }  // namespace
 
-extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w,
-                                      void *const *out, float *const *partials, int m, int n,
-                                      int k, int R, void *stream) {
+namespace {
+
+int tp_check_shape(int m, int n, int k, int R) {
     using namespace ccdp;
-    TraceRange call("cc_tp_matmul_allreduce", static_cast<uint64_t>(m));
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     if (m <= 0 || n <= 0 || k <= 0) return fail(CC_ERR_INVALID, "m, n, k must be > 0");
     if (k % R != 0) return fail(CC_ERR_INVALID, "k=%d is not a multiple of R=%d", k, R);
@@ -1239,7 +1507,35 @@ extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w
         return fail(CC_ERR_INVALID,
                     "shape m=%d n=%d k/R=%d: needs m %% 128 == 0, n a multiple of 128 or "
                     "192, and k/R %% 64 == 0", m, n, kr);
+    return CC_OK;
+}
+
+}  // namespace
+
+extern "C" int cc_tp_matmul_allreduce_workspace(int m, int n, int k, int R, int max_ctas,
+                                                size_t *bytes) {
+    using namespace ccdp;
+    if (!bytes) return fail(CC_ERR_INVALID, "bytes is NULL");
+    *bytes = 0;
+    if (max_ctas < 0) return fail(CC_ERR_INVALID, "max_ctas=%d must be >= 0", max_ctas);
+    int st;
+    if ((st = tp_check_shape(m, n, k, R)) != CC_OK) return st;
+    if ((st = ensure_device()) != CC_OK) return st;
+    return tp_fused_workspace(m, n, R, max_ctas, bytes);
+}
+
+extern "C" int cc_tp_matmul_allreduce_ex(const void *const *x, const void *const *w,
+                                         void *const *out, float *const *partials, int m,
+                                         int n, int k, int R, void *workspace,
+                                         size_t workspace_bytes, int max_ctas, void *stream) {
+    using namespace ccdp;
+    TraceRange call("cc_tp_matmul_allreduce", static_cast<uint64_t>(m));
+    int st;
+    if ((st = tp_check_shape(m, n, k, R)) != CC_OK) return st;
+    if (max_ctas < 0) return fail(CC_ERR_INVALID, "max_ctas=%d must be >= 0", max_ctas);
+    if (max_ctas == 1) return fail(CC_ERR_INVALID, "max_ctas=1: the kernel runs CTA pairs");
     if (!x || !w || !out) return fail(CC_ERR_INVALID, "x/w/out arrays are NULL");
+    const int kr = k / R;
     const size_t mn = static_cast<size_t>(m) * n;
     std::vector<Span> spans;
     auto add = [&](const void *ptr, size_t bytes, bool written, const char *name, int r) {
@@ -1250,7 +1546,6 @@ extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w
         spans.push_back({lo, lo + bytes, written, name, r});
         return static_cast<int>(CC_OK);
     };
-    int st;
     for (int r = 0; r < R; ++r) {
         if ((st = add(x[r], 2 * static_cast<size_t>(m) * kr, false, "x", r)) != CC_OK) return st;
         if ((st = add(w[r], 2 * static_cast<size_t>(n) * kr, false, "w", r)) != CC_OK) return st;
@@ -1258,6 +1553,9 @@ extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w
         if (partials && (st = add(partials[r], 4 * mn, true, "partials", r)) != CC_OK)
             return st;
     }
+    if (workspace && workspace_bytes > 0 &&
+        (st = add(workspace, workspace_bytes, true, "workspace", 0)) != CC_OK)
+        return st;
     for (size_t i = 0; i < spans.size(); ++i)
         for (size_t j = i + 1; j < spans.size(); ++j)
             if ((spans[i].written || spans[j].written) && spans[i].lo < spans[j].hi &&
@@ -1269,6 +1567,13 @@ extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w
         if ((st = check_device_range(reinterpret_cast<const void *>(sp.lo), sp.hi - sp.lo,
                                      sp.name)) != CC_OK)
             return st;
-    return launch_tp_fused(x, w, out, partials, m, n, k, R, 0,
+    return launch_tp_fused(x, w, out, partials, m, n, k, R, max_ctas,
+                           workspace_bytes > 0 ? workspace : nullptr, workspace_bytes,
                            static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int cc_tp_matmul_allreduce(const void *const *x, const void *const *w,
+                                      void *const *out, float *const *partials, int m, int n,
+                                      int k, int R, void *stream) {
+    return cc_tp_matmul_allreduce_ex(x, w, out, partials, m, n, k, R, nullptr, 0, 0, stream);
 }

@@ -554,6 +554,48 @@ CC_API int cc_tp_matmul_allreduce(const void *const *x, const void *const *w,
                                   int k, int R, void *stream);
 
 /*
+ * cc_tp_matmul_allreduce_ex -- cc_tp_matmul_allreduce with a caller
+ * workspace and a CTA budget.  Same results, bit for bit, whatever the
+ * workspace and budget.
+ *
+ * The kernel runs persistent CTA pairs, each taking one pair of 128-row
+ * output tiles ("group") through all R ranks.  When the groups do not fill
+ * the last wave, a workspace lets the kernel split that wave's groups into
+ * their R rank products, spread over every pair: each product goes to the
+ * workspace as fp32 and the pair that finishes a group's last product
+ * (counted with one atomic per group half; no CTA waits for another) adds
+ * the R products in rank order and writes the bf16 outputs.
+ *
+ *   workspace        NULL (or workspace_bytes 0): no group is split.  Else
+ *                    device memory, 16-byte aligned, overlapping no other
+ *                    buffer, of at least the bytes
+ *                    cc_tp_matmul_allreduce_workspace gives for the same
+ *                    shape and max_ctas on the same device
+ *                    (CC_ERR_INVALID if smaller).  The call clears its
+ *                    counters on the stream before the launch; calls that
+ *                    share a workspace must be ordered (one stream).
+ *   max_ctas         0: as many CTA pairs as fit the GPU at once; else at
+ *                    most max_ctas CTAs (>= 2; 1 is CC_ERR_INVALID).
+ * Other arguments and errors as cc_tp_matmul_allreduce.
+ */
+CC_API int cc_tp_matmul_allreduce_ex(const void *const *x, const void *const *w,
+                                     void *const *out, float *const *partials, int m, int n,
+                                     int k, int R, void *workspace, size_t workspace_bytes,
+                                     int max_ctas, void *stream);
+
+/*
+ * cc_tp_matmul_allreduce_workspace -- the workspace bytes
+ * cc_tp_matmul_allreduce_ex uses for this shape and max_ctas on the current
+ * device: 0 when it splits nothing (R = 1, groups that fill every wave, a
+ * wave whose splitting would not shorten it, or an odd count of row tiles).
+ * Otherwise 256 bytes of counters per 32 split groups plus 2 x 128 x BN x R
+ * fp32 products per split group (BN = 256, 192 or 128, the tile width the
+ * kernel picks for n).  Shape errors as cc_tp_matmul_allreduce.
+ */
+CC_API int cc_tp_matmul_allreduce_workspace(int m, int n, int k, int R, int max_ctas,
+                                            size_t *bytes);
+
+/*
  * cc_device_status -- the status word of the library's pipelined kernels on
  * the current device: 0, or an or of codes of pipeline waits that ran out
  * (every such wait is bounded, after which the kernel abandons its pipeline

@@ -44,12 +44,29 @@ def operands(R, m, n, k, seed, integer):
     return x, w
 
 
-def run(x, w, m, n, k, R, with_partials=True):
+# Schedules: (workspace?, CTA budget).  Without a workspace every group of
+# output tiles runs whole; with one the last wave's groups are split into
+# rank products summed by the last to finish.  A budget of 6 CTAs (3 pairs)
+# gives several whole waves per pair followed by a split wave.
+SCHEDULES = {"whole": (False, 0), "split": (True, 0), "whole-3pairs": (False, 6),
+             "split-3pairs": (True, 6)}
+
+
+def run(x, w, m, n, k, R, with_partials=True, schedule="whole"):
     outs = [torch.full((m, n), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
             for _ in range(R)]
     parts = ([torch.full((m, n), float("nan"), device=DEV) for _ in range(R)]
              if with_partials else None)
-    capi.cc_tp_matmul_allreduce(x, w, outs, parts, m, n, k, R)
+    split, max_ctas = SCHEDULES[schedule]
+    if schedule == "whole":
+        capi.cc_tp_matmul_allreduce(x, w, outs, parts, m, n, k, R)
+    else:
+        ws_bytes = capi.cc_tp_matmul_allreduce_workspace(m, n, k, R, max_ctas) if split else 0
+        if schedule == "split-3pairs" and (m // 128) % 2 == 0 and R > 1:
+            assert ws_bytes > 0                  # these shapes do split their last wave
+        ws = (torch.full((max(ws_bytes, 16),), 0x7F, dtype=torch.uint8, device=DEV)
+              if split else None)
+        capi.cc_tp_matmul_allreduce_ex(x, w, outs, parts, m, n, k, R, ws, ws_bytes, max_ctas)
     torch.cuda.synchronize()
     assert capi.cc_device_status() == 0
     return outs, parts
@@ -71,10 +88,11 @@ SHAPES = [(1, 128, 128, 64), (2, 256, 256, 256), (3, 2560, 1280, 192),
           (4, 512, 640, 256)]
 
 
+@pytest.mark.parametrize("schedule", list(SCHEDULES))
 @pytest.mark.parametrize("R,m,n,k", SHAPES)
-def test_integer_operands_are_exact(R, m, n, k):
+def test_integer_operands_are_exact(R, m, n, k, schedule):
     x, w = operands(R, m, n, k, seed=11 + R, integer=True)
-    outs, parts = run(x, w, m, n, k, R)
+    outs, parts = run(x, w, m, n, k, R, schedule=schedule)
     Y = exact_products(x, w)
     total = sum(Y)
     for r in range(R):
@@ -86,10 +104,11 @@ def test_integer_operands_are_exact(R, m, n, k):
         assert_bits(f"out[{r}]", u16(outs[r]).ravel(), want16, "bf16")
 
 
+@pytest.mark.parametrize("schedule", ["whole", "split-3pairs"])
 @pytest.mark.parametrize("R,m,n,k", SHAPES)
-def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k):
+def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k, schedule):
     x, w = operands(R, m, n, k, seed=21 + R, integer=False)
-    outs, parts = run(x, w, m, n, k, R)
+    outs, parts = run(x, w, m, n, k, R, schedule=schedule)
     P = [f32(p).ravel().copy() for p in parts]
     ref = oracle.tp_allreduce(P)
     for r in range(R):
@@ -101,19 +120,23 @@ def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k):
         bound = kr * 2.0 ** -23 * (np.abs(X) @ np.abs(W).T) + 1e-30
         err = np.abs(P[r].reshape(m, n) - Yr)
         assert np.all(err <= bound), f"partial {r}: max excess {np.max(err - bound)}"
-    # the debug store of the partials changes nothing in the outputs
-    outs2, _ = run(x, w, m, n, k, R, with_partials=False)
-    for r in range(R):
-        assert torch.equal(outs2[r].view(torch.int16), outs[r].view(torch.int16))
+    # neither the debug store of the partials nor the schedule changes an
+    # output bit
+    for other in ("whole", "split", "split-3pairs"):
+        outs2, _ = run(x, w, m, n, k, R, with_partials=False, schedule=other)
+        for r in range(R):
+            assert torch.equal(outs2[r].view(torch.int16), outs[r].view(torch.int16)), other
 
 
-def test_gpt2_mlp_shape_sampled():
+@pytest.mark.parametrize("schedule", ["whole", "split"])
+def test_gpt2_mlp_shape_sampled(schedule):
     """The measured shape (R=8, m=8192, n=3072, k=12288): integer operands,
-    so every output is exact; checked on sampled rows against float64."""
+    so every output is exact; checked on sampled rows against float64 (the
+    last row tiles are the split wave's)."""
     R, m, n, k = 8, 8192, 3072, 12288
     x, w = operands(R, m, n, k, seed=5, integer=True)
-    outs, _ = run(x, w, m, n, k, R, with_partials=False)
-    rows = torch.tensor([0, 1, 127, 128, 4095, 4096, 8191], device=DEV)
+    outs, _ = run(x, w, m, n, k, R, with_partials=False, schedule=schedule)
+    rows = torch.tensor([0, 1, 127, 128, 4095, 4096, 7936, 8000, 8191], device=DEV)
     total = sum(x_[rows].double() @ w_.double().T for x_, w_ in zip(x, w))
     want = total.float().to(torch.bfloat16).view(torch.int16)
     for r in range(R):
@@ -134,3 +157,24 @@ def test_rejects_bad_shapes_and_aliases():
     with pytest.raises(capi.CCError) as ei:
         capi.cc_tp_matmul_allreduce(x, w, [outs[0], x[1]], None, m, n, k, R)
     assert ei.value.status == capi.CC_ERR_ALIAS
+
+
+def test_rejects_small_workspace_and_one_cta():
+    R, m, n, k = 4, 512, 640, 256
+    x, w = operands(R, m, n, k, seed=4, integer=True)
+    outs = [torch.empty(m, n, dtype=torch.bfloat16, device=DEV) for _ in range(R)]
+    need = capi.cc_tp_matmul_allreduce_workspace(m, n, k, R, 6)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, ws, need - 16, 6)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, None, 0, 1)
+    assert ei.value.status == capi.CC_ERR_INVALID
+    with pytest.raises(capi.CCError) as ei:
+        capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, outs[1], need, 6)
+    assert ei.value.status == capi.CC_ERR_ALIAS
+    # one split-free launch later nothing is left armed
+    torch.cuda.synchronize()
+    assert capi.cc_device_status() == 0
