@@ -766,6 +766,9 @@ def run_ours(args):
                 rows = run_overlap(args, wk, dev, [1, 4, 25, 100, 500], rank_share=share)
                 sweep["rank_share" if share else "all_replicas"] = [
                     {k: r[k] for k in OVERLAP_KEEP} for r in rows]
+            sweep["tuned_bucket_mib"] = {mode: next(r["bucket_mib"] for r in rows
+                                                    if r["tuner_choice"])
+                                         for mode, rows in list(sweep.items())}
             result["overlap_sweep"] = sweep
         # the rank share with the opt-in fast arithmetic: fewer instructions
         # per element, so the reduction takes less SM time beside the GEMMs
@@ -786,6 +789,9 @@ def run_ours(args):
                                    acc=acc)
                 red["rank_share" if share else "all_replicas"] = [
                     {k: r[k] for k in OVERLAP_KEEP} for r in rows]
+            red["tuned_bucket_mib"] = {mode: next(r["bucket_mib"] for r in rows
+                                                  if r["tuner_choice"])
+                                       for mode, rows in list(red.items())}
             result["overlap_reducing_step"] = red
             del acc
             torch.cuda.empty_cache()
@@ -1257,28 +1263,26 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0, acc=None,
     A = torch.randn(M * K, generator=g, device=dev).to(torch.bfloat16)
     B = torch.randn(K * N, generator=g, device=dev).to(torch.bfloat16)
     C = torch.empty(M * N, dtype=torch.bfloat16, device=dev)
+    # every size through the library's tuner: it plans each cap (and rank
+    # 0's shard of each bucket), times it and names the shortest step
+    _, _, n_slab = capi.cc_plan_buckets(wk["numel"], 0)
+    assert n_slab == wk["n_slab"]
+    best, results = capi.cc_tune_bucket_bytes(
+        numel=wk["numel"], layer_of=wk["layer_of"], candidates=[mib << 20 for mib in mibs],
+        rank=0 if rank_share else -1,
+        grads=wk["grads"], master=wk["master"], m=wk["m"], v=wk["v"],
+        params_out=wk["outs"], n=n_slab, R=w.R, num_layers=num_layers, gemms_per_layer=3,
+        gemm_m=M, gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
+        warmup=args.warmup, iters=args.overlap_iters,
+        max_ctas=args.overlap_ctas, stream_priority=args.stream_priority,
+        comm_sms=comm_sms, gemm_algo=args.overlap_gemm_algo,
+        budget_buckets=args.overlap_budget_buckets, acc=acc, arith_flags=arith_flags,
+        **step_args(wk, w.step))
     out = []
-    for mib in mibs:
-        offsets, buckets, n_slab = capi.cc_plan_buckets(wk["numel"], mib << 20)
-        assert n_slab == wk["n_slab"] and offsets == wk["offsets"]
-        ready = capi.cc_bucket_ready_layers(wk["numel"], wk["layer_of"], offsets, buckets)
-        if rank_share:
-            shards, _, _ = capi.cc_shard_plan(buckets, w.R)     # rank 0's shard of each
-            pairs = [(row[0], rl) for row, rl in zip(shards, ready)]
-            pairs = [(br, rl) for br, rl in pairs if br[1] > br[0]]
-            buckets, ready = [br for br, _ in pairs], [rl for _, rl in pairs]
-        r = capi.cc_overlap_bench(
-            grads=wk["grads"], master=wk["master"], m=wk["m"], v=wk["v"],
-            params_out=wk["outs"], n=n_slab, R=w.R, buckets=buckets,
-            ready_layers=ready, num_layers=num_layers, gemms_per_layer=3, gemm_m=M,
-            gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
-            warmup=args.warmup, iters=args.overlap_iters,
-            max_ctas=args.overlap_ctas, stream_priority=args.stream_priority,
-            comm_sms=comm_sms, gemm_algo=args.overlap_gemm_algo,
-            budget_buckets=args.overlap_budget_buckets, acc=acc, arith_flags=arith_flags,
-            **step_args(wk, w.step))
+    for mib, r in zip(mibs, results):
         r = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()}
         r["bucket_mib"] = mib
+        r["tuner_choice"] = (mib << 20) == best
         r["mode"] = (("rank share (1/R of each bucket)" if rank_share else "all R replicas")
                      + (", reducing step with fp32 accumulators" if acc is not None else "")
                      + (", fast arithmetic" if arith_flags else ""))
@@ -1292,9 +1296,9 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0, acc=None,
     return out[0] if len(out) == 1 else out
 
 
-OVERLAP_KEEP = ("bucket_mib", "num_buckets", "t_bwd_ms", "t_comm_ms", "t_step_overlap_ms",
-                "t_step_seq_ms", "exposed_ms", "exposed_bound_ms", "t_overlap_ms",
-                "overlap_eff")
+OVERLAP_KEEP = ("bucket_mib", "tuner_choice", "num_buckets", "t_bwd_ms", "t_comm_ms",
+                "t_step_overlap_ms", "t_step_seq_ms", "exposed_ms", "exposed_bound_ms",
+                "t_overlap_ms", "overlap_eff")
 
 
 def small_overlap_workload(wk, num_layers):

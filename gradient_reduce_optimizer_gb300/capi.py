@@ -23,6 +23,7 @@ CC_MAX_R = 16
 CC_PAD_ELEMS = 8
 CC_NOALLOC_SCRATCH_ELEMS = 16 * 1024 * 1024   # fixed scratch of the allocation-free entry point
 CC_ARITH_FAST = 1                             # opt-in fast arithmetic of the bucket kernels
+CC_TUNE_MAX_CANDIDATES = 64                   # bucket caps one tuning call may try
 CC_OK = 0
 CC_ERR_INVALID = -1
 CC_ERR_ALIAS = -2
@@ -71,6 +72,16 @@ class cc_overlap_result(ctypes.Structure):
     ]
 
 
+class cc_tune_cfg(ctypes.Structure):
+    _fields_ = [("overlap", cc_overlap_cfg), ("numel", _vp), ("layer_of", _vp),
+                ("num_tensors", _i), ("candidates", _vp), ("num_candidates", _i),
+                ("rank", _i)]
+
+
+class cc_tune_result(ctypes.Structure):
+    _fields_ = [("best", _i), ("best_bucket_bytes", _sz), ("num_candidates", _i)]
+
+
 class cc_tp_cfg(ctypes.Structure):
     _fields_ = [
         ("R", _i), ("m", _i), ("n", _i), ("k", _i), ("chunks", _i),
@@ -100,6 +111,8 @@ _SIGNATURES = {
     "cc_bucket_ready_layers": ([_vp, _vp, _vp, _i, _vp, _vp, _i, _vp], _i),
     "cc_overlap_bench": ([ctypes.POINTER(cc_overlap_cfg),
                           ctypes.POINTER(cc_overlap_result)], _i),
+    "cc_tune_bucket_bytes": ([ctypes.POINTER(cc_tune_cfg), ctypes.POINTER(cc_overlap_result),
+                              ctypes.POINTER(cc_tune_result)], _i),
     "cc_l2_flush": ([_vp, _sz, _vp], _i),
     "cc_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
     "cc_unfused_dp_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _sz, _sz, _i, _sz,
@@ -309,16 +322,15 @@ def cc_bucket_ready_layers(numel: Sequence[int], layer_of: Sequence[int],
     return list(out)[:B]
 
 
-def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
-                     buckets: Sequence[Tuple[int, int]],
-                     ready_layers: Sequence[int], lr: float, beta1: float,
-                     beta2: float, eps: float, weight_decay: float, step: int,
-                     grad_scale: float, num_layers: int, gemms_per_layer: int,
-                     gemm_m: int, gemm_n: int, gemm_k: int, gemm_a, gemm_b,
-                     gemm_c, warmup: int = 3, iters: int = 20,
-                     max_ctas: int = 0, stream_priority: int = 0, comm_sms: int = 0,
-                     budget_buckets: int = 0, gemm_algo: int = 0,
-                     acc=None, arith_flags: int = 0) -> Dict[str, float]:
+def _overlap_cfg(*, grads, master, m, v, params_out, n: int, R: int,
+                 buckets: Sequence[Tuple[int, int]], ready_layers: Sequence[int], lr: float,
+                 beta1: float, beta2: float, eps: float, weight_decay: float, step: int,
+                 grad_scale: float, num_layers: int, gemms_per_layer: int, gemm_m: int,
+                 gemm_n: int, gemm_k: int, gemm_a, gemm_b, gemm_c, warmup: int = 3,
+                 iters: int = 20, max_ctas: int = 0, stream_priority: int = 0,
+                 comm_sms: int = 0, budget_buckets: int = 0, gemm_algo: int = 0, acc=None,
+                 arith_flags: int = 0):
+    """A cc_overlap_cfg and the ctypes arrays it points into (keep both)."""
     B = len(buckets)
     keep = dict(
         g=_addr_array(grads), o=_addr_array(params_out),
@@ -331,9 +343,9 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
         acc=ctypes.cast(keep["a"], _vp) if keep["a"] is not None else None,
         master=_addr(master), m=_addr(m), v=_addr(v),
         params_out=ctypes.cast(keep["o"], _vp), n=n, R=R,
-        bucket_begin=ctypes.cast(keep["bb"], _vp),
-        bucket_end=ctypes.cast(keep["be"], _vp),
-        bucket_ready_layer=ctypes.cast(keep["rl"], _vp), num_buckets=B,
+        bucket_begin=ctypes.cast(keep["bb"], _vp) if B else None,
+        bucket_end=ctypes.cast(keep["be"], _vp) if B else None,
+        bucket_ready_layer=ctypes.cast(keep["rl"], _vp) if B else None, num_buckets=B,
         lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay,
         step=step, grad_scale=grad_scale, num_layers=num_layers,
         gemms_per_layer=gemms_per_layer, gemm_m=gemm_m, gemm_n=gemm_n,
@@ -341,10 +353,45 @@ def cc_overlap_bench(*, grads, master, m, v, params_out, n: int, R: int,
         gemm_c=_addr(gemm_c), warmup=warmup, iters=iters, max_ctas=max_ctas,
         stream_priority=stream_priority, comm_sms=comm_sms,
         budget_buckets=budget_buckets, gemm_algo=gemm_algo, arith_flags=arith_flags)
+    return cfg, keep
+
+
+def _result_dict(res) -> Dict[str, float]:
+    return {name: getattr(res, name) for name, _ in res._fields_}
+
+
+def cc_overlap_bench(**kw) -> Dict[str, float]:
+    """The four timing arms of the bucketed step behind a proxy backward
+    (keyword arguments: the cc_overlap_cfg fields; buckets as (begin, end)
+    pairs and ready_layers)."""
+    cfg, keep = _overlap_cfg(**kw)
     res = cc_overlap_result()
     _check(lib().cc_overlap_bench(ctypes.byref(cfg), ctypes.byref(res)),
            "cc_overlap_bench")
-    return {name: getattr(res, name) for name, _ in res._fields_}
+    return _result_dict(res)
+
+
+def cc_tune_bucket_bytes(*, numel: Sequence[int], layer_of: Sequence[int],
+                         candidates: Optional[Sequence[int]] = None, rank: int = -1,
+                         **kw) -> Tuple[int, List[Dict[str, float]]]:
+    """The measured best bucket cap: (cap in bytes, each candidate's overlap
+    result).  Keyword arguments as cc_overlap_bench, without buckets and
+    ready_layers; candidates None tries 1, 4, 25, 100 and 500 MiB."""
+    cfg, keep = _overlap_cfg(buckets=[], ready_layers=[], **kw)
+    T = len(numel)
+    nm = (_sz * T)(*numel)
+    lo = (_i * T)(*layer_of)
+    cand = (_sz * len(candidates))(*candidates) if candidates is not None else None
+    count = len(candidates) if candidates is not None else 5
+    tcfg = cc_tune_cfg(overlap=cfg, numel=ctypes.cast(nm, _vp), layer_of=ctypes.cast(lo, _vp),
+                       num_tensors=T, candidates=ctypes.cast(cand, _vp) if cand is not None else None,
+                       num_candidates=len(candidates) if candidates is not None else 0,
+                       rank=rank)
+    results = (cc_overlap_result * max(count, 1))()
+    out = cc_tune_result()
+    _check(lib().cc_tune_bucket_bytes(ctypes.byref(tcfg), results, ctypes.byref(out)),
+           "cc_tune_bucket_bytes")
+    return out.best_bucket_bytes, [_result_dict(results[i]) for i in range(out.num_candidates)]
 
 
 def cc_device_status(clear: bool = False) -> int:

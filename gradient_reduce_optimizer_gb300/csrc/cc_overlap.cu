@@ -420,3 +420,119 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     *out = r;
     return CC_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Bucket-size tuning: the overlap bench over a list of bucket caps
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// Bucket caps tried when the caller gives none: the range the bucket-sizing
+// advice spans (25 MB to a few hundred), and two smaller caps.
+constexpr size_t kDefaultCaps[] = {size_t(1) << 20, size_t(4) << 20, size_t(25) << 20,
+                                   size_t(100) << 20, size_t(500) << 20};
+
+// One candidate's launch list: the planner's buckets (or one rank's shard of
+// each, empty shards dropped) and the layer after which each is ready.
+struct CandidatePlan {
+    std::vector<size_t> begin, end;
+    std::vector<int> ready;
+};
+
+int plan_candidate(const cc_tune_cfg &t, size_t cap, CandidatePlan *out) {
+    const int T = t.num_tensors;
+    std::vector<size_t> offsets(T);
+    int nb = 0;
+    size_t n_padded = 0;
+    int st = cc_plan_buckets(t.numel, T, cap, offsets.data(), nullptr, nullptr, 0, &nb,
+                             &n_padded);
+    if (st != CC_OK && st != CC_ERR_CAPACITY) return st;
+    if (n_padded != t.overlap.n)
+        return fail(CC_ERR_INVALID,
+                    "the tensors' slab has %zu elements, the overlap config's n is %zu",
+                    n_padded, t.overlap.n);
+    std::vector<size_t> bb(nb), be(nb);
+    if ((st = cc_plan_buckets(t.numel, T, cap, offsets.data(), bb.data(), be.data(), nb, &nb,
+                              nullptr)) != CC_OK)
+        return st;
+    std::vector<int> ready(nb);
+    if ((st = cc_bucket_ready_layers(t.numel, t.layer_of, offsets.data(), T, bb.data(),
+                                     be.data(), nb, ready.data())) != CC_OK)
+        return st;
+    out->begin.clear();
+    out->end.clear();
+    out->ready.clear();
+    if (t.rank < 0) {
+        out->begin = bb;
+        out->end = be;
+        out->ready = ready;
+        return CC_OK;
+    }
+    const int R = t.overlap.R;
+    std::vector<size_t> sb(static_cast<size_t>(nb) * R), se(sb.size()), so(sb.size());
+    std::vector<size_t> elems(R);
+    if ((st = cc_shard_plan(bb.data(), be.data(), nb, R, sb.data(), se.data(), so.data(),
+                            elems.data())) != CC_OK)
+        return st;
+    for (int b = 0; b < nb; ++b) {
+        const size_t lo = sb[static_cast<size_t>(b) * R + t.rank];
+        const size_t hi = se[static_cast<size_t>(b) * R + t.rank];
+        if (hi > lo) {
+            out->begin.push_back(lo);
+            out->end.push_back(hi);
+            out->ready.push_back(ready[b]);
+        }
+    }
+    return CC_OK;
+}
+
+}  // namespace
+
+extern "C" int cc_tune_bucket_bytes(const cc_tune_cfg *cfg, cc_overlap_result *results,
+                                    cc_tune_result *out) {
+    TraceRange call("cc_tune_bucket_bytes", 0);
+    if (!cfg || !out) return fail(CC_ERR_INVALID, "cfg/out is NULL");
+    const cc_tune_cfg &t = *cfg;
+    if (t.num_tensors < 1 || !t.numel || !t.layer_of)
+        return fail(CC_ERR_INVALID, "need at least one tensor with numel and layer_of");
+    const size_t *caps = t.candidates ? t.candidates : kDefaultCaps;
+    const int count = t.candidates ? t.num_candidates
+                                   : static_cast<int>(sizeof(kDefaultCaps) / sizeof(size_t));
+    if (count < 1 || count > CC_TUNE_MAX_CANDIDATES)
+        return fail(CC_ERR_INVALID, "num_candidates=%d must be in 1..%d", count,
+                    CC_TUNE_MAX_CANDIDATES);
+    if (!results) return fail(CC_ERR_INVALID, "results is NULL");
+    if (t.overlap.R < 1 || t.overlap.R > CC_MAX_R)
+        return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", t.overlap.R, CC_MAX_R);
+    if (t.rank < -1 || t.rank >= t.overlap.R)
+        return fail(CC_ERR_INVALID, "rank=%d must be -1 or in 0..R-1", t.rank);
+    // Every candidate is planned, and its plan checked, before anything runs.
+    std::vector<CandidatePlan> plans(count);
+    int st;
+    for (int i = 0; i < count; ++i) {
+        if ((st = plan_candidate(t, caps[i], &plans[i])) != CC_OK) return st;
+        if (plans[i].begin.empty())
+            return fail(CC_ERR_INVALID, "candidate %d (%zu bytes) gives rank %d no elements", i,
+                        caps[i], t.rank);
+        for (int r : plans[i].ready)
+            if (r < 0 || r >= t.overlap.num_layers)
+                return fail(CC_ERR_INVALID,
+                            "candidate %d: a bucket is ready after layer %d, the proxy "
+                            "backward has %d", i, r, t.overlap.num_layers);
+    }
+    int best = -1;
+    for (int i = 0; i < count; ++i) {
+        cc_overlap_cfg c = t.overlap;
+        c.bucket_begin = plans[i].begin.data();
+        c.bucket_end = plans[i].end.data();
+        c.bucket_ready_layer = plans[i].ready.data();
+        c.num_buckets = static_cast<int>(plans[i].begin.size());
+        if ((st = cc_overlap_bench(&c, &results[i])) != CC_OK) return st;
+        if (best < 0 || results[i].t_step_overlap_ms < results[best].t_step_overlap_ms)
+            best = i;
+    }
+    out->best = best;
+    out->best_bucket_bytes = caps[best];
+    out->num_candidates = count;
+    return CC_OK;
+}

@@ -475,6 +475,58 @@ typedef struct cc_overlap_result {
 CC_API int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *out);
 
 /*
+ * cc_tune_bucket_bytes -- choose the DDP bucket size by measurement
+ * ("LIT-735 (CoCoNet)", Key takeaways: the schedule is autotuned;
+ * "Communication Overlap", bucket sizing: caps of 25 to 500 MB work well,
+ * larger models favouring larger buckets, so the best cap is measured, not
+ * fixed).  For each candidate cap the tensors are planned with
+ * cc_plan_buckets and cc_bucket_ready_layers (and, for one rank, cut with
+ * cc_shard_plan), and cc_overlap_bench times that launch list; the
+ * candidate whose overlapped step (t_step_overlap_ms) is shortest wins,
+ * the first listed on a tie.
+ *
+ *   overlap        every cc_overlap_cfg field but the bucket arrays and
+ *                  num_buckets, which are ignored: the slabs (n must be the
+ *                  planner's slab length for numel), hyperparameters, proxy
+ *                  backward and arm settings.  The slabs are stepped for real
+ *                  by every candidate's runs.
+ *   numel, layer_of [num_tensors]  the slab's tensors in forward order and
+ *                  the backward layer of each (in [0, overlap.num_layers)
+ *                  for every bucket's ready layer, else CC_ERR_INVALID).
+ *   candidates     [num_candidates] caps in bf16 bytes (0: one bucket), or
+ *                  NULL for 1, 4, 25, 100 and 500 MiB (num_candidates is
+ *                  then ignored).  1..CC_TUNE_MAX_CANDIDATES.
+ *   rank           -1: every bucket whole (the emulated R replicas);
+ *                  0..R-1: only that rank's shard of each bucket (the
+ *                  per-rank work of the multi-GPU form); a candidate that
+ *                  leaves the rank no elements is CC_ERR_INVALID.
+ *   results        [count] written: each candidate's cc_overlap_result.
+ *   out            written: the winner's index and cap, and the count.
+ * Every candidate is planned and checked on the host before the first
+ * measurement; an error from a measurement stops the call there.
+ */
+#define CC_TUNE_MAX_CANDIDATES 64
+
+typedef struct cc_tune_cfg {
+    cc_overlap_cfg overlap;
+    const size_t *numel;
+    const int *layer_of;
+    int num_tensors;
+    const size_t *candidates;
+    int num_candidates;
+    int rank;
+} cc_tune_cfg;
+
+typedef struct cc_tune_result {
+    int best;                      /* index into the candidates */
+    size_t best_bucket_bytes;
+    int num_candidates;            /* results written */
+} cc_tune_result;
+
+CC_API int cc_tune_bucket_bytes(const cc_tune_cfg *cfg, cc_overlap_result *results,
+                                cc_tune_result *out);
+
+/*
  * cc_tp_allreduce -- the AllReduce of a tensor-parallel row-parallel layer,
  * for R emulated ranks ("LIT-735 (CoCoNet)", Key takeaways: the
  * model-parallel MatMul and the AllReduce that follows it).  Every rank's

@@ -415,3 +415,41 @@ def test_rank_step_validation():
     assert status(grad_slices=[g[0], g[0], g[0]]) in (capi.CC_ERR_UNSUPPORTED,
                                                       capi.CC_ERR_INVALID)   # aliasing reads ok
     assert status() in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID)
+
+
+def test_tune_bucket_bytes_refuses_before_measuring():
+    """The bucket-size tuner plans and checks every candidate on the host
+    before its first measurement: bad tensor lists, candidate counts, ranks,
+    slab lengths and ready layers are refused with no device call."""
+    numel = [1000, 3000, 500, 7000]
+    layer_of = [0, 1, 2, 3]
+    _, _, n = capi.cc_plan_buckets(numel, 0)
+    R = 2
+    g, acc, p, m, v, o = fake_slabs(R, n)
+    kw = dict(grads=g, master=p, m=m, v=v, params_out=o, n=n, R=R, num_layers=4,
+              gemms_per_layer=1, gemm_m=64, gemm_n=64, gemm_k=64, gemm_a=None, gemm_b=None,
+              gemm_c=None, **ADAM)
+
+    def status(**over):
+        args = dict(kw, numel=numel, layer_of=layer_of, candidates=[4096, 16384])
+        args.update(over)
+        try:
+            capi.cc_tune_bucket_bytes(**args)
+            return capi.CC_OK
+        except capi.CCError as err:
+            return err.status
+    assert status(numel=[], layer_of=[]) == capi.CC_ERR_INVALID
+    assert status(candidates=[]) == capi.CC_ERR_INVALID
+    assert status(candidates=[4096] * (capi.CC_TUNE_MAX_CANDIDATES + 1)) == capi.CC_ERR_INVALID
+    assert status(n=n + 8) == capi.CC_ERR_INVALID              # not this tensor list's slab
+    assert status(rank=R) == capi.CC_ERR_INVALID
+    assert status(rank=-2) == capi.CC_ERR_INVALID
+    assert status(num_layers=3) == capi.CC_ERR_INVALID         # a bucket ready after layer 3
+    # a one-unit slab gives rank 0 of 2 no elements
+    _, _, n8 = capi.cc_plan_buckets([8], 0)
+    assert status(numel=[8], layer_of=[0], n=n8, rank=0) == capi.CC_ERR_INVALID
+    # well-formed: planning passes and the first measurement refuses the fake
+    # (host) addresses
+    assert status() in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID, capi.CC_ERR_CUDA)
+    assert status(candidates=None, rank=1) in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID,
+                                               capi.CC_ERR_CUDA)

@@ -656,6 +656,56 @@ def test_overlap_bench_rejects_bad_schedules():
         assert ei.value.status == capi.CC_ERR_INVALID
 
 
+@pytest.mark.parametrize("rank", [-1, 1])
+def test_tune_bucket_bytes_measures_every_candidate(rank):
+    """The bucket-size tuner times each candidate cap's launch list with the
+    overlap bench and returns the cap whose overlapped step is shortest.
+    With warmup 0 and one iteration every candidate steps its buckets (or
+    the rank's shards of them) three times: the slabs must equal the oracle
+    stepping each element three times per candidate whose launch list covers
+    it, bucket lists taken from the oracle's own planner."""
+    t = wl.bert_large_tensors(layers=4, hidden=256, ffn=1024, vocab=997, positions=64)
+    numel = [x[1] for x in t]
+    layer_of = [x[2] for x in t]
+    caps = [64 * 1024, 256 * 1024, 0]
+    R = 3
+    _, _, n_slab = oracle.plan_buckets(numel, 0)
+    s = new_slabs(*random_inputs(R, n_slab, seed=73, step=5))
+    grads, state, _ = host_copy(s)
+    hp = dict(HP10, step=5)
+    M = N = K = 256
+    A = torch.randn(M * K, device=DEV).to(torch.bfloat16)
+    B = torch.randn(K * N, device=DEV).to(torch.bfloat16)
+    C = torch.empty(M * N, dtype=torch.bfloat16, device=DEV)
+    best, results = capi.cc_tune_bucket_bytes(
+        numel=numel, layer_of=layer_of, candidates=caps, rank=rank, grads=s.grads,
+        master=s.master, m=s.m, v=s.v, params_out=s.outs, n=n_slab, R=R, num_layers=4,
+        gemms_per_layer=2, gemm_m=M, gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
+        warmup=0, iters=1, **hp)
+    assert len(results) == len(caps)
+    step_ms = [r["t_step_overlap_ms"] for r in results]
+    assert best == caps[min(range(len(caps)), key=lambda i: (step_ms[i], i))]
+    outs = [np.full(n_slab, 0xFFFF, dtype=np.uint16) for _ in range(R)]
+    for cap, res in zip(caps, results):
+        _, buckets, _ = oracle.plan_buckets(numel, cap)
+        if rank >= 0:
+            shards = oracle.shard_plan(buckets, R)[0]
+            buckets = [row[rank] for row in shards if row[rank][1] > row[rank][0]]
+        assert res["num_buckets"] == len(buckets)
+        idx = np.concatenate([np.arange(lo, hi) for lo, hi in buckets])
+        sub = [a[idx].copy() for a in state]
+        sub_grads = [g[idx] for g in grads]
+        for _ in range(3):
+            sub_outs = oracle.fused_dp_step(sub_grads, *sub, **hp)
+        for a, b in zip(state, sub):
+            a[idx] = b
+        for o, b in zip(outs, sub_outs):
+            o[idx] = b
+    torch.cuda.synchronize()
+    compare_all(s, state, outs)
+    assert capi.cc_device_status() == 0
+
+
 # ---------------------------------------------------------------------------
 # The tensor-parallel MatMul-then-AllReduce
 # ---------------------------------------------------------------------------
