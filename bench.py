@@ -851,7 +851,10 @@ def run_launch_floor(args, dev, reps=100, samples=50):
     fit in the 129 MB L2, so this measures the launch and L2 floor, three
     ways:
       flushed  one launch at a time, a 512 MiB write before each (the
-               step's inputs come from HBM), median over `samples`
+               step's inputs come from HBM, and its loads evict the
+               flush's dirty lines), median over `samples`
+      flushed_clean  the same with a 512 MiB read after the write (the L2
+               holds clean lines only: the step's own traffic alone)
       warm     `reps` launches back to back from the stream (L2-resident)
       graph    the same `reps` launches captured once in a CUDA graph and
                replayed, median over `samples` replays."""
@@ -891,6 +894,24 @@ def run_launch_floor(args, dev, reps=100, samples=50):
     torch.cuda.synchronize()
     flushed_us = statistics.median(a.elapsed_time(b) for a, b in pairs) * 1e3
 
+    # the same after a read of another 512 MiB: the flush's dirty lines are
+    # written back before the launch, so the step pays only for its own
+    # traffic from HBM
+    clean = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    clean.fill_(1)
+    pairs = []
+    for _ in range(samples):
+        capi.cc_l2_flush(flush, flush.numel(), stream=stream)
+        clean.max()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        step(stream)
+        e1.record(stream)
+        pairs.append((e0, e1))
+    torch.cuda.synchronize()
+    clean_us = statistics.median(a.elapsed_time(b) for a, b in pairs) * 1e3
+    del clean
+
     e0, e1 = ev(), ev()
     e0.record(stream)
     for _ in range(reps):
@@ -904,6 +925,8 @@ def run_launch_floor(args, dev, reps=100, samples=50):
            "bytes_per_step": step_bytes,
            "flushed_us": round(flushed_us, 2),
            "flushed_gbs": round(step_bytes / (flushed_us * 1e-6) / 1e9, 1),
+           "flushed_clean_us": round(clean_us, 2),
+           "flushed_clean_gbs": round(step_bytes / (clean_us * 1e-6) / 1e9, 1),
            "warm_us": round(warm_us, 2),
            "warm_gbs": round(step_bytes / (warm_us * 1e-6) / 1e9, 1),
            "reps": reps}

@@ -278,7 +278,8 @@ int run_step(const Slabs &s, const AdamScalars &c, size_t n, size_t bucket_bytes
         if (injected_failure())
             return fail(CC_ERR_CUDA, "injected launch failure before the bucket at element %zu", b);
         TraceRange bucket("bucket", b);
-        const cudaError_t err = launch_fused(s, c, b, e, 0, /*chain=*/b > 0, stream);
+        const cudaError_t err = launch_fused(s, c, b, e, 0, /*chain=*/b > 0, stream,
+                                             /*wait_first=*/b == 0);
         if (err != cudaSuccess) return fail_cuda(err, "fused step launch");
     }
     return CC_OK;

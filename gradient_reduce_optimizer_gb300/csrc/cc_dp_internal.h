@@ -41,10 +41,14 @@ struct Slabs {
 // aligned slab bases (checked by the caller).  max_ctas > 0 caps the grid.
 // chain = true launches it as a programmatic dependent of the kernel just
 // before it on `stream`, which must be a fused-step launch on a disjoint
-// element range (the next bucket of the same step).
+// element range (the next bucket of the same step).  wait_first = true
+// launches it as a programmatic dependent of whatever kernel precedes it,
+// on whose results it may depend: its CTAs may become resident while that
+// kernel finishes, but touch no memory before it has completed (the first
+// bucket of a step, after the previous step's last bucket).
 cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
                          size_t end, int max_ctas, bool chain,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool wait_first = false);
 
 // Enqueue the bulk-copy engine of the same step over [begin, end) on at most
 // num_ctas SMs (one persistent CTA per SM; 0 = every SM).  Same arithmetic

@@ -59,6 +59,9 @@
 #ifndef CC_DP_PDL
 #define CC_DP_PDL 1            // chain consecutive buckets with programmatic launch
 #endif
+#ifndef CC_DP_PDL_FIRST
+#define CC_DP_PDL_FIRST 1      // a step's first bucket too, waiting for the previous step
+#endif
 #ifndef CC_DP_ACC_HALF
 #define CC_DP_ACC_HALF 1       // accumulator variant: 4 elements per thread
 #endif
@@ -86,6 +89,7 @@ struct FusedParams {
     size_t num_vec;                // full vectors in the range
     size_t tail_begin;             // first element of the partial vector
     int tail_len;                  // 0..7 elements after the full vectors
+    int wait_first;                // wait for the preceding grid before any access
 };
 
 // ONE_OUT: the parameters go to out[0] only (one rank's own slab in the
@@ -266,6 +270,7 @@ template <int R, bool ACC, bool ONE_OUT, bool FAST>
 __global__ void __launch_bounds__(kThreads, CC_DP_MIN_BLOCKS)
 fused_step_kernel(const __grid_constant__ FusedParams p) {
     allow_dependents_to_launch();
+    if (p.wait_first) wait_for_predecessor_grid();
     const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
     const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
     if constexpr (threads_per_vector<ACC>() == 2) {
@@ -490,7 +495,8 @@ cudaError_t check_device(int *major, int *minor) {
 }
 
 cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
-                         size_t end, int max_ctas, bool chain, cudaStream_t stream) {
+                         size_t end, int max_ctas, bool chain, cudaStream_t stream,
+                         bool wait_first) {
     if (end <= begin) return cudaSuccess;
     DeviceInfo *d = nullptr;
     cudaError_t e = device_info(&d);
@@ -512,6 +518,8 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     p.num_vec = (end - begin) / CC_PAD_ELEMS;
     p.tail_begin = begin + p.num_vec * CC_PAD_ELEMS;
     p.tail_len = static_cast<int>(end - p.tail_begin);
+    wait_first = wait_first && CC_DP_PDL_FIRST;
+    p.wait_first = wait_first && CC_DP_PDL;
 
     const size_t units = p.num_vec * (acc ? threads_per_vector<true>()
                                           : threads_per_vector<false>());
@@ -532,7 +540,7 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = (chain && CC_DP_PDL) ? 1 : 0;
+    cfg.numAttrs = ((chain || wait_first) && CC_DP_PDL) ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

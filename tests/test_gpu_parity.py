@@ -191,6 +191,36 @@ def test_consecutive_steps_captured_in_a_cuda_graph():
     compare_all(s, state, outs, label="graph ")
 
 
+@pytest.mark.parametrize("graph", [False, True])
+def test_back_to_back_single_bucket_steps(graph):
+    """Twenty one-bucket steps of the same slab with nothing between them
+    (the launch-bound small case: R = 2, 1,048,576 parameters): each step's
+    kernel may become resident while the previous one finishes, but reads
+    master/m/v only after it has completed.  Same bits as twenty oracle
+    steps, from the stream and from a CUDA graph."""
+    R, n, steps = 2, 1 << 20, 20
+    s = new_slabs(*random_inputs(R, n, seed=33, step=3))
+    hp = dict(HP10, step=3)
+    grads, state, _ = host_copy(s)
+    if graph:
+        gpu_step(s, hp)                          # per-device state set up
+        torch.cuda.synchronize()
+        grads, state, _ = host_copy(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(steps // 2):
+                gpu_step(s, hp)
+        for _ in range(2):
+            g.replay()
+    else:
+        for _ in range(steps):
+            gpu_step(s, hp)
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        outs = oracle_step(grads, state, hp)
+    compare_all(s, state, outs, label="graph " if graph else "stream ")
+
+
 @pytest.mark.parametrize("R", [1, 2, 3, 8, 16])
 def test_integer_gradients_sum_exactly(R):
     n = 100_003
