@@ -655,13 +655,14 @@ def run_ours(args):
                                         wk["outs"], n_slab, R, bb, accum_k=4,
                                         stream=stream, **step_args(wk, step))
         elif args.engine_ctas > 0:
-            # the bulk-copy engine on a budget of SMs, bucket by bucket
+            # a budget of SMs, bucket by bucket: the wide-CTA kernel, or the
+            # bulk-copy engine
+            flags = ((capi.CC_ARITH_FAST if args.fast_arith else 0) |
+                     (capi.CC_ENGINE_BULK_COPY if args.bulk_copy else 0))
             for b, e in cuts:
                 capi.cc_fused_dp_bucket_ex(wk["grads"], None, wk["master"], wk["m"],
                                            wk["v"], wk["outs"], n_slab, R, b, e,
-                                           max_ctas=args.engine_ctas,
-                                           arith_flags=(capi.CC_ARITH_FAST if args.fast_arith
-                                                        else 0),
+                                           max_ctas=args.engine_ctas, arith_flags=flags,
                                            stream=stream, **step_args(wk, step))
         else:
             capi.cc_fused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"],
@@ -708,7 +709,9 @@ def run_ours(args):
                            f"accumulate_kernel<R={R}, first={args.micro == 'first'}>"
                            if args.micro else
                            f"fused_step_kernel<R={R}, accumulators>" if acc is not None else
-                           f"fused_step_bulk_kernel<R={R}> on {args.engine_ctas} SMs"
+                           (f"fused_step_bulk_kernel<R={R}> on {args.engine_ctas} SMs"
+                            if args.bulk_copy else
+                            f"fused_step_kernel<R={R}, wide CTAs> on {args.engine_ctas} SMs")
                            if args.engine_ctas > 0 else f"fused_step_kernel<R={R}>"),
                 "launches_per_step": launches}
 
@@ -1045,10 +1048,11 @@ def run_tp_fused(args, dev, x, w, outs, R, m, n, k, sequential_ms=None, reps=20)
 
 
 def run_bulk_rates(args, wk, stream, elems=1 << 25, ctas_list=(16, 32, 64, 96), reps=5):
-    """What one SM streams through the bulk-copy engine (the engine a CTA
-    budget selects), exact and fast arithmetic: the first 2^25 slab elements
-    of the headline workload stepped on 16..96 persistent CTAs.  GB/s of the
-    step's (4R + 24) algorithmic bytes per parameter, in total and per SM."""
+    """What one SM streams under a CTA budget, exact and fast arithmetic,
+    on both budget engines: the wide-CTA kernel (the default) and the TMA
+    bulk-copy engine (CC_ENGINE_BULK_COPY).  The first 2^25 slab elements of
+    the headline workload stepped on 16..96 SMs.  GB/s of the step's
+    (4R + 24) algorithmic bytes per parameter, in total and per SM."""
     import torch
     from gradient_reduce_optimizer_gb300 import capi
 
@@ -1058,7 +1062,9 @@ def run_bulk_rates(args, wk, stream, elems=1 << 25, ctas_list=(16, 32, 64, 96), 
     rows = []
     for ctas in ctas_list:
         row = {"ctas": ctas}
-        for name, flags in (("exact", 0), ("fast", capi.CC_ARITH_FAST)):
+        for name, flags in (("exact", 0), ("fast", capi.CC_ARITH_FAST),
+                            ("bulk_copy_exact", capi.CC_ENGINE_BULK_COPY),
+                            ("bulk_copy_fast", capi.CC_ENGINE_BULK_COPY | capi.CC_ARITH_FAST)):
             def one(i):
                 capi.cc_fused_dp_bucket_ex(wk["grads"], None, wk["master"], wk["m"], wk["v"],
                                            wk["outs"], n_slab, R, 0, elems, max_ctas=ctas,
@@ -1399,8 +1405,11 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--bucket-mib", type=int, default=25)
     p.add_argument("--engine-ctas", type=int, default=0,
-                   help="run each bucket on the bulk-copy engine with this many "
-                        "SMs (cc_fused_dp_bucket max_ctas); 0 = the plain kernel")
+                   help="run each bucket on a budget of this many SMs "
+                        "(cc_fused_dp_bucket max_ctas: the wide-CTA kernel); 0 = the "
+                        "plain kernel over the whole GPU")
+    p.add_argument("--bulk-copy", action="store_true",
+                   help="with --engine-ctas: the TMA bulk-copy engine (CC_ENGINE_BULK_COPY)")
     p.add_argument("--small", type=int, default=0,
                    help="profile case: a flat R=8 slab of this many elements, "
                         "one bucket, device timing only")

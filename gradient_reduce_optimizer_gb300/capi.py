@@ -23,6 +23,7 @@ CC_MAX_R = 16
 CC_PAD_ELEMS = 8
 CC_NOALLOC_SCRATCH_ELEMS = 16 * 1024 * 1024   # fixed scratch of the allocation-free entry point
 CC_ARITH_FAST = 1                             # opt-in fast arithmetic of the bucket kernels
+CC_ENGINE_BULK_COPY = 2                       # CTA budgets on the TMA bulk-copy engine
 CC_TUNE_MAX_CANDIDATES = 64                   # bucket caps one tuning call may try
 CC_OK = 0
 CC_ERR_INVALID = -1

@@ -360,7 +360,7 @@ int cc_fused_dp_bucket_ex(const void *const *grads, const float *const *acc,
                           float grad_scale, int max_ctas, unsigned arith_flags,
                           void *stream) {
     TraceRange call("cc_fused_dp_bucket", begin);
-    if (arith_flags & ~CC_ARITH_FAST)
+    if (arith_flags & ~(CC_ARITH_FAST | CC_ENGINE_BULK_COPY))
         return fail(CC_ERR_INVALID, "arith_flags=%#x has unknown bits", arith_flags);
     if (R < 1 || R > CC_MAX_R) return fail(CC_ERR_INVALID, "R=%d must be in 1..%d", R, CC_MAX_R);
     if (begin > end || end > n)
@@ -376,6 +376,7 @@ int cc_fused_dp_bucket_ex(const void *const *grads, const float *const *acc,
     st = validate_slabs(grads, acc, master, m, v, params_out, n, R, acc != nullptr, &s);
     if (st != CC_OK) return st;
     s.fast = (arith_flags & CC_ARITH_FAST) != 0;
+    s.bulk_copy = (arith_flags & CC_ENGINE_BULK_COPY) != 0;
     const cudaError_t e =
         launch_step_range(s, c, begin, end, max_ctas, false, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "fused bucket launch");

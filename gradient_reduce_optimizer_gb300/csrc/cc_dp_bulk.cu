@@ -13,22 +13,27 @@
 //     shared-memory stages, all signalling the stage's "full" mbarrier with
 //     the byte count; up to S tiles (about 180 KB at R = 8) are in flight per
 //     SM, independent of how many threads wait;
-//   * warps 1..8 are consumers, each owning a fixed 128-element slice of
-//     every tile (four elements per lane): once the stage is full a warp
-//     reduces its R gradient slices, applies AdamW and stores master/m/v and
-//     the R bf16 parameter copies (the redistribution) straight to global
-//     memory with coalesced vector stores, then arrives on the stage's
-//     "empty" mbarrier.  The stage returns to the producer when all 8 warps
-//     have arrived; warps never wait for each other.
+//   * the other warps are consumers, in groups of 8 that take the CTA's
+//     tiles in turn (two groups: even and odd tiles).  Each warp owns a
+//     fixed 128-element slice of a tile (four elements per lane): once the
+//     stage is full it reads its slice and reduces the R gradient slices in
+//     fixed order, arrives on the stage's "empty" mbarrier -- the stage goes
+//     back to the producer when all 8 warps of the group have arrived --
+//     and only then applies AdamW and stores master/m/v and the R bf16
+//     parameter copies (the redistribution) straight to global memory with
+//     coalesced vector stores.  Warps never wait for each other, and the
+//     producer refills a stage while its consumers still compute.
 //
-// Measured on GB300: one such CTA streams about 57 GB/s, the same as a
-// 256-thread CTA of the plain kernel, because the SM's arithmetic pipes,
-// not its memory path, are then full: the per-element chain of IEEE
-// divisions and the square root costs about 120 instructions.  So the
-// engine reaches HBM bandwidth only with most SMs (6.8 TB/s on 128); what
-// it adds is a hard, persistent SM budget for running beside other work.
-// Loads carry an evict-first L2 policy and stores are streaming (.cs): the
-// stream is used once.
+// The stage count is a multiple of the group count, so every use of a
+// stage falls to the same group: a group, taking its tiles in order, never
+// waits on a stage whose previous use is still in flight (the mbarrier's
+// parity test would let it through a phase early).
+//
+// Measured on GB300 (2^25 elements, R = 8): one 8-warp consumer group
+// streams about 57 GB/s per SM with the IEEE-exact arithmetic; the SM is
+// then issuing about half the time and otherwise waiting for its stages,
+// not on its arithmetic pipes.  Loads carry an evict-first L2 policy and
+// stores are streaming (.cs): the stream is used once.
 //
 // Every mbarrier wait is bounded by the global timer.  A wait that runs out
 // records a code in a device status word (cc_device_status in
@@ -53,10 +58,17 @@ namespace {
 
 using namespace dev;
 
-constexpr int kConsumerWarps = 8;
+#ifndef CC_DP_BULK_GROUPS
+#define CC_DP_BULK_GROUPS 2    // consumer groups of 8 warps, taking tiles in turn
+#endif
+
+constexpr int kConsumerWarps = 8;              // per group: one tile's consumers
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kBulkThreads = kConsumers + 32;  // + one producer warp
-constexpr int kMaxStages = 8;
+constexpr int kGroups = CC_DP_BULK_GROUPS;
+constexpr int kBulkThreads = kGroups * kConsumers + 32;  // + one producer warp
+constexpr int kMaxStages = 16;
+constexpr int kMaxTile = 1024;                 // a group's 256 threads x 4 elements
+static_assert(kMaxTile == 4 * kConsumers, "one four-element slice per consumer thread");
 constexpr int kSmemBudget = 200 * 1024;        // dynamic shared memory per CTA
 constexpr unsigned kStatusConsumerTimeout = 1u;
 constexpr unsigned kStatusProducerTimeout = 2u;
@@ -155,16 +167,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 }
 
 
-// Four consecutive elements of one tile: operands from shared memory,
-// results straight to global memory (element e = tile start + j).
-template <int R, bool ACC, bool FAST>
-__device__ __forceinline__ void consume4(const unsigned char *st, const StageLayout &L,
-                                         int T, int j, size_t e, const BulkParams &p) {
+// Four consecutive elements of one tile, read from their stage: the fixed-
+// order sum of the R gradients (plus accumulators) and master/m/v.
+struct Operands4 {
+    float s[4];
+    float4 p4, m4, v4;
+};
+
+template <int R, bool ACC>
+__device__ __forceinline__ Operands4 read_reduce4(const unsigned char *st, const StageLayout &L,
+                                                  int T, int j) {
+    Operands4 x;
     uint2 gq[R];
 #pragma unroll
     for (int r = 0; r < R; ++r)
         gq[r] = *reinterpret_cast<const uint2 *>(st + L.g + 2u * (r * T + j));
-    float s[4];
+    float *s = x.s;
     if constexpr (ACC) {
         const float4 a = *reinterpret_cast<const float4 *>(st + L.acc + 4u * j);
         s[0] = add_bf16_lo(a.x, gq[0].x); s[1] = add_bf16_hi(a.y, gq[0].x);
@@ -186,17 +204,24 @@ __device__ __forceinline__ void consume4(const unsigned char *st, const StageLay
             s[2] = add_bf16_lo(s[2], gq[r].y); s[3] = add_bf16_hi(s[3], gq[r].y);
         }
     }
-    float4 p4 = *reinterpret_cast<const float4 *>(st + L.master + 4u * j);
-    float4 m4 = *reinterpret_cast<const float4 *>(st + L.m + 4u * j);
-    float4 v4 = *reinterpret_cast<const float4 *>(st + L.v + 4u * j);
-    adamw_step<FAST>(s[0], p4.x, m4.x, v4.x, p.c);
-    adamw_step<FAST>(s[1], p4.y, m4.y, v4.y, p.c);
-    adamw_step<FAST>(s[2], p4.z, m4.z, v4.z, p.c);
-    adamw_step<FAST>(s[3], p4.w, m4.w, v4.w, p.c);
-    __stcs(reinterpret_cast<float4 *>(p.master + e), p4);
-    __stcs(reinterpret_cast<float4 *>(p.m + e), m4);
-    __stcs(reinterpret_cast<float4 *>(p.v + e), v4);
-    const uint2 o = make_uint2(pack_bf16x2(p4.x, p4.y), pack_bf16x2(p4.z, p4.w));
+    x.p4 = *reinterpret_cast<const float4 *>(st + L.master + 4u * j);
+    x.m4 = *reinterpret_cast<const float4 *>(st + L.m + 4u * j);
+    x.v4 = *reinterpret_cast<const float4 *>(st + L.v + 4u * j);
+    return x;
+}
+
+// AdamW on the four elements and their stores, straight to global memory
+// (element e = tile start + j): needs nothing from the stage any more.
+template <int R, bool FAST>
+__device__ __forceinline__ void update_store4(Operands4 &x, size_t e, const BulkParams &p) {
+    adamw_step<FAST>(x.s[0], x.p4.x, x.m4.x, x.v4.x, p.c);
+    adamw_step<FAST>(x.s[1], x.p4.y, x.m4.y, x.v4.y, p.c);
+    adamw_step<FAST>(x.s[2], x.p4.z, x.m4.z, x.v4.z, p.c);
+    adamw_step<FAST>(x.s[3], x.p4.w, x.m4.w, x.v4.w, p.c);
+    __stcs(reinterpret_cast<float4 *>(p.master + e), x.p4);
+    __stcs(reinterpret_cast<float4 *>(p.m + e), x.m4);
+    __stcs(reinterpret_cast<float4 *>(p.v + e), x.v4);
+    const uint2 o = make_uint2(pack_bf16x2(x.p4.x, x.p4.y), pack_bf16x2(x.p4.z, x.p4.w));
 #pragma unroll
     for (int r = 0; r < R; ++r) __stcs(reinterpret_cast<uint2 *>(p.out[r] + e), o);
 }
@@ -299,12 +324,17 @@ fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
     }
 
     // ---------------- consumer warps ----------------
-    // Warp w (0..7) owns elements [128 w, 128 w + 128) of every tile; lane l
-    // of it the four at 128 w + 4 l.
-    const int ct = tid - 32;
+    // Group q of kGroups takes this CTA's tiles q, q + kGroups, ... (with S a
+    // multiple of kGroups, every use of a stage belongs to one group); its warp
+    // w (0..7) owns elements [128 w, 128 w + 128) of each, lane l the four
+    // at 128 w + 4 l.  Several tiles are in arithmetic at once, so the
+    // latency of one element's chain of operations hides behind the others.
+    const int group = (tid - 32) / kConsumers;
+    const int ct = (tid - 32) % kConsumers;
     const int j = 4 * ct;
-    size_t i = 0;
-    for (size_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++i) {
+    size_t i = static_cast<size_t>(group);
+    for (size_t t = blockIdx.x + static_cast<size_t>(group) * gridDim.x; t < p.num_tiles;
+         t += static_cast<size_t>(kGroups) * gridDim.x, i += kGroups) {
         const int s = static_cast<int>(i % S);
         const int k = static_cast<int>(i / S);
         const bool ready = mbar_wait(smem_addr(&full_bar[s]), k & 1, p.timeout_ns);
@@ -318,12 +348,16 @@ fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
         const int len = static_cast<int>(left < static_cast<size_t>(T) ? left : T);
         const unsigned char *st = smem + static_cast<size_t>(s) * L.bytes;
         const size_t e0 = p.begin + t * static_cast<size_t>(T);
-        for (int jj = j; jj < len; jj += 4 * kConsumers)
-            consume4<R, ACC, FAST>(st, L, T, jj, e0 + jj, p);
+        // Read and reduce, hand the stage back, then update and store: the
+        // producer refills the stage while this warp does the arithmetic.
+        const bool mine = j < len;
+        Operands4 x;
+        if (mine) x = read_reduce4<R, ACC>(st, L, T, j);
         __syncwarp();
         if ((ct & 31) == 0) mbar_arrive(smem_addr(&empty_bar[s]));
+        if (mine) update_store4<R, FAST>(x, e0 + j, p);
     }
-    if (blockIdx.x == gridDim.x - 1 && ct < p.tail_len)
+    if (blockIdx.x == gridDim.x - 1 && group == 0 && ct < p.tail_len)
         tail_element<R, ACC, FAST>(p, p.tail_begin + ct);
 }
 
@@ -358,16 +392,25 @@ BulkKernel bulk_kernel_for(int R, bool acc, bool fast) {
 }
 
 // Tile length and stage count for R replicas: the largest tile (1024, 512
-// or 256 elements) that still gives at least 4 stages in the budget.
-void choose_tiling(int R, bool acc, int *tile, int *stages) {
-    for (int T = 1024; T >= 256; T /= 2) {
-        const int S = kSmemBudget / static_cast<int>(stage_layout(R, acc, T).bytes);
-        if (S >= 4 || T == 256) {
+// or 256 elements) that still gives every consumer group a stage and three
+// more stages in flight, within the budget.  The stage count is a multiple
+// of the group count, so that a stage's consecutive uses (tiles i and i + S)
+// always fall to the same group, which takes its tiles in order: a group
+// then never waits on a stage whose previous use has not completed, where
+// the parity test of the mbarrier would pass a phase early.  Returns false
+// if no tile leaves at least one stage per group.
+bool choose_tiling(int R, bool acc, int *tile, int *stages) {
+    for (int T = kMaxTile; T >= 256; T /= 2) {
+        int S = kSmemBudget / static_cast<int>(stage_layout(R, acc, T).bytes);
+        if (S >= kGroups + 3 || T == 256) {
+            S = S < kMaxStages ? S : kMaxStages;
+            S -= S % kGroups;
             *tile = T;
-            *stages = S < kMaxStages ? S : kMaxStages;
-            return;
+            *stages = S;
+            return S >= kGroups;
         }
     }
+    return false;
 }
 
 constexpr int kMaxDevices = 64;
@@ -400,7 +443,7 @@ cudaError_t launch_fused_bulk(const Slabs &s, const AdamScalars &c, size_t begin
     if (s.one_out) return cudaErrorInvalidValue;   // the bulk engine writes all R slabs
     BulkKernel kern = bulk_kernel_for(s.R, acc, s.fast);
     int T = 0, S = 0;
-    choose_tiling(s.R, acc, &T, &S);
+    if (!choose_tiling(s.R, acc, &T, &S)) return cudaErrorInvalidConfiguration;
     const unsigned smem = static_cast<unsigned>(S) * stage_layout(s.R, acc, T).bytes;
     {
         std::lock_guard<std::mutex> lock(g_smem_attr_mutex);

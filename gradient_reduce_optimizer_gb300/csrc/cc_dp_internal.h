@@ -34,11 +34,15 @@ struct Slabs {
     bool one_out = false;          // parameters to out[0] only (the multi-GPU
                                    // rank step; plain kernel, no accumulators)
     bool fast = false;             // the opt-in fast arithmetic (CC_ARITH_FAST)
+    bool bulk_copy = false;        // CTA budgets on the TMA bulk-copy engine
+                                   // (CC_ENGINE_BULK_COPY), not the wide kernel
 };
 
 // Enqueue the fused reduce + AdamW + redistribute kernel over elements
 // [begin, end) on `stream`.  Requires begin % CC_PAD_ELEMS == 0 and 16-byte
-// aligned slab bases (checked by the caller).  max_ctas > 0 caps the grid.
+// aligned slab bases (checked by the caller).  max_ctas > 0 launches the
+// CTA-budget form: at most max_ctas wide CTAs (one per SM), each thread
+// striding over the range.
 // chain = true launches it as a programmatic dependent of the kernel just
 // before it on `stream`, which must be a fused-step launch on a disjoint
 // element range (the next bucket of the same step).  wait_first = true
@@ -57,13 +61,16 @@ cudaError_t launch_fused_bulk(const Slabs &s, const AdamScalars &c, size_t begin
                               size_t end, int num_ctas, cudaStream_t stream);
 
 // The fused step over [begin, end) with the engine a CTA budget calls for:
-// max_ctas > 0 runs the bulk-copy engine on that many SMs, 0 the plain
-// kernel over the whole GPU (chained to the previous bucket if `chain`).
+// max_ctas > 0 runs the wide-CTA form of the fused kernel on that many SMs
+// (or, with s.bulk_copy, the TMA bulk-copy engine), 0 the plain kernel over
+// the whole GPU.  Either kernel form chains to the previous bucket if
+// `chain`.
 inline cudaError_t launch_step_range(const Slabs &s, const AdamScalars &c, size_t begin,
                                      size_t end, int max_ctas, bool chain,
                                      cudaStream_t stream) {
-    return max_ctas > 0 ? launch_fused_bulk(s, c, begin, end, max_ctas, stream)
-                        : launch_fused(s, c, begin, end, 0, chain, stream);
+    return (max_ctas > 0 && s.bulk_copy)
+               ? launch_fused_bulk(s, c, begin, end, max_ctas, stream)
+               : launch_fused(s, c, begin, end, max_ctas, chain, stream);
 }
 
 // Enqueue the unfused schedule of one bucket: reduce into `workspace`

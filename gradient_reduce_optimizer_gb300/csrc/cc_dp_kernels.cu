@@ -78,6 +78,10 @@ namespace {
 using namespace dev;
 
 constexpr int kThreads = CC_DP_THREADS;
+#ifndef CC_DP_WIDE_THREADS
+#define CC_DP_WIDE_THREADS 768  // threads of one CTA of the CTA-budget form
+#endif
+constexpr int kWideThreads = CC_DP_WIDE_THREADS;
 
 struct FusedParams {
     const uint4 *g[CC_MAX_R];      // 8 bf16 per vector
@@ -266,13 +270,16 @@ __device__ __forceinline__ void wait_for_predecessor_grid() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <int R, bool ACC, bool ONE_OUT, bool FAST>
-__global__ void __launch_bounds__(kThreads, CC_DP_MIN_BLOCKS)
+// THREADS = kThreads: the whole-GPU form, several CTAs per SM.  THREADS =
+// kWideThreads: the CTA-budget form, one wide CTA per SM and a grid of at
+// most the budget, each thread striding over the range.
+template <int R, bool ACC, bool ONE_OUT, bool FAST, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS == kThreads ? CC_DP_MIN_BLOCKS : 1)
 fused_step_kernel(const __grid_constant__ FusedParams p) {
     allow_dependents_to_launch();
     if (p.wait_first) wait_for_predecessor_grid();
-    const size_t stride = static_cast<size_t>(gridDim.x) * kThreads;
-    const size_t first = static_cast<size_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const size_t stride = static_cast<size_t>(gridDim.x) * THREADS;
+    const size_t first = static_cast<size_t>(blockIdx.x) * THREADS + threadIdx.x;
     if constexpr (threads_per_vector<ACC>() == 2) {
         for (size_t i = first; i < 2 * p.num_vec; i += stride)
             fused_half<R, ACC, ONE_OUT, FAST>(p, 2 * p.vec_begin + i);
@@ -401,34 +408,45 @@ using FusedKernel = void (*)(FusedParams);
 // The one-output form exists without accumulators and in the exact
 // arithmetic only (the multi-GPU rank step); other combinations with it are
 // null.
+// The wide (CTA-budget) form exists without the one-output switch.
 template <int R>
-FusedKernel pick_fused(bool acc, bool one_out, bool fast) {
-    if (one_out) return (acc || fast) ? nullptr : fused_step_kernel<R, false, true, false>;
+FusedKernel pick_fused(bool acc, bool one_out, bool fast, bool wide) {
+    if (wide) {
+        if (one_out) return nullptr;
+        if (fast)
+            return acc ? fused_step_kernel<R, true, false, true, kWideThreads>
+                       : fused_step_kernel<R, false, false, true, kWideThreads>;
+        return acc ? fused_step_kernel<R, true, false, false, kWideThreads>
+                   : fused_step_kernel<R, false, false, false, kWideThreads>;
+    }
+    if (one_out)
+        return (acc || fast) ? nullptr : fused_step_kernel<R, false, true, false, kThreads>;
     if (fast)
-        return acc ? fused_step_kernel<R, true, false, true>
-                   : fused_step_kernel<R, false, false, true>;
-    return acc ? fused_step_kernel<R, true, false, false>
-               : fused_step_kernel<R, false, false, false>;
+        return acc ? fused_step_kernel<R, true, false, true, kThreads>
+                   : fused_step_kernel<R, false, false, true, kThreads>;
+    return acc ? fused_step_kernel<R, true, false, false, kThreads>
+               : fused_step_kernel<R, false, false, false, kThreads>;
 }
 
-FusedKernel fused_kernel_for(int R, bool acc, bool one_out = false, bool fast = false) {
+FusedKernel fused_kernel_for(int R, bool acc, bool one_out = false, bool fast = false,
+                             bool wide = false) {
     switch (R) {
-        case 1: return pick_fused<1>(acc, one_out, fast);
-        case 2: return pick_fused<2>(acc, one_out, fast);
-        case 3: return pick_fused<3>(acc, one_out, fast);
-        case 4: return pick_fused<4>(acc, one_out, fast);
-        case 5: return pick_fused<5>(acc, one_out, fast);
-        case 6: return pick_fused<6>(acc, one_out, fast);
-        case 7: return pick_fused<7>(acc, one_out, fast);
-        case 8: return pick_fused<8>(acc, one_out, fast);
-        case 9: return pick_fused<9>(acc, one_out, fast);
-        case 10: return pick_fused<10>(acc, one_out, fast);
-        case 11: return pick_fused<11>(acc, one_out, fast);
-        case 12: return pick_fused<12>(acc, one_out, fast);
-        case 13: return pick_fused<13>(acc, one_out, fast);
-        case 14: return pick_fused<14>(acc, one_out, fast);
-        case 15: return pick_fused<15>(acc, one_out, fast);
-        case 16: return pick_fused<16>(acc, one_out, fast);
+        case 1: return pick_fused<1>(acc, one_out, fast, wide);
+        case 2: return pick_fused<2>(acc, one_out, fast, wide);
+        case 3: return pick_fused<3>(acc, one_out, fast, wide);
+        case 4: return pick_fused<4>(acc, one_out, fast, wide);
+        case 5: return pick_fused<5>(acc, one_out, fast, wide);
+        case 6: return pick_fused<6>(acc, one_out, fast, wide);
+        case 7: return pick_fused<7>(acc, one_out, fast, wide);
+        case 8: return pick_fused<8>(acc, one_out, fast, wide);
+        case 9: return pick_fused<9>(acc, one_out, fast, wide);
+        case 10: return pick_fused<10>(acc, one_out, fast, wide);
+        case 11: return pick_fused<11>(acc, one_out, fast, wide);
+        case 12: return pick_fused<12>(acc, one_out, fast, wide);
+        case 13: return pick_fused<13>(acc, one_out, fast, wide);
+        case 14: return pick_fused<14>(acc, one_out, fast, wide);
+        case 15: return pick_fused<15>(acc, one_out, fast, wide);
+        case 16: return pick_fused<16>(acc, one_out, fast, wide);
         default: return nullptr;
     }
 }
@@ -502,7 +520,8 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     cudaError_t e = device_info(&d);
     if (e != cudaSuccess) return e;
     const bool acc = s.acc[0] != nullptr;
-    FusedKernel kern = fused_kernel_for(s.R, acc, s.one_out, s.fast);
+    const bool wide = max_ctas > 0;
+    FusedKernel kern = fused_kernel_for(s.R, acc, s.one_out, s.fast, wide);
     if (!kern) return cudaErrorInvalidValue;
     FusedParams p{};
     for (int r = 0; r < s.R; ++r) {
@@ -523,17 +542,22 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
 
     const size_t units = p.num_vec * (acc ? threads_per_vector<true>()
                                           : threads_per_vector<false>());
-    size_t blocks = div_up(units, kThreads);
-    const size_t per_sm = CC_DP_BLOCKS_PER_SM > 0
-                              ? static_cast<size_t>(CC_DP_BLOCKS_PER_SM)
-                              : static_cast<size_t>(d->fused_blocks_per_sm[s.R][acc ? 1 : 0]);
-    const size_t resident = static_cast<size_t>(d->sm_count) * per_sm;
-    if (CC_DP_PERSISTENT && resident > 0 && blocks > resident) blocks = resident;
-    if (max_ctas > 0 && blocks > static_cast<size_t>(max_ctas)) blocks = max_ctas;
+    const int threads = wide ? kWideThreads : kThreads;
+    size_t blocks = div_up(units, static_cast<size_t>(threads));
+    if (wide) {
+        // the budget: at most max_ctas wide CTAs, one per SM
+        if (blocks > static_cast<size_t>(max_ctas)) blocks = max_ctas;
+    } else {
+        const size_t per_sm = CC_DP_BLOCKS_PER_SM > 0
+                                  ? static_cast<size_t>(CC_DP_BLOCKS_PER_SM)
+                                  : static_cast<size_t>(d->fused_blocks_per_sm[s.R][acc ? 1 : 0]);
+        const size_t resident = static_cast<size_t>(d->sm_count) * per_sm;
+        if (CC_DP_PERSISTENT && resident > 0 && blocks > resident) blocks = resident;
+    }
     if (blocks == 0) blocks = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

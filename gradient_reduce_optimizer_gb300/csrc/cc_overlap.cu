@@ -339,7 +339,7 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
     if (c.gemm_algo < 0) return fail(CC_ERR_INVALID, "gemm_algo=%d must be >= 0", c.gemm_algo);
     if (c.budget_buckets < 0)
         return fail(CC_ERR_INVALID, "budget_buckets=%d must be >= 0", c.budget_buckets);
-    if (c.arith_flags & ~CC_ARITH_FAST)
+    if (c.arith_flags & ~(CC_ARITH_FAST | CC_ENGINE_BULK_COPY))
         return fail(CC_ERR_INVALID, "arith_flags=%#x has unknown bits", c.arith_flags);
     if (c.num_buckets < 1 || !c.bucket_begin || !c.bucket_end || !c.bucket_ready_layer)
         return fail(CC_ERR_INVALID, "need at least one bucket");
@@ -363,6 +363,7 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
                         c.acc != nullptr, &slabs);
     if (st != CC_OK) return st;
     slabs.fast = (c.arith_flags & CC_ARITH_FAST) != 0;
+    slabs.bulk_copy = (c.arith_flags & CC_ENGINE_BULK_COPY) != 0;
     if (c.gemms_per_layer > 0) {
         if (!c.gemm_a || !c.gemm_b || !c.gemm_c)
             return fail(CC_ERR_INVALID, "GEMM operand buffers are NULL");

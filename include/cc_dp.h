@@ -172,10 +172,12 @@ CC_API int cc_fused_dp_step_accum(const void *const *grads, const float *const *
  * (acc may be NULL).  begin must be a multiple of CC_PAD_ELEMS (else
  * CC_ERR_MISALIGNED) and begin <= end <= n.
  *   max_ctas  0: the plain kernel over the whole GPU.  > 0: a CTA budget that
- *             leaves SMs to concurrent compute -- the bulk-copy engine runs
- *             one persistent CTA on each of at most max_ctas SMs, streaming
- *             tiles through shared memory with cp.async.bulk so that few SMs
- *             reach HBM bandwidth.  Same values either way.
+ *             leaves SMs to concurrent compute -- the same kernel in wide
+ *             CTAs (768 threads, one per SM) on at most max_ctas SMs, each
+ *             thread striding over the range with every load of its vector
+ *             in flight, so that few SMs reach HBM bandwidth (about 78 GB/s
+ *             per SM on GB300).  cc_fused_dp_bucket_ex can select the
+ *             bulk-copy engine instead.  Same values either way.
  */
 CC_API int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
                        float *master, float *m, float *v,
@@ -198,9 +200,19 @@ CC_API int cc_fused_dp_bucket(const void *const *grads, const float *const *acc,
  *                a few ulp of its update (well inside a relative 1e-5 of the
  *                parameter unless the update cancels it), the bf16 copies by
  *                at most one bf16 ulp.  Requires eps > 0 for that bound.
+ *                CC_ENGINE_BULK_COPY (or-ed in, with max_ctas > 0): the
+ *                budget runs on the TMA bulk-copy engine instead of the wide
+ *                CTAs -- one persistent CTA per SM whose producer warp
+ *                streams tiles into a ring of shared-memory stages with
+ *                cp.async.bulk and whose consumer warps reduce, update and
+ *                store them; every pipeline wait is bounded (cc_device_status
+ *                reports one that ran out).  It streams about 61 GB/s per SM
+ *                (the copies of one replica slice are 2 KB, and a bulk copy's
+ *                throughput falls with its size).  Same values.
  *                Other bits: CC_ERR_INVALID.
  */
 #define CC_ARITH_FAST 1u
+#define CC_ENGINE_BULK_COPY 2u
 CC_API int cc_fused_dp_bucket_ex(const void *const *grads, const float *const *acc,
                                  float *master, float *m, float *v,
                                  void *const *params_out, size_t n, int R, size_t begin,
@@ -459,8 +471,10 @@ typedef struct cc_overlap_cfg {
     int gemm_algo;                 /* 0: the proxy GEMMs through cublasGemmEx (cuBLAS's
                                       choice); k > 0: through cuBLASLt with the k-th
                                       candidate of its heuristic (no workspace) */
-    unsigned arith_flags;          /* the buckets' arithmetic: 0 exact, CC_ARITH_FAST
-                                      (see cc_fused_dp_bucket_ex) */
+    unsigned arith_flags;          /* the buckets' arithmetic and budget engine: 0
+                                      exact, or CC_ARITH_FAST and/or
+                                      CC_ENGINE_BULK_COPY (see
+                                      cc_fused_dp_bucket_ex) */
 } cc_overlap_cfg;
 
 typedef struct cc_overlap_result {
@@ -674,15 +688,17 @@ CC_API int cc_inject_launch_failure(int after_launches);
 /*
  * cc_inject_bulk_stall -- failure injection on the GPU without a fault, for
  * testing the bulk-copy engine's bounded waits.  Arms a one-shot for the
- * calling thread: in the next bulk-engine launch it makes (cc_fused_dp_bucket
- * with max_ctas > 0, or cc_overlap_bench with a CTA budget), the producer
- * never issues tile `tile` (tiles of 1024, 512 or 256 elements, counted from
- * the launch's first element; the CTA tile % grid owns it), and that
- * launch's pipeline waits give up after timeout_us (1..1000000) instead of
- * one second.  The consumers waiting for the tile then give up (status code
- * 1); a producer that comes back to the tile's stage gives up too (code 2);
+ * calling thread: in the next bulk-engine launch it makes
+ * (cc_fused_dp_bucket_ex with max_ctas > 0 and CC_ENGINE_BULK_COPY, or
+ * cc_overlap_bench with a CTA budget and that flag), the producer never
+ * issues tile `tile` (tiles of 1024, 512 or 256 elements, counted from the
+ * launch's first element; the CTA tile % grid owns it), and that launch's
+ * pipeline waits give up after timeout_us (1..1000000) instead of one
+ * second.  The consumers waiting for the tile then give up (status code 1);
+ * a producer that comes back to the tile's stage gives up too (code 2);
  * every copy issued still lands before the CTA exits.  The launch returns
- * with that CTA's range from the skipped tile on not stepped, and
+ * with the skipped tile, and possibly later tiles of its CTA, not stepped
+ * (each tile either stepped exactly or left as it was), and
  * cc_device_status reports the codes.  tile = -1 disarms.
  */
 CC_API int cc_inject_bulk_stall(long long tile, unsigned timeout_us);

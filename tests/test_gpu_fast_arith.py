@@ -37,10 +37,15 @@ def ordered(bits16):
     return np.where(b & 0x8000, 0x8000 - b, b)
 
 
-@pytest.mark.parametrize("R,n,max_ctas,use_acc,step", [
-    (1, 4099, 0, False, 1), (3, 100_003, 0, False, 7), (8, 100_003, 0, True, 10),
-    (3, 100_003, 16, False, 7), (8, 262_147, 16, True, 10), (16, 9_001, 5, False, 2)])
-def test_fast_step_within_the_bound(R, n, max_ctas, use_acc, step):
+BULK = capi.CC_ENGINE_BULK_COPY
+
+
+@pytest.mark.parametrize("R,n,max_ctas,use_acc,step,engine", [
+    (1, 4099, 0, False, 1, 0), (3, 100_003, 0, False, 7, 0), (8, 100_003, 0, True, 10, 0),
+    (3, 100_003, 16, False, 7, 0), (8, 262_147, 16, True, 10, 0), (16, 9_001, 5, False, 2, 0),
+    (3, 100_003, 16, False, 7, BULK), (8, 262_147, 16, True, 10, BULK),
+    (16, 9_001, 5, False, 2, BULK)])
+def test_fast_step_within_the_bound(R, n, max_ctas, use_acc, step, engine):
     grads, master, m, v = random_inputs(R, n, seed=90 + R, sigma=1e-3, step=step,
                                         premultiply=4.0)
     s = new_slabs(grads, master, m, v, with_acc=use_acc)
@@ -51,7 +56,8 @@ def test_fast_step_within_the_bound(R, n, max_ctas, use_acc, step):
     before = h_state[0].copy()
     hp = dict(HP, step=step)
     capi.cc_fused_dp_bucket_ex(s.grads, s.acc, s.master, s.m, s.v, s.outs, n, R, 0, n,
-                               max_ctas=max_ctas, arith_flags=capi.CC_ARITH_FAST, **hp)
+                               max_ctas=max_ctas, arith_flags=capi.CC_ARITH_FAST | engine,
+                               **hp)
     torch.cuda.synchronize()
     assert capi.cc_device_status() == 0
     ref_outs = oracle_step(h_grads, h_state, hp, acc=h_acc)
@@ -98,7 +104,8 @@ def test_fast_integer_gradients_keep_the_exact_sum():
 def test_unknown_arith_flags_rejected():
     R, n = 2, 64
     s = new_slabs(*random_inputs(R, n, seed=1))
-    with pytest.raises(capi.CCError) as ei:
-        capi.cc_fused_dp_bucket_ex(s.grads, None, s.master, s.m, s.v, s.outs, n, R, 0, n,
-                                   arith_flags=2, step=1, **HP)
-    assert ei.value.status == capi.CC_ERR_INVALID
+    for bad in (4, 8, 1 << 31):
+        with pytest.raises(capi.CCError) as ei:
+            capi.cc_fused_dp_bucket_ex(s.grads, None, s.master, s.m, s.v, s.outs, n, R, 0, n,
+                                       arith_flags=bad, step=1, **HP)
+        assert ei.value.status == capi.CC_ERR_INVALID

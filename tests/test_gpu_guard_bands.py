@@ -72,9 +72,9 @@ def test_guard_bands_around_every_slab_stay_intact(R, n):
     capi.cc_fused_dp_step(grads, master, m, v, outs, n, R, 2048, **HP)
     capi.cc_fused_dp_step_accum(grads, acc, master, m, v, outs, n, R, 2048, accum_k=3, **HP)
     for use_acc in (None, acc):
-        for ctas in (0, 7):
-            capi.cc_fused_dp_bucket(grads, use_acc, master, m, v, outs, n, R, 0, n,
-                                    max_ctas=ctas, **HP)
+        for ctas, flags in ((0, 0), (7, 0), (7, capi.CC_ENGINE_BULK_COPY)):
+            capi.cc_fused_dp_bucket_ex(grads, use_acc, master, m, v, outs, n, R, 0, n,
+                                       max_ctas=ctas, arith_flags=flags, **HP)
     cut = n // 16 * 8
     for b, e in ((0, cut), (cut, n)):
         shard = [guarded(torch.float32, f"{nm} shard [{b}, {e})", t[b:e], length=e - b)

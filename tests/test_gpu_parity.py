@@ -442,51 +442,61 @@ def test_full_size_bert_large_accumulation_k4():
 
 
 # ---------------------------------------------------------------------------
-# The bulk-copy engine (a CTA budget: cc_fused_dp_bucket with max_ctas > 0)
+# CTA budgets (cc_fused_dp_bucket with max_ctas > 0): the wide-CTA kernel,
+# and the TMA bulk-copy engine (CC_ENGINE_BULK_COPY)
 # ---------------------------------------------------------------------------
 
-def bulk_step(s, hp, max_ctas, begin=0, end=None, use_acc=False):
+ENGINES = {"wide": 0, "bulk_copy": capi.CC_ENGINE_BULK_COPY}
+
+
+def bulk_step(s, hp, max_ctas, begin=0, end=None, use_acc=False, engine="wide"):
     end = s.n if end is None else end
-    capi.cc_fused_dp_bucket(s.grads, s.acc if use_acc else None, s.master, s.m, s.v,
-                            s.outs, s.n, s.R, begin, end, max_ctas=max_ctas, **hp)
+    capi.cc_fused_dp_bucket_ex(s.grads, s.acc if use_acc else None, s.master, s.m, s.v,
+                               s.outs, s.n, s.R, begin, end, max_ctas=max_ctas,
+                               arith_flags=ENGINES[engine], **hp)
 
 
-def check_bulk(s, hp, max_ctas, use_acc=False, label=""):
+def check_bulk(s, hp, max_ctas, use_acc=False, label="", engine="wide"):
     grads, state, acc = host_copy(s)
-    bulk_step(s, hp, max_ctas, use_acc=use_acc)
+    bulk_step(s, hp, max_ctas, use_acc=use_acc, engine=engine)
     torch.cuda.synchronize()
     outs = oracle_step(grads, state, hp, acc=acc if use_acc else None)
     compare_all(s, state, outs, label=label)
     assert capi.cc_device_status() == 0
 
 
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("n", [1, 7, 8, 9, 1023, 1024, 1025, 4096 + 3, 300_007])
 @pytest.mark.parametrize("R", [1, 3, 8, 16])
-def test_bulk_engine_ragged(R, n):
+def test_bulk_engine_ragged(R, n, engine):
     s = new_slabs(*random_inputs(R, n, seed=500 + R * 7 + n % 97, step=4))
-    check_bulk(s, dict(HP10, step=4), max_ctas=5, label=f"bulk R={R} n={n} ")
+    check_bulk(s, dict(HP10, step=4), max_ctas=5, label=f"{engine} R={R} n={n} ",
+               engine=engine)
 
 
+@pytest.mark.parametrize("engine", list(ENGINES))
 @pytest.mark.parametrize("R", [1, 2, 8, 16])
 @pytest.mark.parametrize("max_ctas", [1, 3, 152, 1000])
-def test_bulk_engine_accumulators(R, max_ctas):
-    """With accumulators the tile shrinks to 512 (R=8) or 256 (R=16)."""
+def test_bulk_engine_accumulators(R, max_ctas, engine):
+    """With accumulators the bulk-copy engine's tile shrinks to 512 (R=8)
+    or 256 (R=16)."""
     n = 100_003
     s = new_slabs(*random_inputs(R, n, seed=R + max_ctas, step=3), with_acc=True)
     g = torch.Generator(device=DEV)
     g.manual_seed(17)
     for a in s.acc:
         a.copy_(torch.randn(n, generator=g, device=DEV) * 1e-3)
-    check_bulk(s, dict(HP10, step=3), max_ctas, use_acc=True)
+    check_bulk(s, dict(HP10, step=3), max_ctas, use_acc=True, engine=engine)
 
 
-def test_bulk_engine_subrange_leaves_the_rest_untouched():
+@pytest.mark.parametrize("engine", list(ENGINES))
+def test_bulk_engine_subrange_leaves_the_rest_untouched(engine):
     n = 50_000
     s = new_slabs(*random_inputs(4, n, seed=99, step=2))
     before = [t.clone() for t in (s.master, s.m, s.v)] + [o.clone() for o in s.outs]
     grads, state, _ = host_copy(s)
     b, e = 8 * 1000, 8 * 4000 + 5
-    bulk_step(s, dict(HP10, step=2), 7, begin=b, end=e)
+    bulk_step(s, dict(HP10, step=2), 7, begin=b, end=e, engine=engine)
     torch.cuda.synchronize()
     sub = [x[b:e].copy() for x in state]
     outs = oracle_step([g_[b:e].copy() for g_ in grads], sub, dict(HP10, step=2))
@@ -500,7 +510,40 @@ def test_bulk_engine_subrange_leaves_the_rest_untouched():
     assert capi.cc_device_status() == 0
 
 
-def test_full_size_bert_large_r8_bulk_engine():
+@pytest.mark.parametrize("engine", list(ENGINES))
+@pytest.mark.parametrize("ctas", [48, 96, 152])
+def test_bulk_engine_streams_every_sm(ctas, engine):
+    """2^25 elements at R = 8 (32,768 bulk-copy tiles, hundreds per CTA) on
+    48, 96 and all 152 SMs: the bulk-copy engine's consumer groups run far
+    apart in time, and no group may read a stage before its fill has
+    landed.  Every element equals the oracle and no pipeline wait runs out.
+    The opt-in fast arithmetic on the same inputs gives the same bits as the
+    whole-GPU kernel's."""
+    R, n = 8, 1 << 25
+    capi.cc_device_status(clear=True)
+    inputs = random_inputs(R, n, seed=1000 + ctas, step=6)
+    s = new_slabs(*[x if isinstance(x, list) else x.clone() for x in inputs])
+    grads, state, _ = host_copy(s)
+    hp = dict(HP10, step=6)
+    bulk_step(s, hp, ctas, engine=engine)
+    torch.cuda.synchronize()
+    assert capi.cc_device_status() == 0
+    compare_all(s, state, oracle_step(grads, state, hp), label=f"{engine} {ctas} CTAs ")
+    a = new_slabs(*[x if isinstance(x, list) else x.clone() for x in inputs])
+    b = new_slabs(*[x if isinstance(x, list) else x.clone() for x in inputs])
+    for slabs, budget in ((a, ctas), (b, 0)):
+        capi.cc_fused_dp_bucket_ex(slabs.grads, None, slabs.master, slabs.m, slabs.v,
+                                   slabs.outs, n, R, 0, n, max_ctas=budget,
+                                   arith_flags=capi.CC_ARITH_FAST | ENGINES[engine], **hp)
+    torch.cuda.synchronize()
+    assert capi.cc_device_status() == 0
+    for x, y in zip([a.master, a.m, a.v] + a.outs, [b.master, b.m, b.v] + b.outs):
+        bits = torch.int16 if x.dtype == torch.bfloat16 else torch.int32
+        assert torch.equal(x.view(bits), y.view(bits))
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
+def test_full_size_bert_large_r8_bulk_engine(engine):
     """The 336M R=8 slab in its planned buckets on a 64-SM budget."""
     w = wl.bert_large_r8()
     s, offsets, n_slab = planned_workload_slabs(w)
@@ -508,8 +551,9 @@ def test_full_size_bert_large_r8_bulk_engine():
     idx = sample_indices(n_slab, [b for b, _ in buckets] + offsets, 1 << 20, seed=4)
     grads, state, _ = host_copy(s, idx)
     for b, e in buckets:
-        capi.cc_fused_dp_bucket(s.grads, None, s.master, s.m, s.v, s.outs, n_slab,
-                                w.R, b, e, max_ctas=64, **hp_of(w))
+        capi.cc_fused_dp_bucket_ex(s.grads, None, s.master, s.m, s.v, s.outs, n_slab,
+                                   w.R, b, e, max_ctas=64, arith_flags=ENGINES[engine],
+                                   **hp_of(w))
     torch.cuda.synchronize()
     compare_all(s, state, oracle_step(grads, state, hp_of(w)), idx=idx)
     assert capi.cc_device_status() == 0

@@ -64,9 +64,11 @@ def test_random_configuration(case):
     elif engine == "bucket_bulk":
         per = max(8, bucket_bytes // 16 * 8) if bucket_bytes else n
         ctas = rnd.choice([1, 3, 16, 152])
+        flags = rnd.choice([0, capi.CC_ENGINE_BULK_COPY])   # wide CTAs or bulk copies
         for b in range(0, n, per):
-            capi.cc_fused_dp_bucket(grads, None, master, m, v, outs, n, R, b,
-                                    min(n, b + per), max_ctas=ctas, **hp)
+            capi.cc_fused_dp_bucket_ex(grads, None, master, m, v, outs, n, R, b,
+                                       min(n, b + per), max_ctas=ctas, arith_flags=flags,
+                                       **hp)
     elif engine == "unfused":
         per = max(8, bucket_bytes // 16 * 8) if bucket_bytes else n
         ws = torch.empty(min(per, n), dtype=torch.float32, device=DEV)
