@@ -82,6 +82,10 @@ constexpr int kThreads = CC_DP_THREADS;
 #define CC_DP_WIDE_THREADS 768  // threads of one CTA of the CTA-budget form
 #endif
 constexpr int kWideThreads = CC_DP_WIDE_THREADS;
+#ifndef CC_DP_WIDE_V8
+#define CC_DP_WIDE_V8 1         // the wide form's fp32 state in 256-bit accesses where aligned
+#endif
+constexpr bool kWideV8 = CC_DP_WIDE_V8 != 0;
 
 struct FusedParams {
     const uint4 *g[CC_MAX_R];      // 8 bf16 per vector
@@ -94,12 +98,30 @@ struct FusedParams {
     size_t tail_begin;             // first element of the partial vector
     int tail_len;                  // 0..7 elements after the full vectors
     int wait_first;                // wait for the preceding grid before any access
+    int v8;                        // master/m/v 32-byte aligned: 256-bit accesses (wide form)
 };
+
+// 256-bit streaming accesses of 8 consecutive floats (sm_100 and later; the
+// address must be 32-byte aligned).
+__device__ __forceinline__ void ldcs8(const float *p, float (&r)[8]) {
+    asm volatile("ld.global.cs.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]),
+                   "=f"(r[6]), "=f"(r[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void stcs8(float *p, const float (&r)[8]) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(p), "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]),
+                   "f"(r[6]), "f"(r[7])
+                 : "memory");
+}
 
 // ONE_OUT: the parameters go to out[0] only (one rank's own slab in the
 // multi-GPU form, from where the AllGather distributes them); otherwise to
 // all R replica slabs.
-template <int R, bool ACC, bool ONE_OUT, bool FAST>
+// V8: the fp32 state moves as one 32-byte access per array instead of two
+// 16-byte ones (fewer memory instructions; the wide CTA-budget form).
+template <int R, bool ACC, bool ONE_OUT, bool FAST, bool V8 = false>
 __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
     // Issue every load of this vector before any arithmetic.
     uint4 gq[R];
@@ -113,9 +135,25 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
             aq[r][1] = __ldcs(p.acc[r] + 2 * vi + 1);
         }
     }
-    const float4 w0 = __ldcs(p.master + 2 * vi), w1 = __ldcs(p.master + 2 * vi + 1);
-    const float4 m0 = __ldcs(p.m + 2 * vi), m1 = __ldcs(p.m + 2 * vi + 1);
-    const float4 v0 = __ldcs(p.v + 2 * vi), v1 = __ldcs(p.v + 2 * vi + 1);
+    float pw[8], mm[8], vv[8];
+    if constexpr (V8) {
+        ldcs8(reinterpret_cast<const float *>(p.master) + 8 * vi, pw);
+        ldcs8(reinterpret_cast<const float *>(p.m) + 8 * vi, mm);
+        ldcs8(reinterpret_cast<const float *>(p.v) + 8 * vi, vv);
+    } else {
+        const float4 w0 = __ldcs(p.master + 2 * vi), w1 = __ldcs(p.master + 2 * vi + 1);
+        const float4 m0 = __ldcs(p.m + 2 * vi), m1 = __ldcs(p.m + 2 * vi + 1);
+        const float4 v0 = __ldcs(p.v + 2 * vi), v1 = __ldcs(p.v + 2 * vi + 1);
+        const float w8[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const float m8[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        const float v8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            pw[k] = w8[k];
+            mm[k] = m8[k];
+            vv[k] = v8[k];
+        }
+    }
 
     // Reduce in replica order.
     float s[8];
@@ -141,18 +179,21 @@ __device__ __forceinline__ void fused_vector(const FusedParams &p, size_t vi) {
         }
     }
 
-    float pw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    float mm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) adamw_step<FAST>(s[k], pw[k], mm[k], vv[k], p.c);
 
-    __stcs(p.master + 2 * vi, make_float4(pw[0], pw[1], pw[2], pw[3]));
-    __stcs(p.master + 2 * vi + 1, make_float4(pw[4], pw[5], pw[6], pw[7]));
-    __stcs(p.m + 2 * vi, make_float4(mm[0], mm[1], mm[2], mm[3]));
-    __stcs(p.m + 2 * vi + 1, make_float4(mm[4], mm[5], mm[6], mm[7]));
-    __stcs(p.v + 2 * vi, make_float4(vv[0], vv[1], vv[2], vv[3]));
-    __stcs(p.v + 2 * vi + 1, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    if constexpr (V8) {
+        stcs8(reinterpret_cast<float *>(p.master) + 8 * vi, pw);
+        stcs8(reinterpret_cast<float *>(p.m) + 8 * vi, mm);
+        stcs8(reinterpret_cast<float *>(p.v) + 8 * vi, vv);
+    } else {
+        __stcs(p.master + 2 * vi, make_float4(pw[0], pw[1], pw[2], pw[3]));
+        __stcs(p.master + 2 * vi + 1, make_float4(pw[4], pw[5], pw[6], pw[7]));
+        __stcs(p.m + 2 * vi, make_float4(mm[0], mm[1], mm[2], mm[3]));
+        __stcs(p.m + 2 * vi + 1, make_float4(mm[4], mm[5], mm[6], mm[7]));
+        __stcs(p.v + 2 * vi, make_float4(vv[0], vv[1], vv[2], vv[3]));
+        __stcs(p.v + 2 * vi + 1, make_float4(vv[4], vv[5], vv[6], vv[7]));
+    }
     uint4 o;
     o.x = pack_bf16x2(pw[0], pw[1]);
     o.y = pack_bf16x2(pw[2], pw[3]);
@@ -283,6 +324,9 @@ fused_step_kernel(const __grid_constant__ FusedParams p) {
     if constexpr (threads_per_vector<ACC>() == 2) {
         for (size_t i = first; i < 2 * p.num_vec; i += stride)
             fused_half<R, ACC, ONE_OUT, FAST>(p, 2 * p.vec_begin + i);
+    } else if (kWideV8 && THREADS == kWideThreads && p.v8) {
+        for (size_t i = first; i < p.num_vec; i += stride)
+            fused_vector<R, ACC, ONE_OUT, FAST, true>(p, p.vec_begin + i);
     } else {
         for (size_t i = first; i < p.num_vec; i += stride)
             fused_vector<R, ACC, ONE_OUT, FAST>(p, p.vec_begin + i);
@@ -537,6 +581,8 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     p.num_vec = (end - begin) / CC_PAD_ELEMS;
     p.tail_begin = begin + p.num_vec * CC_PAD_ELEMS;
     p.tail_len = static_cast<int>(end - p.tail_begin);
+    p.v8 = wide && ((reinterpret_cast<uintptr_t>(s.master) | reinterpret_cast<uintptr_t>(s.m) |
+                     reinterpret_cast<uintptr_t>(s.v)) % 32 == 0);
     wait_first = wait_first && CC_DP_PDL_FIRST;
     p.wait_first = wait_first && CC_DP_PDL;
 

@@ -543,6 +543,26 @@ def test_bulk_engine_streams_every_sm(ctas, engine):
 
 
 @pytest.mark.parametrize("engine", list(ENGINES))
+@pytest.mark.parametrize("offset", [0, 4])
+def test_budget_slabs_aligned_to_16_or_32_bytes(engine, offset):
+    """Under a CTA budget the wide form moves the fp32 state in 32-byte
+    accesses when master, m and v are 32-byte aligned, and in 16-byte ones
+    when they are only 16-byte aligned (offset 4 floats): same bits."""
+    R, n = 8, 300_007
+    grads, master, m, v = random_inputs(R, n, seed=63 + offset, step=5)
+
+    def place(t):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=DEV)
+        view = buf[offset:offset + t.numel()]
+        assert view.data_ptr() % 32 == (16 if offset else 0)
+        view.copy_(t)
+        return view
+    s = new_slabs(grads, place(master), place(m), place(v))
+    check_bulk(s, dict(HP10, step=5), max_ctas=11, label=f"{engine} +{4 * offset} B ",
+               engine=engine)
+
+
+@pytest.mark.parametrize("engine", list(ENGINES))
 def test_full_size_bert_large_r8_bulk_engine(engine):
     """The 336M R=8 slab in its planned buckets on a 64-SM budget."""
     w = wl.bert_large_r8()
