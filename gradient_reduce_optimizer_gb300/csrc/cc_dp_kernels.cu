@@ -86,6 +86,10 @@ constexpr int kWideThreads = CC_DP_WIDE_THREADS;
 #define CC_DP_WIDE_V8 1         // the wide form's fp32 state in 256-bit accesses where aligned
 #endif
 constexpr bool kWideV8 = CC_DP_WIDE_V8 != 0;
+#ifndef CC_DP_FULL_V8
+#define CC_DP_FULL_V8 0         // the whole-GPU form too (measured slower: off)
+#endif
+constexpr bool kFullV8 = CC_DP_FULL_V8 != 0;
 
 struct FusedParams {
     const uint4 *g[CC_MAX_R];      // 8 bf16 per vector
@@ -324,7 +328,8 @@ fused_step_kernel(const __grid_constant__ FusedParams p) {
     if constexpr (threads_per_vector<ACC>() == 2) {
         for (size_t i = first; i < 2 * p.num_vec; i += stride)
             fused_half<R, ACC, ONE_OUT, FAST>(p, 2 * p.vec_begin + i);
-    } else if (kWideV8 && THREADS == kWideThreads && p.v8) {
+    } else if (((kWideV8 && THREADS == kWideThreads) || (kFullV8 && THREADS == kThreads)) &&
+               p.v8) {
         for (size_t i = first; i < p.num_vec; i += stride)
             fused_vector<R, ACC, ONE_OUT, FAST, true>(p, p.vec_begin + i);
     } else {
@@ -581,7 +586,7 @@ cudaError_t launch_fused(const Slabs &s, const AdamScalars &c, size_t begin,
     p.num_vec = (end - begin) / CC_PAD_ELEMS;
     p.tail_begin = begin + p.num_vec * CC_PAD_ELEMS;
     p.tail_len = static_cast<int>(end - p.tail_begin);
-    p.v8 = wide && ((reinterpret_cast<uintptr_t>(s.master) | reinterpret_cast<uintptr_t>(s.m) |
+    p.v8 = (wide || kFullV8) && ((reinterpret_cast<uintptr_t>(s.master) | reinterpret_cast<uintptr_t>(s.m) |
                      reinterpret_cast<uintptr_t>(s.v)) % 32 == 0);
     wait_first = wait_first && CC_DP_PDL_FIRST;
     p.wait_first = wait_first && CC_DP_PDL;
