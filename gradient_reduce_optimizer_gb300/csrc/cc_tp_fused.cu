@@ -1269,8 +1269,12 @@ size_t tail_counter_bytes(int tail_groups) {
 
 // The pair kernel's schedule: how many clusters run, and which groups are
 // split into rank phases.  The last wave is split when its groups do not
-// fill every cluster and splitting shortens it: ceil(tail * R / clusters)
-// phases per cluster instead of R (so never for R = 1).
+// fill every cluster and each cluster then has at most one split phase:
+// tail * R <= clusters (and R > 1).  A split phase costs far more than its
+// share of the MMAs -- its product goes out in fp32 and the last of the R
+// reads them all back and stores the R outputs -- so on the GPT-2 MLP
+// layer (m = 8192, 4 groups left over) it gains 0.035 ms, while spreading
+// 40 leftover groups over 5 phases per cluster (m = 4096) loses 0.12 ms.
 struct PairPlan {
     int clusters, full_groups, tail_phases;
     size_t ws_bytes;                                     // 0: nothing split
@@ -1317,7 +1321,7 @@ int pair_plan(int m, int n, int R, int max_ctas, bool split, PairPlan *plan) {
     if (max_ctas > 0 && 2 * clusters > max_ctas) clusters = max_ctas / 2;
     if (clusters < 1) clusters = 1;
     const int tail = num_groups % clusters;
-    if (split && tail > 0 && tail * R <= (R - 1) * clusters) {
+    if (split && tail > 0 && R > 1 && tail * R <= clusters) {
         plan->full_groups = num_groups - tail;
         plan->tail_phases = tail * R;
         plan->clusters = plan->full_groups > 0 ? clusters : std::min(clusters, tail * R);
@@ -1412,17 +1416,60 @@ int launch_bn(TpFusedParams &p, const void *const *x, const void *const *w, int 
 }
 #endif
 
-// The tile width for n output columns.  The pair kernel prefers 256 (fewer
-// operand bytes per FLOP: 0.464 ms on the GPT-2 MLP shape against 0.478 ms
-// at 192, despite 384 tile pairs filling 76 clusters only 5.05 times); the
-// single-CTA kernel 192 (16 column tiles for n = 3072), then 256, then 128.
-int pick_bn(int n, bool pair) {
+// The single-CTA kernel's tile width for n output columns: 192 (16 column
+// tiles for n = 3072), then 256, then 128.  The pair kernel's is chosen by
+// pick_pair_bn.
+int pick_bn(int n, bool) {
 #ifdef CC_TP_BN
-    (void)pair;
     return n % CC_TP_BN == 0 ? CC_TP_BN : 0;
 #else
-    if (pair && n % 256 == 0) return 256;
     return n % 192 == 0 ? 192 : n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 0;
+#endif
+}
+
+// The pair kernel's modelled time at tile width BN: its waves (a split last
+// wave counted as half) times one wave's operand intake per CTA and k-block,
+// X 128 x 64 plus half of W (BN/2 x 64) in bf16 = 16384 + 64 BN bytes.  One
+// SM's operand intake bounds a wave, so this ranks the widths: on the GPT-2
+// MLP layer (R = 8, n = 3072, k = 12288) it picks 256 at m = 4096 and 8192
+// (measured 0.228 / 0.4155 ms against 0.264 / 0.457 at 192) and 192 at
+// m = 2048 (0.137 against 0.154), where both widths take two waves.
+template <int BN>
+int pair_cost(int m, int n, int R, int max_ctas, bool split, double *cost) {
+    *cost = -1.0;
+    if (n % BN != 0) return CC_OK;
+    PairPlan plan;
+    const int st = pair_plan<BN>(m, n, R, max_ctas, split, &plan);
+    if (st != CC_OK) return st;
+    const int full_waves = plan.full_groups / plan.clusters;
+    const double waves = full_waves + (plan.tail_phases > 0 ? 0.5
+                                       : plan.full_groups % plan.clusters ? 1.0 : 0.0);
+    *cost = waves * (16384.0 + 64.0 * BN);
+    return CC_OK;
+}
+
+// The pair kernel's tile width for this shape and budget (0: n fits none).
+int pick_pair_bn(int m, int n, int R, int max_ctas, bool split, int *bn) {
+#ifdef CC_TP_BN
+    (void)m; (void)R; (void)max_ctas; (void)split;
+    *bn = n % CC_TP_BN == 0 ? CC_TP_BN : 0;
+    return CC_OK;
+#else
+    double c256, c192, c128;
+    int st;
+    if ((st = pair_cost<256>(m, n, R, max_ctas, split, &c256)) != CC_OK) return st;
+    if ((st = pair_cost<192>(m, n, R, max_ctas, split, &c192)) != CC_OK) return st;
+    if ((st = pair_cost<128>(m, n, R, max_ctas, split, &c128)) != CC_OK) return st;
+    *bn = 0;
+    double best = 0.0;
+    const int widths[3] = {256, 192, 128};
+    const double costs[3] = {c256, c192, c128};
+    for (int i = 0; i < 3; ++i)
+        if (costs[i] >= 0.0 && (*bn == 0 || costs[i] < best)) {
+            *bn = widths[i];
+            best = costs[i];
+        }
+    return CC_OK;
 #endif
 }
 
@@ -1441,7 +1488,13 @@ int launch_tp_fused(const void *const *x, const void *const *w, void *const *out
     p.m = m;
     p.n = n;
     p.kb_per_rank = kr / kBK;
-    switch (pick_bn(n, CC_TP_PAIR && (m / kBM) % 2 == 0)) {
+    const bool pair = CC_TP_PAIR && (m / kBM) % 2 == 0;
+    int bn = pick_bn(n, false);
+    if (pair) {
+        const int st = pick_pair_bn(m, n, R, max_ctas, ws != nullptr, &bn);
+        if (st != CC_OK) return st;
+    }
+    switch (bn) {
         case 128: return launch_bn<128>(p, x, w, m, n, kr, R, max_ctas, ws, ws_bytes, stream);
         case 192: return launch_bn<192>(p, x, w, m, n, kr, R, max_ctas, ws, ws_bytes, stream);
         case 256: return launch_bn<256>(p, x, w, m, n, kr, R, max_ctas, ws, ws_bytes, stream);
@@ -1457,8 +1510,10 @@ int tp_fused_workspace(int m, int n, int R, int max_ctas, size_t *bytes) {
     *bytes = 0;
     if (!CC_TP_PAIR || (m / kBM) % 2 != 0) return CC_OK;   // the single-CTA kernel
     PairPlan plan;
-    int st = CC_OK;
-    switch (pick_bn(n, true)) {
+    int bn = 0;
+    int st = pick_pair_bn(m, n, R, max_ctas, true, &bn);
+    if (st != CC_OK) return st;
+    switch (bn) {
         case 128: st = pair_plan<128>(m, n, R, max_ctas, true, &plan); break;
         case 192: st = pair_plan<192>(m, n, R, max_ctas, true, &plan); break;
         case 256: st = pair_plan<256>(m, n, R, max_ctas, true, &plan); break;

@@ -627,9 +627,10 @@ CC_API int cc_tp_matmul_allreduce(const void *const *x, const void *const *w,
  * workspace and budget.
  *
  * The kernel runs persistent CTA pairs, each taking one pair of 128-row
- * output tiles ("group") through all R ranks.  When the groups do not fill
- * the last wave, a workspace lets the kernel split that wave's groups into
- * their R rank products, spread over every pair: each product goes to the
+ * output tiles ("group") through all R ranks.  When a few groups are left
+ * for a last wave (at most pairs / R of them), a workspace lets the kernel
+ * split them into their R rank products, spread over the pairs, at most
+ * one each: each product goes to the
  * workspace as fp32 and the pair that finishes a group's last product
  * (counted with one atomic per group half; no CTA waits for another) adds
  * the R products in rank order and writes the bf16 outputs.
@@ -655,7 +656,9 @@ CC_API int cc_tp_matmul_allreduce_ex(const void *const *x, const void *const *w,
  * cc_tp_matmul_allreduce_workspace -- the workspace bytes
  * cc_tp_matmul_allreduce_ex uses for this shape and max_ctas on the current
  * device: 0 when it splits nothing (R = 1, groups that fill every wave, a
- * wave whose splitting would not shorten it, or an odd count of row tiles).
+ * leftover wave of more than pairs / R groups -- it is split only where
+ * every CTA pair gets at most one rank product of it -- or an odd count of
+ * row tiles).
  * Otherwise 256 bytes of counters per 32 split groups plus 2 x 128 x BN x R
  * fp32 products per split group (BN = 256, 192 or 128, the tile width the
  * kernel picks for n).  Shape errors as cc_tp_matmul_allreduce.

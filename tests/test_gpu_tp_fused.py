@@ -45,11 +45,22 @@ def operands(R, m, n, k, seed, integer):
 
 
 # Schedules: (workspace?, CTA budget).  Without a workspace every group of
-# output tiles runs whole; with one the last wave's groups are split into
-# rank products summed by the last to finish.  A budget of 6 CTAs (3 pairs)
-# gives several whole waves per pair followed by a split wave.
+# output tiles runs whole; with one, a small last wave's groups are split
+# into rank products summed by the last to finish.  A budget of 6 CTAs (3
+# pairs) gives several whole waves per pair.  "split-budget" takes the
+# smallest budget for which the library splits (it asks the workspace
+# query); for the pair shapes with R > 1 one exists, and with it the
+# groups before the split wave run whole.
 SCHEDULES = {"whole": (False, 0), "split": (True, 0), "whole-3pairs": (False, 6),
-             "split-3pairs": (True, 6)}
+             "split-budget": (True, None)}
+
+
+def split_budget(m, n, k, R):
+    """The smallest CTA budget at which the last wave is split (0: none)."""
+    for ctas in range(4, 153, 2):
+        if capi.cc_tp_matmul_allreduce_workspace(m, n, k, R, ctas) > 0:
+            return ctas
+    return 0
 
 
 def run(x, w, m, n, k, R, with_partials=True, schedule="whole"):
@@ -61,9 +72,11 @@ def run(x, w, m, n, k, R, with_partials=True, schedule="whole"):
     if schedule == "whole":
         capi.cc_tp_matmul_allreduce(x, w, outs, parts, m, n, k, R)
     else:
+        if max_ctas is None:
+            max_ctas = split_budget(m, n, k, R)
+            if (m // 128) % 2 == 0 and R > 1:
+                assert max_ctas > 0              # these shapes can split a last wave
         ws_bytes = capi.cc_tp_matmul_allreduce_workspace(m, n, k, R, max_ctas) if split else 0
-        if schedule == "split-3pairs" and (m // 128) % 2 == 0 and R > 1:
-            assert ws_bytes > 0                  # these shapes do split their last wave
         ws = (torch.full((max(ws_bytes, 16),), 0x7F, dtype=torch.uint8, device=DEV)
               if split else None)
         capi.cc_tp_matmul_allreduce_ex(x, w, outs, parts, m, n, k, R, ws, ws_bytes, max_ctas)
@@ -104,7 +117,7 @@ def test_integer_operands_are_exact(R, m, n, k, schedule):
         assert_bits(f"out[{r}]", u16(outs[r]).ravel(), want16, "bf16")
 
 
-@pytest.mark.parametrize("schedule", ["whole", "split-3pairs"])
+@pytest.mark.parametrize("schedule", ["whole", "split-budget"])
 @pytest.mark.parametrize("R,m,n,k", SHAPES)
 def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k, schedule):
     x, w = operands(R, m, n, k, seed=21 + R, integer=False)
@@ -122,7 +135,7 @@ def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k, schedu
         assert np.all(err <= bound), f"partial {r}: max excess {np.max(err - bound)}"
     # neither the debug store of the partials nor the schedule changes an
     # output bit
-    for other in ("whole", "split", "split-3pairs"):
+    for other in ("whole", "split", "split-budget", "whole-3pairs"):
         outs2, _ = run(x, w, m, n, k, R, with_partials=False, schedule=other)
         for r in range(R):
             assert torch.equal(outs2[r].view(torch.int16), outs[r].view(torch.int16)), other
@@ -163,17 +176,18 @@ def test_rejects_small_workspace_and_one_cta():
     R, m, n, k = 4, 512, 640, 256
     x, w = operands(R, m, n, k, seed=4, integer=True)
     outs = [torch.empty(m, n, dtype=torch.bfloat16, device=DEV) for _ in range(R)]
-    need = capi.cc_tp_matmul_allreduce_workspace(m, n, k, R, 6)
-    assert need > 0
+    ctas = split_budget(m, n, k, R)
+    need = capi.cc_tp_matmul_allreduce_workspace(m, n, k, R, ctas)
+    assert ctas > 0 and need > 0
     ws = torch.empty(need, dtype=torch.uint8, device=DEV)
     with pytest.raises(capi.CCError) as ei:
-        capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, ws, need - 16, 6)
+        capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, ws, need - 16, ctas)
     assert ei.value.status == capi.CC_ERR_INVALID
     with pytest.raises(capi.CCError) as ei:
         capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, None, 0, 1)
     assert ei.value.status == capi.CC_ERR_INVALID
     with pytest.raises(capi.CCError) as ei:
-        capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, outs[1], need, 6)
+        capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, outs[1], need, ctas)
     assert ei.value.status == capi.CC_ERR_ALIAS
     # one split-free launch later nothing is left armed
     torch.cuda.synchronize()
