@@ -722,6 +722,11 @@ tp_fused_kernel(const __grid_constant__ TpFusedParams p) {
 // TMEM is allocated for the pair (both CTAs' allocating warps take part).
 // ---------------------------------------------------------------------------
 
+#ifndef CC_TP_PAIR_SMEM
+#define CC_TP_PAIR_SMEM (220 * 1024)  // stages + output boxes of the pair kernel (226 KB, a
+                                      // sixth stage at 256 columns, measured no faster)
+#endif
+
 template <int BN>
 struct PairCfg {
     static_assert(BN % 64 == 0 && BN <= kAccCols, "BN: 128, 192 or 256");
@@ -737,11 +742,13 @@ struct PairCfg {
     static constexpr int kOutBox = 32 * kBoxCols * 2;
     static constexpr int kOutBytes = kEpiWarps * kOutBox;
     static constexpr int kStages =
-        (220 * 1024 - kOutBytes) / kStageBytes < 8 ? (220 * 1024 - kOutBytes) / kStageBytes : 8;
+        (CC_TP_PAIR_SMEM - kOutBytes) / kStageBytes < 8 ? (CC_TP_PAIR_SMEM - kOutBytes) / kStageBytes
+                                                        : 8;
     static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;
     static constexpr int kChunks = kEpiCols / kChunk;
     static_assert(kTileB % 1024 == 0, "swizzle atoms");
     static_assert(kBoxCols == 32 || kBoxCols == 64, "output boxes of 32 or 64 columns");
+    static_assert(kSmemBytes <= 227 * 1024 - 1024, "dynamic shared memory beside the barriers");
     // tcgen05.mma kind::f16, bf16 A and B (K-major), fp32 accumulator,
     // M = 256 (the pair), N = BN.
     static constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10)
