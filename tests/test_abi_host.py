@@ -453,3 +453,56 @@ def test_tune_bucket_bytes_refuses_before_measuring():
     assert status() in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID, capi.CC_ERR_CUDA)
     assert status(candidates=None, rank=1) in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID,
                                                capi.CC_ERR_CUDA)
+
+
+def test_tp_matmul_allreduce_refuses_before_any_launch():
+    """The fused tensor-parallel entry points check shapes, budgets, NULLs,
+    alignment and aliasing (the workspace included) on the host before any
+    device call."""
+    R, m, n, k = 2, 256, 256, 256
+    kr = k // R
+    base = 1 << 40
+    stride = 1 << 22                       # fake, aligned, disjoint device addresses
+    addrs = iter(range(base, base + 64 * stride, stride))
+    x = [next(addrs) for _ in range(R)]
+    w = [next(addrs) for _ in range(R)]
+    outs = [next(addrs) for _ in range(R)]
+    ws = next(addrs)
+
+    def ex(**over):
+        args = dict(x=x, w=w, out=outs, partials=None, m=m, n=n, k=k, R=R, workspace=ws,
+                    workspace_bytes=1 << 20, max_ctas=0)
+        args.update(over)
+        try:
+            capi.cc_tp_matmul_allreduce_ex(args.pop("x"), args.pop("w"), args.pop("out"),
+                                           args.pop("partials"), args.pop("m"), args.pop("n"),
+                                           args.pop("k"), args.pop("R"), stream=0, **args)
+            return capi.CC_OK
+        except capi.CCError as err:
+            return err.status
+
+    def query(**over):
+        args = dict(m=m, n=n, k=k, R=R, max_ctas=0)
+        args.update(over)
+        try:
+            capi.cc_tp_matmul_allreduce_workspace(**args)
+            return capi.CC_OK
+        except capi.CCError as err:
+            return err.status
+
+    for bad in (dict(m=m + 8), dict(n=n + 16), dict(k=k + 1), dict(k=96), dict(R=0),
+                dict(R=17), dict(max_ctas=-1)):
+        assert query(**bad) == capi.CC_ERR_INVALID, bad
+        assert ex(**bad) == capi.CC_ERR_INVALID, bad
+    assert ex(max_ctas=1) == capi.CC_ERR_INVALID                 # the kernel runs CTA pairs
+    assert ex(out=[outs[0], None]) == capi.CC_ERR_INVALID
+    assert ex(workspace=ws + 8) == capi.CC_ERR_MISALIGNED
+    assert ex(workspace=outs[1]) == capi.CC_ERR_ALIAS            # written twice
+    assert ex(workspace=x[0] + 16 * kr) == capi.CC_ERR_ALIAS     # inside an input
+    assert ex(out=[outs[0], x[1]]) == capi.CC_ERR_ALIAS
+    # well-formed: the host checks pass and the device range check refuses
+    # the fake addresses (no GPU here)
+    assert ex() in (capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_INVALID, capi.CC_ERR_CUDA)
+    assert ex(workspace=None, workspace_bytes=0) in (capi.CC_ERR_UNSUPPORTED,
+                                                     capi.CC_ERR_INVALID, capi.CC_ERR_CUDA)
+    assert query() in (capi.CC_OK, capi.CC_ERR_UNSUPPORTED, capi.CC_ERR_CUDA)
