@@ -428,8 +428,8 @@ extern "C" int cc_overlap_bench(const cc_overlap_cfg *cfg, cc_overlap_result *ou
 
 namespace {
 
-// Bucket caps tried when the caller gives none: the range the bucket-sizing
-// advice spans (25 MB to a few hundred), and two smaller caps.
+// Bucket caps tried when the caller gives none: the range that bucket-sizing
+// guidance for DDP spans (25 MB to a few hundred), and two smaller caps.
 constexpr size_t kDefaultCaps[] = {size_t(1) << 20, size_t(4) << 20, size_t(25) << 20,
                                    size_t(100) << 20, size_t(500) << 20};
 

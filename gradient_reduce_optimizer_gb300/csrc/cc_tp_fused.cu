@@ -741,9 +741,8 @@ struct PairCfg {
     static constexpr int kBoxCols = CC_TP_PAIR_BOX_COLS;
     static constexpr int kOutBox = 32 * kBoxCols * 2;
     static constexpr int kOutBytes = kEpiWarps * kOutBox;
-    static constexpr int kStages =
-        (CC_TP_PAIR_SMEM - kOutBytes) / kStageBytes < 8 ? (CC_TP_PAIR_SMEM - kOutBytes) / kStageBytes
-                                                        : 8;
+    static constexpr int kStagesFit = (CC_TP_PAIR_SMEM - kOutBytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit < 8 ? kStagesFit : 8;
     static constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024;
     static constexpr int kChunks = kEpiCols / kChunk;
     static_assert(kTileB % 1024 == 0, "swizzle atoms");
@@ -762,10 +761,10 @@ __device__ __forceinline__ float4 quad(const uint32_t (&y)[32], int q) {
                        __uint_as_float(y[4 * q + 2]), __uint_as_float(y[4 * q + 3]));
 }
 
-// Round 64 running sums of one row to bf16 into this warp's staging box and
-// TMA-store it to every rank's output, kBoxCols columns at a time.  Swizzle:
-// 16-byte chunk j of row i at chunk j ^ (i % 8) in 128-byte rows, j ^ ((i /
-// 2) % 4) in 64-byte rows.
+// Convert 64 running sums of one row to bf16 (nearest-even) into this warp's
+// staging box and TMA-store it to every rank's output, kBoxCols columns at a
+// time.  Swizzle: 16-byte chunk j of row i at chunk j ^ (i % 8) in 128-byte
+// rows, j ^ ((i / 2) % 4) in 64-byte rows.
 template <int kBoxCols>
 __device__ __forceinline__ void store_sums_bf16(const float (&sum)[kEpiCols], int lane,
                                                 uint32_t out_box, const CUtensorMap *tout,
