@@ -746,6 +746,8 @@ def run_ours(args):
         result["gpt2_slice_r4"] = run_gpt2_slice(args, dev)
     if not args.no_accum and not args.small:
         result["accumulation"] = run_accumulation(args, wk, stream)
+    if not args.no_unfused and not args.small:
+        result["rank_step"] = run_rank_step(args, wk, stream)
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, wk, stream, world, dev)
     if args.small and args.overlap_small:
@@ -1144,6 +1146,71 @@ def run_accumulation(args, wk, stream, k=4):
     del acc
     torch.cuda.empty_cache()
     return out
+
+
+def run_rank_step(args, wk, stream):
+    """One rank's compute in the real multi-GPU form, on this GPU: rank 0's
+    shard of every planned bucket of the headline slab (cc_shard_plan over
+    R ranks), its R gradient slices read straight from the replica slabs
+    (where the ReduceScatter would have put them), its state shard packed
+    in launch order, its bf16 parameters written once.  (2R + 24 + 2)
+    algorithmic bytes per shard element; the exchanges themselves need
+    several GPUs and are not in this figure."""
+    import torch
+    from gradient_reduce_optimizer_gb300 import capi
+
+    w, R = wk["w"], wk["w"].R
+    shards, state_off, elems = capi.cc_shard_plan(wk["buckets"], R)
+    n0 = elems[0]
+    dev = wk["master"].device
+    master = wk["master"][:n0].clone()
+    m = wk["m"][:n0].clone()
+    v = wk["v"][:n0].clone()
+    # the views each launch takes, built once
+    calls = [([g[lo:hi] for g in wk["grads"]], master[o:o + hi - lo], m[o:o + hi - lo],
+              v[o:o + hi - lo], wk["outs"][0][lo:hi], hi - lo)
+             for (lo, hi), o in ((row[0], off[0]) for row, off in zip(shards, state_off))
+             if hi > lo]
+
+    def one(step, strm):
+        hp = step_args(wk, step)
+        for sl, ms_, mm_, vv_, out, length in calls:
+            capi.cc_fused_dp_rank_step(sl, ms_, mm_, vv_, out, length, R, stream=strm, **hp)
+
+    def timed(fn, reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for i in range(3):
+        one(w.step + i, stream)
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 20))
+    # issued from Python, one call per bucket (host-bound at these sizes)
+    host_ms = timed(lambda i: one(w.step + 3 + i, stream), reps)
+    # the same launches captured once in a CUDA graph and replayed: the
+    # device's own time for the step
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        one(w.step, torch.cuda.current_stream())
+    graph.replay()
+    torch.cuda.synchronize()
+    ms = timed(lambda i: graph.replay(), reps)
+    del graph
+    bpp = 2 * R + 26
+    gbs = bpp * n0 / (ms * 1e-3) / 1e9
+    peak, _ = measured_hbm_peak()
+    del master, m, v, calls
+    return {"workload": f"rank 0 of {R}: its shard of each of the {len(shards)} planned buckets",
+            "shard_elements": n0, "ms": round(ms, 4), "timing": "CUDA graph of one step",
+            "bytes_per_element": bpp, "hbm_gbs": round(gbs, 1),
+            "frac_of_measured_copy": round(gbs / peak, 3),
+            "launches_per_step": len(shards), "ms_issued_from_python": round(host_ms, 4)}
 
 
 def run_unfused(args, wk, stream, fused_ms):

@@ -508,7 +508,11 @@ int cc_fused_dp_rank_step(const void *const *grad_slices, float *master, float *
     s.m = m;
     s.v = v;
     s.one_out = true;
-    const cudaError_t e = launch_fused(s, c, 0, len, 0, false, static_cast<cudaStream_t>(stream));
+    // A programmatic dependent of whatever precedes it (a previous rank step,
+    // the exchange that filled the slices): resident early, reading nothing
+    // before that grid has completed.
+    const cudaError_t e = launch_fused(s, c, 0, len, 0, false, static_cast<cudaStream_t>(stream),
+                                       /*wait_first=*/true);
     return e == cudaSuccess ? CC_OK : fail_cuda(e, "rank step launch");
 }
 

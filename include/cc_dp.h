@@ -304,6 +304,10 @@ CC_API int cc_shard_plan(const size_t *bucket_begin, const size_t *bucket_end,
  *   the rest        as cc_fused_dp_step.  One kernel launch; allocates nothing.
  *   Gradient slices and param_out may be page-locked host memory, as replica
  *   slabs may elsewhere; the state must be device memory.
+ * The launch is a programmatic dependent of the work before it on the
+ * stream: its blocks may become resident while that kernel finishes, but
+ * read and write nothing before it has completed, so back-to-back rank
+ * steps (one per bucket) overlap their launch gaps.
  */
 CC_API int cc_fused_dp_rank_step(const void *const *grad_slices, float *master, float *m,
                                  float *v, void *param_out, size_t len, int R, float lr,
