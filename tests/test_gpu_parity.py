@@ -689,17 +689,18 @@ def test_fp32_slabs_aligned_to_16_but_not_32_bytes(use_acc):
 # per arm
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("max_ctas,prio,comm_sms,budget,algo", [(0, 0, 0, 0, 0),
-                                                               (0, 2, 0, 0, 0),
-                                                               (24, 1, 0, 0, 0),
-                                                               (0, 2, 48, 0, 0),
-                                                               (8, 2, 0, 3, 0),
-                                                               (0, 2, 0, 0, 1)])
+@pytest.mark.parametrize("max_ctas,prio,comm_sms,budget,algo,use_acc,flags", [
+    (0, 0, 0, 0, 0, False, 0), (0, 2, 0, 0, 0, False, 0), (24, 1, 0, 0, 0, False, 0),
+    (0, 2, 48, 0, 0, False, 0), (8, 2, 0, 3, 0, False, 0), (0, 2, 0, 0, 1, False, 0),
+    (24, 2, 0, 0, 0, False, 2), (0, 2, 0, 0, 0, True, 0), (16, 2, 0, 0, 0, True, 0),
+    (16, 2, 0, 0, 0, True, 2)])
 def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sms, budget,
-                                                         algo):
+                                                         algo, use_acc, flags):
     """With warmup 0 and one iteration the four arms step the slabs three
     times (buckets alone, overlapped, sequential; the backward-only arm does
-    not step): the result must be three oracle steps, bit for bit."""
+    not step): the result must be three oracle steps, bit for bit.  Also the
+    reducing step with accumulators (read, not written, by each arm), and
+    budgets on the bulk-copy engine (flags 2)."""
     t = wl.bert_large_tensors(layers=4, hidden=256, ffn=1024, vocab=997, positions=64)
     numel = [x[1] for x in t]
     layer_of = [x[2] for x in t]
@@ -707,8 +708,13 @@ def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sm
     ready = oracle.bucket_ready_layers(numel, layer_of, offsets, buckets)
     assert len(buckets) >= 8 and len(set(ready)) == 4
     R = 4
-    s = new_slabs(*random_inputs(R, n_slab, seed=71, step=5))
-    grads, state, _ = host_copy(s)
+    s = new_slabs(*random_inputs(R, n_slab, seed=71, step=5), with_acc=use_acc)
+    if use_acc:
+        gen = torch.Generator(device=DEV)
+        gen.manual_seed(72)
+        for a in s.acc:
+            a.copy_(torch.randn(n_slab, generator=gen, device=DEV) * 1e-3)
+    grads, state, acc = host_copy(s)
     hp = dict(HP10, step=5)
     M = N = K = 256
     A = torch.randn(M * K, device=DEV).to(torch.bfloat16)
@@ -720,14 +726,15 @@ def test_overlap_bench_applies_every_bucket_once_per_arm(max_ctas, prio, comm_sm
                               gemm_m=M, gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B,
                               gemm_c=C, warmup=0, iters=1, max_ctas=max_ctas,
                               stream_priority=prio, comm_sms=comm_sms,
-                              budget_buckets=budget, gemm_algo=algo, **hp)
+                              budget_buckets=budget, gemm_algo=algo,
+                              acc=s.acc if use_acc else None, arith_flags=flags, **hp)
     assert r["num_buckets"] == len(buckets) and r["t_bwd_ms"] > 0
     assert (r["gemm_algos"] >= 1) == (algo > 0)
     if comm_sms:   # a spatial partition: green contexts on disjoint SM sets
         assert r["comm_sms"] >= comm_sms and r["compute_sms"] > 0
     torch.cuda.synchronize()
     for _ in range(3):
-        outs = oracle_step(grads, state, hp)
+        outs = oracle_step(grads, state, hp, acc=acc if use_acc else None)
     compare_all(s, state, outs)
     assert capi.cc_device_status() == 0
 
