@@ -964,7 +964,8 @@ def run_tp(args, dev, R=8, m=8192, n=3072, k=12288, chunk_list=(1, 2, 4, 8, 16))
     """The tensor-parallel MatMul-then-AllReduce of a GPT-2 8.3B MLP output
     projection (row-parallel: k = 12288 -> n = 3072 over m = 8192 tokens) at
     tensor-parallel degree R = 8, sequential and overlapped in chunks of rows
-    ("LIT-735", Key takeaways: hides most of the MatMul, up to 1.36x)."""
+    ("LIT-735", Key takeaways: chunked overlap of the two, reported to hide
+    most of the MatMul's time)."""
     import torch
     from gradient_reduce_optimizer_gb300 import capi
 
@@ -1094,8 +1095,9 @@ def run_accumulation(args, wk, stream, k=4):
     """Gradient accumulation with k micro-steps on the same workload: k-1
     local micro-steps (first: acc = g, 6R bytes per parameter; later:
     acc += g, 10R) and the reducing step, the fused kernel with the
-    accumulators (8R + 24).  "The reducing step, not the average step, is
-    the one to profile" (Overlapping Communication and Computation)."""
+    accumulators (8R + 24).  The reducing step, not a typical micro-step,
+    is the one the accumulation paragraph of Overlapping Communication and
+    Computation says to profile."""
     import torch
     from gradient_reduce_optimizer_gb300 import capi
 
@@ -1346,9 +1348,10 @@ def run_overlap(args, wk, dev, mibs, rank_share=False, comm_sms=0, acc=None,
     parameters to all R replica slabs, (4 + 24/R) bytes per parameter.
     acc: the R fp32 accumulators of gradient accumulation, which makes every
     bucket the reducing k-th step ((8R + 24) bytes per parameter; a rank's
-    share (8 + 24/R)): "That reducing step has only its own backward compute
-    to hide a full model's worth of gradient traffic" (Overlapping
-    Communication and Computation)."""
+    share (8 + 24/R)): with accumulation, the reducing step must hide the
+    whole model's gradient traffic behind only its own backward
+    (Overlapping Communication and Computation, the accumulation
+    paragraph)."""
     import torch
     from gradient_reduce_optimizer_gb300 import capi
 

@@ -12,7 +12,7 @@
  * Sources.  "LIT-735: Breaking the Computation and Communication Abstraction
  * Barrier in Distributed Machine Learning Workloads" (CoCoNet), Key
  * takeaways: the data-parallel result is a fused ReduceScatter-optimizer-
- * AllGather for BERT training with Adam.  "Communication Optimization ›
+ * AllGather, measured on BERT with the Adam optimizer.  "Communication Optimization ›
  * Communication Overlap": DDP groups parameters into fixed-size buckets
  * (default 25 MB), launches each bucket as soon as its gradients are ready on
  * a separate stream, last layer first; the step-time equation T_step ~
