@@ -142,14 +142,17 @@ def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k, schedu
 
 
 @pytest.mark.parametrize("schedule", ["whole", "split"])
-def test_gpt2_mlp_shape_sampled(schedule):
-    """The measured shape (R=8, m=8192, n=3072, k=12288): integer operands,
-    so every output is exact; checked on sampled rows against float64 (the
-    last row tiles are the split wave's)."""
-    R, m, n, k = 8, 8192, 3072, 12288
+@pytest.mark.parametrize("m", [2048, 8192])
+def test_gpt2_mlp_shape_sampled(m, schedule):
+    """The measured shape (R=8, n=3072, k=12288; m=8192 runs 256-column tiles
+    with a split last wave, m=2048 192-column tiles): integer operands, so
+    every output is exact; checked on sampled rows against float64 (the last
+    row tiles are the split wave's)."""
+    R, n, k = 8, 3072, 12288
     x, w = operands(R, m, n, k, seed=5, integer=True)
     outs, _ = run(x, w, m, n, k, R, with_partials=False, schedule=schedule)
-    rows = torch.tensor([0, 1, 127, 128, 4095, 4096, 7936, 8000, 8191], device=DEV)
+    rows = torch.tensor([0, 1, 127, 128, m // 2 - 1, m // 2, m - 256, m - 192, m - 1],
+                        device=DEV)
     total = sum(x_[rows].double() @ w_.double().T for x_, w_ in zip(x, w))
     want = total.float().to(torch.bfloat16).view(torch.int16)
     for r in range(R):
