@@ -195,3 +195,38 @@ def test_rejects_small_workspace_and_one_cta():
     # one split-free launch later nothing is left armed
     torch.cuda.synchronize()
     assert capi.cc_device_status() == 0
+
+
+def _random_cases(count=28, seed=2024):
+    import random
+    rnd = random.Random(seed)
+    cases = []
+    while len(cases) < count:
+        R = rnd.choice([1, 2, 3, 4, 5, 8, 12, 16])
+        m = 128 * rnd.randint(1, 24)
+        n = rnd.choice([128, 192, 256, 384, 512, 576, 640, 768, 1024])
+        kr = 64 * rnd.randint(1, 4)
+        max_ctas = rnd.choice([0, 0, 4, 6, 10, 32])
+        use_ws = rnd.random() < 0.7
+        cases.append((R, m, n, kr * R, max_ctas, use_ws))
+    return cases
+
+
+@pytest.mark.parametrize("R,m,n,k,max_ctas,use_ws", _random_cases())
+def test_random_shapes_and_schedules_are_exact(R, m, n, k, max_ctas, use_ws):
+    """Seeded random shapes, CTA budgets and workspaces: whichever kernel,
+    tile width and schedule (whole or split last wave) the library picks,
+    integer operands give outputs equal to the bf16 rounding of the exact
+    sum (|x|, |w| <= 3, so every partial and sum is exact in fp32)."""
+    x, w = operands(R, m, n, k, seed=m + n + k + R, integer=True)
+    outs = [torch.full((m, n), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+            for _ in range(R)]
+    ws_bytes = capi.cc_tp_matmul_allreduce_workspace(m, n, k, R, max_ctas) if use_ws else 0
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV) if use_ws else None
+    capi.cc_tp_matmul_allreduce_ex(x, w, outs, None, m, n, k, R, ws, ws_bytes, max_ctas)
+    torch.cuda.synchronize()
+    assert capi.cc_device_status() == 0
+    total = sum(x_.double() @ w_.double().T for x_, w_ in zip(x, w))
+    want = total.float().to(torch.bfloat16).view(torch.int16)
+    for r in range(R):
+        assert torch.equal(outs[r].view(torch.int16), want), f"out[{r}]"
