@@ -757,8 +757,8 @@ def test_overlap_bench_rejects_bad_schedules():
         assert ei.value.status == capi.CC_ERR_INVALID
 
 
-@pytest.mark.parametrize("rank", [-1, 1])
-def test_tune_bucket_bytes_measures_every_candidate(rank):
+@pytest.mark.parametrize("rank,use_acc", [(-1, False), (1, False), (-1, True)])
+def test_tune_bucket_bytes_measures_every_candidate(rank, use_acc):
     """The bucket-size tuner times each candidate cap's launch list with the
     overlap bench and returns the cap whose overlapped step is shortest.
     With warmup 0 and one iteration every candidate steps its buckets (or
@@ -771,8 +771,13 @@ def test_tune_bucket_bytes_measures_every_candidate(rank):
     caps = [64 * 1024, 256 * 1024, 0]
     R = 3
     _, _, n_slab = oracle.plan_buckets(numel, 0)
-    s = new_slabs(*random_inputs(R, n_slab, seed=73, step=5))
-    grads, state, _ = host_copy(s)
+    s = new_slabs(*random_inputs(R, n_slab, seed=73, step=5), with_acc=use_acc)
+    if use_acc:                     # the reducing step: accumulators read by every arm
+        gen = torch.Generator(device=DEV)
+        gen.manual_seed(74)
+        for a in s.acc:
+            a.copy_(torch.randn(n_slab, generator=gen, device=DEV) * 1e-3)
+    grads, state, acc = host_copy(s)
     hp = dict(HP10, step=5)
     M = N = K = 256
     A = torch.randn(M * K, device=DEV).to(torch.bfloat16)
@@ -782,7 +787,7 @@ def test_tune_bucket_bytes_measures_every_candidate(rank):
         numel=numel, layer_of=layer_of, candidates=caps, rank=rank, grads=s.grads,
         master=s.master, m=s.m, v=s.v, params_out=s.outs, n=n_slab, R=R, num_layers=4,
         gemms_per_layer=2, gemm_m=M, gemm_n=N, gemm_k=K, gemm_a=A, gemm_b=B, gemm_c=C,
-        warmup=0, iters=1, **hp)
+        warmup=0, iters=1, acc=s.acc if use_acc else None, **hp)
     assert len(results) == len(caps)
     step_ms = [r["t_step_overlap_ms"] for r in results]
     assert best == caps[min(range(len(caps)), key=lambda i: (step_ms[i], i))]
@@ -796,8 +801,9 @@ def test_tune_bucket_bytes_measures_every_candidate(rank):
         idx = np.concatenate([np.arange(lo, hi) for lo, hi in buckets])
         sub = [a[idx].copy() for a in state]
         sub_grads = [g[idx] for g in grads]
+        sub_acc = [a[idx].copy() for a in acc] if use_acc else None
         for _ in range(3):
-            sub_outs = oracle.fused_dp_step(sub_grads, *sub, **hp)
+            sub_outs = oracle.fused_dp_step(sub_grads, *sub, acc=sub_acc, **hp)
         for a, b in zip(state, sub):
             a[idx] = b
         for o, b in zip(outs, sub_outs):
