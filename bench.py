@@ -641,7 +641,13 @@ def run_ours(args):
         ws = torch.empty(n_slab, dtype=torch.float32, device=dev)
 
     def one_step(step):
-        if ws is not None:
+        if args.small and args.rank_step:
+            # profile case: one rank's compute of the multi-GPU form over the
+            # whole flat slab (R gradient slices in, the parameters out once)
+            capi.cc_fused_dp_rank_step(wk["grads"], wk["master"], wk["m"], wk["v"],
+                                       wk["outs"][0], n_slab, R, stream=stream,
+                                       **step_args(wk, step))
+        elif ws is not None:
             # profile case: the unfused schedule (reduce, AdamW, R-1 copies)
             capi.cc_unfused_dp_step(wk["grads"], wk["master"], wk["m"], wk["v"], wk["outs"],
                                     ws, ws.numel() * 4, n_slab, R, bb, stream=stream,
@@ -689,7 +695,8 @@ def run_ours(args):
     ms_local = ev0.elapsed_time(ev1) / args.steps
     ms, value = aggregate(ms_local, float(n_params), world, device=dev)
 
-    bytes_per_param = (6 * R + 30 if ws is not None else
+    bytes_per_param = (2 * R + 26 if args.small and args.rank_step else
+                       6 * R + 30 if ws is not None else
                        4 * R + 24 if acc is None else
                        (6 * R if args.micro == "first" else 10 * R) if args.micro else
                        8 * R + 24)
@@ -699,13 +706,16 @@ def run_ours(args):
     achieved = bytes_per_param * per_launch_elems / (launch_ms * 1e-3) / 1e9
     peak, peak_src = measured_hbm_peak()
     tpp = (profiled_traffic_per_param(R)
-           if args.engine_ctas == 0 and acc is None and ws is None else None)
+           if args.engine_ctas == 0 and acc is None and ws is None and not args.rank_step
+           else None)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": (round(tpp * per_launch_elems) if tpp else None),
                 "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": round(bytes_per_param * per_launch_elems),
-                "kernel": ("reduce_kernel + adamw_kernel + copies" if ws is not None else
+                "kernel": (f"fused_step_kernel<R={R}, one output> (rank step)"
+                           if args.small and args.rank_step else
+                           "reduce_kernel + adamw_kernel + copies" if ws is not None else
                            f"accumulate_kernel<R={R}, first={args.micro == 'first'}>"
                            if args.micro else
                            f"fused_step_kernel<R={R}, accumulators>" if acc is not None else
@@ -1478,6 +1488,9 @@ def parse_args(argv=None):
                    help="run each bucket on a budget of this many SMs "
                         "(cc_fused_dp_bucket max_ctas: the wide-CTA kernel); 0 = the "
                         "plain kernel over the whole GPU")
+    p.add_argument("--rank-step", action="store_true",
+                   help="with --small: one rank's compute of the multi-GPU form "
+                        "(cc_fused_dp_rank_step over the flat slab)")
     p.add_argument("--bulk-copy", action="store_true",
                    help="with --engine-ctas: the TMA bulk-copy engine (CC_ENGINE_BULK_COPY)")
     p.add_argument("--small", type=int, default=0,
