@@ -14,26 +14,35 @@
 //
 // Unfused, the R partial products go to HBM in fp32 and an AllReduce pass
 // reads them back (4R bytes written + 4R read + 2R written per output
-// element).  Here no partial product leaves the SM: one persistent CTA per
-// SM walks output tiles of 128 x BN, and for each tile
-//   * a producer warp streams 128 x 64 tiles of X_r and BN x 64 tiles of W_r
-//     for r = 0..R-1 with TMA (cp.async.bulk.tensor, 128-byte swizzle) into a
+// element).  Here no partial product leaves the SM.  Persistent CTAs walk
+// output tiles, and for each tile
+//   * a producer warp streams 64-wide k-blocks of X_r and W_r for
+//     r = 0..R-1 with TMA (cp.async.bulk.tensor, 128-byte swizzle) into a
 //     ring of shared-memory stages;
-//   * an MMA warp issues tcgen05.mma (M = 128, N = BN, K = 16, bf16 in, fp32
-//     accumulate) from those stages into one of two TMEM accumulators: rank
-//     r of the CTA's j-th job goes to accumulator (j*R + r) % 2, so the next
-//     rank's MMAs run while the epilogue drains the previous one;
+//   * an MMA warp issues tcgen05.mma (bf16 in, fp32 accumulate) from those
+//     stages into one of two TMEM accumulators, alternating per rank, so the
+//     next rank's MMAs run while the epilogue drains the previous one;
 //   * 4 * BN / 64 epilogue warps (each thread one row and 64 columns) read
 //     each finished accumulator from TMEM (tcgen05.ld), add it to a running
 //     fp32 sum in registers in rank order, and hand the accumulator back at
-//     once, so the MMAs of rank r+2 never wait for more than that read.
-//     After the last rank they round the sum to bf16 once and store it to
-//     all R outputs -- the AllReduce's broadcast -- while the MMA warp
-//     already works on the next tile.
-// Only the operands are read and only the R bf16 outputs are written.  The
-// producer also prefetches the operands into L2 several k-blocks ahead: all
-// CTAs work on the same k-block at about the same time, so without it every
-// stage would wait for DRAM.
+//     once.  After the last rank they round the sum to bf16 once and store
+//     it to all R outputs through swizzled shared-memory boxes and TMA
+//     stores -- the AllReduce's broadcast -- while the MMA warp already
+//     works on the next tile.
+// Only the operands are read and only the R bf16 outputs are written.
+//
+// Two kernels share this design.  The pair kernel (tp_fused_pair_kernel,
+// used wherever the 128-row tiles pair up) runs one MMA over two SMs
+// (tcgen05.mma.cta_group::2, M = 256): each CTA of a cluster of two loads
+// its own 128 rows of X and half of the W tile, and the leader issues the
+// MMAs for both.  Its tile width BN (256, 192 or 128) is chosen per shape
+// by a model of its waves times its operand intake.  When a few groups of
+// tiles are left for a last wave, a caller workspace lets it split them
+// into their R rank products spread over the pairs: each product goes to
+// the workspace in fp32 and the last of a group's R to finish, counted
+// with an atomic ticket, sums them in rank order and stores the outputs.
+// The single-CTA kernel (tp_fused_kernel, M = 128, optionally in clusters
+// that share operand tiles by TMA multicast) takes odd row-tile counts.
 //
 // Every wait on an mbarrier is bounded by the global timer.  A wait that
 // runs out records a code in this file's status word (read through
