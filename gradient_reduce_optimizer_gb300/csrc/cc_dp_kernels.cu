@@ -27,7 +27,14 @@
 //     only when its own work is done.  Buckets touch disjoint elements, so
 //     the next bucket's blocks fill SMs as this bucket's tail drains, and
 //     the final wait keeps completion transitive (the last bucket of a call
-//     completes only after every earlier one).
+//     completes only after every earlier one).  A step's first bucket (and
+//     a rank step) is a programmatic dependent too, but waits before it
+//     touches memory, since it may read what the previous kernel wrote;
+//   * under a CTA budget the same per-vector code runs in wide CTAs (768
+//     threads, one per SM, grid = the budget, each thread striding over the
+//     range), with the fp32 state in 32-byte accesses where it is 32-byte
+//     aligned: one SM then streams about 98 GB/s, so a budget of about 70
+//     SMs reaches HBM bandwidth.
 //
 // Arithmetic is IEEE binary32 with each operation rounded on its own
 // (__fadd_rn/__fmul_rn/__fdiv_rn/__fsqrt_rn never contract to FMA), in the
