@@ -73,6 +73,21 @@ constexpr int kSmemBudget = 200 * 1024;        // dynamic shared memory per CTA
 constexpr unsigned kStatusConsumerTimeout = 1u;
 constexpr unsigned kStatusProducerTimeout = 2u;
 constexpr unsigned kStatusDrainTimeout = 4u;
+constexpr unsigned kStatusBounds = 128u;        // debug builds: an access outside its range
+
+#ifndef CC_DEBUG_BOUNDS
+#define CC_DEBUG_BOUNDS 0   // 1: check the computed element ranges; skip and report
+#endif
+constexpr bool kDebugBounds = CC_DEBUG_BOUNDS != 0;
+
+// Debug builds: whether [off, off + len) lies inside [0, limit); if not, the
+// status word says so and the access is skipped.
+__device__ __forceinline__ bool debug_in_bounds(size_t off, size_t len, size_t limit) {
+    if constexpr (!kDebugBounds) return true;
+    if (off + len <= limit) return true;
+    atomicOr(&g_bulk_status, kStatusBounds);
+    return false;
+}
 
 struct BulkParams {
     const uint16_t *g[CC_MAX_R];   // bf16 slabs
@@ -293,6 +308,10 @@ fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
                 const uint32_t len = static_cast<uint32_t>(left < static_cast<size_t>(T) ? left : T);
                 unsigned char *st = smem + static_cast<size_t>(s) * L.bytes;
                 const uint32_t bar = smem_addr(&full_bar[s]);
+                // (debug builds) the copies stay inside the range and the stage
+                debug_in_bounds(e0 - p.begin, len, p.tiled);
+                debug_in_bounds(static_cast<size_t>(s) * L.bytes + L.v + 4u * T, 0,
+                                static_cast<size_t>(S) * L.bytes);
                 const uint32_t bytes = len * (2u * R + 12u + (ACC ? 4u * R : 0u));
                 mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
@@ -350,7 +369,8 @@ fused_step_bulk_kernel(const __grid_constant__ BulkParams p) {
         const size_t e0 = p.begin + t * static_cast<size_t>(T);
         // Read and reduce, hand the stage back, then update and store: the
         // producer refills the stage while this warp does the arithmetic.
-        const bool mine = j < len;
+        const bool mine = j < len && debug_in_bounds(e0 + j - p.begin, 4, p.tiled) &&
+                          debug_in_bounds(j, 4, len);
         Operands4 x;
         if (mine) x = read_reduce4<R, ACC>(st, L, T, j);
         __syncwarp();

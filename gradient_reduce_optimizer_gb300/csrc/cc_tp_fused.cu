@@ -124,6 +124,12 @@ constexpr unsigned kStatusProducer = 8u;
 constexpr unsigned kStatusMma = 16u;
 constexpr unsigned kStatusEpilogue = 32u;
 constexpr unsigned kStatusDrain = 64u;
+constexpr unsigned kStatusBounds = 128u;   // debug builds: an access outside its buffer
+
+#ifndef CC_DEBUG_BOUNDS
+#define CC_DEBUG_BOUNDS 0   // 1: check the epilogue's computed offsets; skip and report
+#endif
+constexpr bool kDebugBounds = CC_DEBUG_BOUNDS != 0;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // two seconds per wait
 
 struct TpFusedParams {
@@ -141,7 +147,17 @@ struct TpFusedParams {
     float *tail_ws;
     unsigned *tail_count;
     int full_groups, tail_phases;
+    size_t tail_ws_floats;        // the slots' extent, for the debug bounds checks
 };
+
+// Debug builds: whether [off, off + len) lies inside a buffer of `limit`
+// elements; if not, the status word says so and the access is skipped.
+__device__ __forceinline__ bool debug_in_bounds(size_t off, size_t len, size_t limit) {
+    if constexpr (!kDebugBounds) return true;
+    if (off + len <= limit) return true;
+    atomicOr(&g_tp_status, kStatusBounds);
+    return false;
+}
 
 // The (group, rank) phases one cluster works through, numbered 0, 1, ...:
 // first its whole groups (every rank of group first, then first + stride,
@@ -1076,7 +1092,8 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
                     uint32_t y[32];
                     tmem_ld32(y_addr + kChunk * c, y);
                     tmem_wait_ld();
-                    if (keep_partials) {
+                    if (keep_partials &&
+                        debug_in_bounds(off + kChunk * c, kChunk, static_cast<size_t>(p.m) * n)) {
                         float4 *dst = reinterpret_cast<float4 *>(partials[r] + off + kChunk * c);
 #pragma unroll
                         for (int q = 0; q < 8; ++q) dst[q] = quad(y, q);
@@ -1115,14 +1132,19 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
                 uint32_t y[32];
                 tmem_ld32(y_addr + kChunk * c, y);
                 tmem_wait_ld();
-                if (keep_partials) {
+                if (keep_partials &&
+                    debug_in_bounds(off + kChunk * c, kChunk, static_cast<size_t>(p.m) * n)) {
                     float4 *dst = reinterpret_cast<float4 *>(partials[r] + off + kChunk * c);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) dst[q] = quad(y, q);
                 }
                 float4 *dst = reinterpret_cast<float4 *>(slot) + (kChunk / 4) * c * kBM;
+                // the chunk's last float4 lies 7 * kBM float4s past its first
+                if (debug_in_bounds(static_cast<size_t>(reinterpret_cast<float *>(dst) - p.tail_ws),
+                                    4 * (7 * kBM + 1), p.tail_ws_floats)) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) dst[q * kBM] = quad(y, q);
+                    for (int q = 0; q < 8; ++q) dst[q * kBM] = quad(y, q);
+                }
             }
             release_acc(job);
             __threadfence();
@@ -1147,7 +1169,12 @@ tp_fused_pair_kernel(const __grid_constant__ TpFusedParams p) {
                 ok = false;
                 break;
             }
-            if (tail_last)
+            // the fixup reads R slots, each 16 column quads of 128 rows deep
+            if (tail_last &&
+                debug_in_bounds(static_cast<size_t>(slots - p.tail_ws),
+                                static_cast<size_t>(R - 1) * 2 * kSlotFloats +
+                                    4 * (15 * kBM + 1),
+                                p.tail_ws_floats))
                 fixup_store_bf16<C::kBoxCols>(reinterpret_cast<const float4 *>(slots),
                                               2 * kSlotFloats / 4, lane, out_box, p.tout, R,
                                               n0 + static_cast<int>(col_off), m0 + 32 * quarter);
@@ -1378,6 +1405,7 @@ int launch_pair(TpFusedParams &p, const void *const *x, const void *const *w, in
         p.tail_count = static_cast<unsigned *>(ws);
         p.tail_ws = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) +
                                               tail_counter_bytes(tail_groups));
+        p.tail_ws_floats = (plan.ws_bytes - tail_counter_bytes(tail_groups)) / sizeof(float);
         e = cudaMemsetAsync(ws, 0, static_cast<size_t>(tail_groups) * 2 * sizeof(unsigned),
                             stream);
         if (e != cudaSuccess) return fail_cuda(e, "tail counters");

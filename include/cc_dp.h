@@ -676,9 +676,11 @@ CC_API int cc_tp_matmul_allreduce_workspace(int m, int n, int k, int R, int max_
  * (every such wait is bounded, after which the kernel abandons its pipeline
  * and returns instead of hanging).  Bulk-copy engine (one second per wait):
  * 1 consumer, 2 producer, 4 drain of copies in flight.  Fused tensor-parallel
- * kernel (two seconds): 8 producer, 16 MMA, 32 epilogue, 64 drain.  A
- * non-zero word means some launch did not finish its range.  Synchronises
- * with the device; clear != 0 resets the word.
+ * kernel (two seconds): 8 producer, 16 MMA, 32 epilogue, 64 drain.  Builds
+ * with CC_DEBUG_BOUNDS=1 only: 128, an access of either kernel fell outside
+ * the buffer or range its arguments describe and was skipped.  A non-zero
+ * word means some launch did not finish its range.  Synchronises with the
+ * device; clear != 0 resets the word.
  */
 CC_API int cc_device_status(unsigned *status, int clear);
 
