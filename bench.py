@@ -64,10 +64,15 @@ def dist_env():
     return rank, world, local
 
 
-def dist_init(world: int, backend: str):
+def dist_init(world: int, backend: str, timeout_s: float = 300.0):
+    """The process group, with a limit on every collective: an exchange that
+    stalls (a rank that died or never joined) ends with an error on the
+    others instead of holding their GPUs."""
+    import datetime
     import torch.distributed as dist
     if world > 1 and not dist.is_initialized():
-        dist.init_process_group(backend=backend)
+        dist.init_process_group(backend=backend,
+                                timeout=datetime.timedelta(seconds=timeout_s))
     return dist
 
 
@@ -1433,7 +1438,8 @@ def small_overlap_workload(wk, num_layers):
 def run_reference(args):
     rank, world, _ = dist_env()
     if world > 1:
-        dist_init(world, "gloo")
+        # rank 0 runs the oracle for minutes before the closing barrier
+        dist_init(world, "gloo", timeout_s=1800.0)
     if rank != 0:
         barrier(world)
         return None
