@@ -116,9 +116,12 @@ def _run_pins_on(mutated_source: str) -> subprocess.CompletedProcess:
         for name in ("__init__.py", "capi.py", "workloads.py"):
             shutil.copy(os.path.join(ROOT, pkg, name), os.path.join(work, pkg))
         shutil.copy(os.path.join(ROOT, "pytest.ini"), work)
+        # the 2^32-pattern bf16 sweep is left out: the rounding-class pin
+        # before it already fails every planted bf16 slip, and the sweep would
+        # cost each Adam mutant half a minute before its failing pin
         return subprocess.run(
             [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:warnings",
-             "tests/test_oracle_pins.py"],
+             "-k", "not every_binary32_pattern", "tests/test_oracle_pins.py"],
             cwd=work, capture_output=True, text=True, timeout=300)
     finally:
         shutil.rmtree(work, ignore_errors=True)

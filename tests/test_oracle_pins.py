@@ -6,7 +6,8 @@ plausible slip (a dropped term, a wrong sign or index, a swapped operand, a
 missing replica) fails at least one of them:
 
 * bf16 cast: every bf16 rounding class for all 65,536 upper halves, against
-  a rounding computed in float64 from frexp/rint (no bit tricks).
+  a rounding computed in float64 from frexp/rint (no bit tricks); and every
+  one of the 2^32 binary32 patterns against torch's own conversion.
 * step 1 closed form: with m = v = 0 and no decay, Adam's first update is
   lr * g / (|g| + eps) (bias correction exactly cancels 1 - beta).
 * R = 1 against torch.optim.AdamW on CPU (fp32, foreach=False), over
@@ -114,6 +115,32 @@ def test_bf16_round_every_rounding_class():
     assert np.array_equal(gn >> 15, (nan.view(np.uint32) >> 31).astype(np.uint16))
     inf = np.array([np.inf, -np.inf], dtype=np.float32)
     assert list(oracle.bf16_round(inf)) == [0x7F80, 0xFF80]
+
+
+def test_bf16_round_every_binary32_pattern():
+    """All 2^32 binary32 bit patterns, in chunks.  Non-NaN inputs (finite
+    values and infinities) against torch's CPU float->bfloat16 conversion,
+    a separate implementation of round-to-nearest-even; NaN inputs stay NaN
+    with their sign (torch returns one canonical NaN, so only the class is
+    compared).  The float64 reference above pins every rounding class; this
+    sweep leaves no input pattern unchecked."""
+    chunk = 1 << 25
+    base = np.arange(chunk, dtype=np.uint32)
+    u = np.empty_like(base)
+    for start in range(0, 1 << 32, chunk):
+        np.add(base, np.uint32(start), out=u)
+        x = u.view(np.float32)
+        got = oracle.bf16_round(x)
+        ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        if ((start + chunk - 1) >> 23) & 0xFF != 0xFF:      # no NaN patterns here
+            assert np.array_equal(got, ref), hex(start)
+            continue
+        nan = (((u >> 23) & 0xFF) == 0xFF) & ((u & 0x7FFFFF) != 0)
+        keep = ~nan
+        assert np.array_equal(got[keep], ref[keep]), hex(start)
+        gn = got[nan]
+        assert np.all(((gn >> 7) & 0xFF) == 0xFF) and np.all((gn & 0x7F) != 0), hex(start)
+        assert np.array_equal(gn >> 15, (u[nan] >> 31).astype(np.uint16)), hex(start)
 
 
 def test_bf16_round_agrees_with_torch_on_finite_values():
