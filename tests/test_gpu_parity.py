@@ -83,7 +83,7 @@ def test_bucket_cut_does_not_change_values():
     n = 3 * 1024 * 1024 + 5
     base = random_inputs(4, n, seed=7, step=4)
     ref = None
-    for bb in (0, 16, 48, 4096, 1 << 20, 25 << 20):
+    for bb in (0, 16, 48, 4096, 1 << 20, 4 << 20, 25 << 20, 100 << 20, 500 << 20):
         s = new_slabs([g.clone() for g in base[0]], *[t.clone() for t in base[1:]])
         gpu_step(s, dict(HP10, step=4), bucket_bytes=bb)
         torch.cuda.synchronize()
