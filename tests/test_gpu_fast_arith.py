@@ -1,7 +1,7 @@
 """The opt-in fast arithmetic of the bucket kernels (CC_ARITH_FAST), through
 the C ABI, against the oracle's exact step.
 
-The benchmark spec's tolerance for floating point is a relative 1e-5 on the fp32
+The method's tolerance for floating point is a relative 1e-5 on the fp32
 master weights and moments and one bf16 ulp on the parameters.  The fast form
 keeps the replica sum, m and v exact (bit for bit), so only the parameter
 moves: by a few ulp of the update.  Worst case, in units of 2^-24 relative:
