@@ -1616,6 +1616,7 @@ extern "C" int cc_tp_matmul_allreduce_workspace(int m, int n, int k, int R, int 
     if (!bytes) return fail(CC_ERR_INVALID, "bytes is NULL");
     *bytes = 0;
     if (max_ctas < 0) return fail(CC_ERR_INVALID, "max_ctas=%d must be >= 0", max_ctas);
+    if (max_ctas == 1) return fail(CC_ERR_INVALID, "max_ctas=1: the kernel runs CTA pairs");
     int st;
     if ((st = tp_check_shape(m, n, k, R)) != CC_OK) return st;
     if ((st = ensure_device()) != CC_OK) return st;

@@ -665,7 +665,8 @@ CC_API int cc_tp_matmul_allreduce_ex(const void *const *x, const void *const *w,
  * row tiles).
  * Otherwise 256 bytes of counters per 32 split groups plus 2 x 128 x BN x R
  * fp32 products per split group (BN = 256, 192 or 128, the tile width the
- * kernel picks for n).  Shape errors as cc_tp_matmul_allreduce.
+ * kernel picks for n).  Shape errors as cc_tp_matmul_allreduce; max_ctas
+ * as cc_tp_matmul_allreduce_ex (0, or >= 2).
  */
 CC_API int cc_tp_matmul_allreduce_workspace(int m, int n, int k, int R, int max_ctas,
                                             size_t *bytes);

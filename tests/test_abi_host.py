@@ -495,6 +495,7 @@ def test_tp_matmul_allreduce_refuses_before_any_launch():
         assert query(**bad) == capi.CC_ERR_INVALID, bad
         assert ex(**bad) == capi.CC_ERR_INVALID, bad
     assert ex(max_ctas=1) == capi.CC_ERR_INVALID                 # the kernel runs CTA pairs
+    assert query(max_ctas=1) == capi.CC_ERR_INVALID
     assert ex(out=[outs[0], None]) == capi.CC_ERR_INVALID
     assert ex(workspace=ws + 8) == capi.CC_ERR_MISALIGNED
     assert ex(workspace=outs[1]) == capi.CC_ERR_ALIAS            # written twice
