@@ -28,12 +28,22 @@ Kernels only ever read local memory.  The exchanges are queued on the
 communication backend's own stream: bucket b+1's ReduceScatter is issued
 before bucket b's update, so it runs while the update computes.
 
+Two schedules.  step() runs every bucket once the whole backward is done.
+begin() / layer_ready() / end() is DDP's ready-driven schedule ("Communication
+Optimization > Communication Overlap": a bucket's collective starts as soon as
+the backward has produced its last gradient, the last layer's bucket first):
+the caller reports each finished layer, from the last down, and every bucket
+that is then complete goes out at once -- its exchange, update and AllGather
+on a side stream ordered after the caller's gradients -- while the backward
+computes the layers below.  Both give the same values.
+
 The exchange helpers take plain tensors and a process group, so the same
 code runs over NCCL on GPUs and over gloo on host tensors.
 """
 from __future__ import annotations
 
-from typing import List, Optional, Sequence, Tuple
+import contextlib
+from typing import Callable, List, Optional, Sequence, Tuple
 
 from . import capi
 
@@ -103,29 +113,45 @@ def finish(works) -> None:
         w.wait()
 
 
+def library_update(slices, master, m, v, out, length: int, R: int, *, stream=None, **hp):
+    """One rank's update of one bucket shard: the library's rank step."""
+    capi.cc_fused_dp_rank_step(slices, master, m, v, out, length, R, stream=stream, **hp)
+
+
 class ShardedStep:
     """The sharded fused step of one rank over a planned slab.
 
     numel: tensor sizes in forward (layer) order; bucket_bytes: the DDP
-    bucket cap.  The rank's gradient and parameter slabs are bf16 tensors of
+    bucket cap; layer_of: each tensor's layer, for the ready-driven
+    schedule.  The rank's gradient and parameter slabs are bf16 tensors of
     n_slab elements laid out by cc_plan_buckets; its master/m/v are fp32
     tensors of state_elems elements, its shards of every bucket in launch
-    order (state_offsets gives each one's place).
+    order (state_offsets gives each one's place).  update: the arithmetic of
+    one shard (library_update, the GPU kernel; host tests pass their own).
+    dtype: of the gradient slab and the staging buffers.
     """
 
     def __init__(self, numel: Sequence[int], bucket_bytes: int, rank: int, world: int,
-                 group=None, device=None):
+                 group=None, device=None, layer_of: Optional[Sequence[int]] = None,
+                 update: Callable = library_update, dtype=None):
         import torch
 
         self.rank, self.world, self.group = rank, world, group
+        self.update = update
         self.offsets, self.buckets, self.n_slab = capi.cc_plan_buckets(list(numel),
                                                                        bucket_bytes)
         self.shards, self.state_offsets, elems = capi.cc_shard_plan(self.buckets, world)
         self.state_elems = elems[rank]
+        # the layer after whose backward each bucket is complete (non-increasing)
+        self.ready = (capi.cc_bucket_ready_layers(list(numel), list(layer_of), self.offsets,
+                                                  self.buckets)
+                      if layer_of is not None else None)
         longest = max((hi - lo for b in self.shards for lo, hi in [b[rank]]), default=0)
         # two staging buffers: bucket b+1's slices arrive while b computes
-        self.staging = [torch.empty(world * staging_stride(longest), dtype=torch.bfloat16,
-                                    device=device) for _ in range(2)]
+        self.staging = [torch.empty(world * staging_stride(longest),
+                                    dtype=dtype or torch.bfloat16, device=device)
+                        for _ in range(2)]
+        self._run = None
 
     def shard_state_ranges(self) -> List[Tuple[Range, Range]]:
         """(slab range, state range) of each of this rank's shards."""
@@ -160,12 +186,96 @@ class ShardedStep:
                                                self.shards[b + 1], self.rank, self.world,
                                                self.group)
                 pending = start(rs[b + 1][1])
-            lo, hi = self.shards[b][self.rank]
-            o = self.state_offsets[b][self.rank]
-            capi.cc_fused_dp_rank_step(slices, master[o:o + hi - lo], m[o:o + hi - lo],
-                                       v[o:o + hi - lo], params[lo:hi], hi - lo, self.world,
-                                       stream=stream, **hp)
+            self._update(b, slices, master, m, v, params, stream, hp)
             gathers += start(all_gather_ops(params, self.shards[b], self.rank, self.world,
                                             self.group))
             rs[b] = None
         finish(gathers)
+
+    def _update(self, b, slices, master, m, v, params, stream, hp) -> None:
+        lo, hi = self.shards[b][self.rank]
+        if hi == lo:
+            return
+        o = self.state_offsets[b][self.rank]
+        self.update(slices, master[o:o + hi - lo], m[o:o + hi - lo], v[o:o + hi - lo],
+                    params[lo:hi], hi - lo, self.world, stream=stream, **hp)
+
+    # ---- the ready-driven schedule -------------------------------------
+
+    def begin(self, grads, master, m, v, params, *, lr: float, beta1: float, beta2: float,
+              eps: float, weight_decay: float, step: int, grad_scale: float,
+              stream=None, side_stream=None) -> None:
+        """Start a step whose buckets go out as the backward produces them.
+        stream: the caller's (the backward's) stream, default the current
+        one; side_stream: where the buckets' exchanges and updates are
+        ordered (CUDA tensors only; default a new stream)."""
+        import torch
+
+        if self.ready is None:
+            raise ValueError("the ready-driven schedule needs layer_of")
+        if self._run is not None:
+            raise RuntimeError("begin() while a step is open: end() it first")
+        cuda = grads.is_cuda
+        if cuda:
+            stream = stream or torch.cuda.current_stream(grads.device)
+            side_stream = side_stream or torch.cuda.Stream(device=grads.device)
+        self._run = dict(grads=grads, state=(master, m, v), params=params, next=0,
+                         gathers=[], stream=stream, side=side_stream, cuda=cuda,
+                         hp=dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps,
+                                 weight_decay=weight_decay, step=step,
+                                 grad_scale=grad_scale))
+
+    def _side(self):
+        import torch
+        run = self._run
+        return torch.cuda.stream(run["side"]) if run["cuda"] else contextlib.nullcontext()
+
+    def layer_ready(self, layer: int) -> int:
+        """The backward has written every gradient of `layer` (and, since it
+        runs from the last layer down, of every later one) on the caller's
+        stream.  Each bucket that is now complete goes out, in plan order:
+        its ReduceScatter, update and AllGather, ordered after those
+        gradients.  Returns how many buckets went out."""
+        import torch
+
+        run = self._run
+        if run is None:
+            raise RuntimeError("layer_ready() outside begin() / end()")
+        B = len(self.buckets)
+        if run["next"] >= B or self.ready[run["next"]] < layer:
+            return 0
+        if run["cuda"]:
+            done = torch.cuda.Event()
+            done.record(run["stream"])
+            run["side"].wait_event(done)
+        count = 0
+        with self._side():
+            while run["next"] < B and self.ready[run["next"]] >= layer:
+                b = run["next"]
+                slices, ops = reduce_scatter_ops(run["grads"], self.staging[b % 2],
+                                                 self.shards[b], self.rank, self.world,
+                                                 self.group)
+                finish(start(ops))               # the slices of bucket b are in place
+                self._update(b, slices, *run["state"], run["params"], run["side"], run["hp"])
+                run["gathers"] += start(all_gather_ops(run["params"], self.shards[b],
+                                                       self.rank, self.world, self.group))
+                run["next"] += 1
+                count += 1
+        return count
+
+    def end(self) -> None:
+        """Close the step: every bucket must have gone out (layer_ready(0)
+        was called).  The caller's stream waits for the last AllGather, so
+        the parameters are complete when it reaches this point."""
+        run = self._run
+        if run is None:
+            raise RuntimeError("end() without begin()")
+        left = len(self.buckets) - run["next"]
+        if left:
+            raise RuntimeError(f"{left} bucket(s) never became ready: report every layer "
+                               "down to layer 0 before end()")
+        with self._side():
+            finish(run["gathers"])
+        if run["cuda"]:
+            run["stream"].wait_stream(run["side"])
+        self._run = None

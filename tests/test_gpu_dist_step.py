@@ -126,3 +126,56 @@ def test_sharded_step_over_nccl_world_one():
                                           want.view(np.uint32))
     finally:
         dist.destroy_process_group()
+
+
+def test_ready_driven_schedule_over_nccl_waits_for_each_layer():
+    """ShardedStep's ready-driven schedule (begin / layer_ready / end) over
+    a one-rank NCCL group.  The gradient slab starts with every tensor NaN;
+    a stand-in backward on the caller's stream restores each layer's
+    gradients, from the last layer down, after a ~50 us spin, and reports
+    the layer.  A bucket's update ordered before its layer's gradients would
+    read NaN: two steps must equal the oracle's, bit for bit."""
+    import torch.distributed as dist
+    from gradient_reduce_optimizer_gb300.dist import ShardedStep
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                            world_size=1)
+    try:
+        t = wl.bert_large_tensors(layers=2, hidden=64, ffn=256, vocab=101, positions=16)
+        numel, layer_of = [x[1] for x in t], [x[2] for x in t]
+        step = ShardedStep(numel, 4096, rank=0, world=1, device=DEV, layer_of=layer_of)
+        n = step.n_slab
+        grads, master, m, v = seeded(n, 1, seed=71)
+        real = grads[0]
+        params = torch.full((n,), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        st = [master.clone(), m.clone(), v.clone()]
+        ref = new_slabs(grads, master, m, v)
+        h_grads, h_state, _ = host_copy(ref)
+        stream = torch.cuda.current_stream()
+        for k in range(2):
+            hp = dict(HP, step=HP["step"] + k)
+            g = real.clone()
+            for off, cnt in zip(step.offsets, numel):
+                g[off:off + cnt] = float("nan")
+            step.begin(g, *st, params, stream=stream, **hp)
+            went = 0
+            for layer in range(max(layer_of), -1, -1):
+                torch.cuda._sleep(100_000)       # a slow layer of the backward
+                for ti, (off, cnt) in enumerate(zip(step.offsets, numel)):
+                    if layer_of[ti] == layer:
+                        g[off:off + cnt].copy_(real[off:off + cnt])
+                went += step.layer_ready(layer)
+            assert went == len(step.buckets)
+            step.end()
+            ref_outs = oracle_step(h_grads, h_state, hp)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(u16(params), ref_outs[0])
+        for got, want in zip(st, h_state):
+            np.testing.assert_array_equal(got.cpu().numpy().view(np.uint32),
+                                          want.view(np.uint32))
+    finally:
+        dist.destroy_process_group()
