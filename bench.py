@@ -538,7 +538,8 @@ def run_dist(args):
     capi.lib()
     w = wl.bert_large_r8(bucket_bytes=args.bucket_mib * wl.MiB)
     numel, layer_of = w.numel(), w.layer_of()
-    step = ShardedStep(numel, w.bucket_bytes, rank=rank, world=world, device=dev)
+    step = ShardedStep(numel, w.bucket_bytes, rank=rank, world=world, device=dev,
+                       layer_of=layer_of)
     n_slab = step.n_slab
     lay = wl.element_layer_map(numel, layer_of, step.offsets, n_slab, device=dev)
     per_layer = wl.layer_scales(max(layer_of) + 1, *w.layer_scale, device=dev)
@@ -601,8 +602,88 @@ def run_dist(args):
         "clocks": clk,
         "gpu_launches": len(step.buckets) * args.steps,
     }
+    if not args.no_overlap:
+        result["overlap_ready_driven"] = run_dist_overlap(args, step, grads, st, params, w,
+                                                          layer_of, world, dev)
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def run_dist_overlap(args, step, grads, st, params, w, layer_of, world, dev):
+    """The real multi-GPU form behind a proxy backward (the model's compute:
+    per layer 3 bf16 GEMMs, M=8192, N=K=1024, as in cc_overlap_bench), in
+    the two schedules: every bucket after the backward (step()), and DDP's
+    ready-driven one (begin / layer_ready / end: each bucket's exchanges go
+    out as soon as the backward has produced it).  Exposed = T_step - T_bwd,
+    slowest rank, median over iterations."""
+    import torch
+
+    L = max(layer_of) + 1
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    a = torch.randn(8192, 1024, generator=g, device=dev).to(torch.bfloat16)
+    bs = [torch.randn(1024, 1024, generator=g, device=dev).to(torch.bfloat16)
+          for _ in range(3)]
+    c = torch.empty(8192, 1024, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    # one layer's GEMMs captured once and replayed: the proxy runs at the
+    # GPU's pace, not at the pace Python issues three launches
+    for b_ in bs:
+        torch.matmul(a, b_, out=c)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for b_ in bs:
+            torch.matmul(a, b_, out=c)
+    torch.cuda.synchronize()
+
+    def layer(l):
+        graph.replay()
+
+    def backward():
+        for l in range(L - 1, -1, -1):
+            layer(l)
+
+    def after(i):
+        backward()
+        step.step(grads, *st, params, stream=stream, **step_args({"w": w}, w.step + i))
+
+    def ready(i):
+        step.begin(grads, *st, params, stream=stream, **step_args({"w": w}, w.step + i))
+        for l in range(L - 1, -1, -1):
+            layer(l)
+            step.layer_ready(l)
+        step.end()
+
+    iters = max(3, min(args.overlap_iters, 20))
+
+    def med_ms(fn):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        times = []
+        for i in range(iters):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(3 + i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        barrier(world)
+        return reduce_scalar(statistics.median(times), world, "max", device=dev)
+
+    t_bwd = med_ms(lambda i: backward())
+    t_after = med_ms(after)
+    t_ready = med_ms(ready)
+    return {"layers": L, "gemm": "3 per layer, 8192 x 1024 x 1024 bf16 (torch.matmul, one "
+                                  "CUDA graph per layer)",
+            "buckets": len(step.buckets), "iters": iters,
+            "t_bwd_ms": round(t_bwd, 4), "t_step_after_backward_ms": round(t_after, 4),
+            "t_step_ready_driven_ms": round(t_ready, 4),
+            "exposed_after_backward_ms": round(t_after - t_bwd, 4),
+            "exposed_ready_driven_ms": round(t_ready - t_bwd, 4)}
     return result
 
 
