@@ -168,6 +168,8 @@ class ShardedStep:
         """One optimizer step: every bucket's ReduceScatter, update and
         AllGather.  Returns once everything is queued; the parameters are
         complete when the stream (and the backend's) reach this point."""
+        if self._run is not None:
+            raise RuntimeError("step() while a ready-driven step is open: end() it first")
         hp = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay,
                   step=step, grad_scale=grad_scale)
         B = len(self.buckets)
@@ -265,8 +267,10 @@ class ShardedStep:
 
     def end(self) -> None:
         """Close the step: every bucket must have gone out (layer_ready(0)
-        was called).  The caller's stream waits for the last AllGather, so
-        the parameters are complete when it reaches this point."""
+        was called); if not, this raises and the step stays open, to be
+        closed once the remaining layers are reported.  The caller's stream
+        waits for the last AllGather, so the parameters are complete when it
+        reaches this point."""
         run = self._run
         if run is None:
             raise RuntimeError("end() without begin()")

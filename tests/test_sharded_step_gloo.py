@@ -240,6 +240,8 @@ def test_ready_driven_schedule_issues_each_bucket_once_its_layer_is_done():
     step.begin(g, *st, params, **HP)
     with pytest.raises(RuntimeError):
         step.begin(g, *st, params, **HP)         # already open
+    with pytest.raises(RuntimeError):
+        step.step(g, *st, params, **HP)          # the other schedule while one is open
     issued = 0
     for layer in range(max(layer_of), -1, -1):
         issued += step.layer_ready(layer)
