@@ -179,3 +179,26 @@ def test_ready_driven_schedule_over_nccl_waits_for_each_layer():
                                           want.view(np.uint32))
     finally:
         dist.destroy_process_group()
+
+
+def test_bench_real_form_runs_at_world_one():
+    """bench.py's real multi-GPU form (the line a torchrun launch prints),
+    forced at one rank with --dist: the step after the backward and the
+    ready-driven schedule behind the proxy backward both run and report."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--dist", "--steps", "3",
+                        "--warmup", "3", "--overlap-iters", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 1 and d["config"]["parallelism"].startswith("dp1")
+    assert d["value"] > 0 and d["gpu_launches"] == 3 * d["config"]["num_buckets"]
+    o = d["overlap_ready_driven"]
+    assert o["buckets"] == d["config"]["num_buckets"]
+    assert o["t_bwd_ms"] > 0 and o["t_step_ready_driven_ms"] > 0
+    assert o["t_step_after_backward_ms"] > o["t_bwd_ms"]
