@@ -142,12 +142,12 @@ def test_outputs_are_the_rank_order_allreduce_of_the_partials(R, m, n, k, schedu
 
 
 @pytest.mark.parametrize("schedule", ["whole", "split"])
-@pytest.mark.parametrize("m", [2048, 8192])
+@pytest.mark.parametrize("m", [2048, 8192, 16384])
 def test_gpt2_mlp_shape_sampled(m, schedule):
     """The measured shape (R=8, n=3072, k=12288; m=8192 runs 256-column tiles
-    with a split last wave, m=2048 192-column tiles): integer operands, so
-    every output is exact; checked on sampled rows against float64 (the last
-    row tiles are the split wave's)."""
+    with a split last wave of 4 groups, m=16384 one of 8 groups, m=2048
+    192-column tiles): integer operands, so every output is exact; checked on
+    sampled rows against float64 (the last row tiles are the split wave's)."""
     R, n, k = 8, 3072, 12288
     x, w = operands(R, m, n, k, seed=5, integer=True)
     outs, _ = run(x, w, m, n, k, R, with_partials=False, schedule=schedule)
