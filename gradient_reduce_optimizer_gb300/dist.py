@@ -152,6 +152,7 @@ class ShardedStep:
                                     dtype=dtype or torch.bfloat16, device=device)
                         for _ in range(2)]
         self._run = None
+        self._side_streams = {}
 
     def shard_state_ranges(self) -> List[Tuple[Range, Range]]:
         """(slab range, state range) of each of this rank's shards."""
@@ -210,7 +211,8 @@ class ShardedStep:
         """Start a step whose buckets go out as the backward produces them.
         stream: the caller's (the backward's) stream, default the current
         one; side_stream: where the buckets' exchanges and updates are
-        ordered (CUDA tensors only; default a new stream)."""
+        ordered (CUDA tensors only; default one stream of this object's,
+        made on first use)."""
         import torch
 
         if self.ready is None:
@@ -220,7 +222,13 @@ class ShardedStep:
         cuda = grads.is_cuda
         if cuda:
             stream = stream or torch.cuda.current_stream(grads.device)
-            side_stream = side_stream or torch.cuda.Stream(device=grads.device)
+            if side_stream is None:
+                # one side stream per device, made once and reused by every step
+                own = self._side_streams.get(grads.device)
+                if own is None:
+                    own = self._side_streams[grads.device] = torch.cuda.Stream(
+                        device=grads.device)
+                side_stream = own
         self._run = dict(grads=grads, state=(master, m, v), params=params, next=0,
                          gathers=[], stream=stream, side=side_stream, cuda=cuda,
                          hp=dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps,
